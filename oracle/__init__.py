@@ -1,0 +1,160 @@
+"""CPU oracle for paged decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the package's ``smoke()`` check and the benchmark's CPU
+baseline may import this package.  The product path (the CUDA library and its
+Python binding) never imports, links or runs anything here, and nothing here
+imports the product.
+
+Contents:
+  * ``pa_oracle.c`` -- fp64 C implementation of reshape_and_cache,
+    copy_blocks, paged attention and the partition-then-merge variant, loaded
+    through ctypes (built with gcc on first use, or by ``build()``).
+  * ``brute.py`` -- an independent NumPy brute force for tiny inputs.
+  * ``accounting.py`` -- the pages' block-count and KV-size formulas.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_lib = None
+
+DTYPE_CODE = {"f16": 0, "bf16": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (-O2 -fopenmp, no fast-math)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16, i32]
+        lib.oracle_half_to_double.restype = dbl
+        lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, P, i64, i64, i32, i32, i32]
+        lib.oracle_reshape_and_cache.restype = i64
+        lib.oracle_copy_blocks.argtypes = [P, P, P, i64, i64, i32, i32, i32]
+        lib.oracle_copy_blocks.restype = i64
+        lib.oracle_paged_attention.argtypes = [P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, dbl]
+        lib.oracle_paged_attention.restype = None
+        lib.oracle_paged_attention_partitioned.argtypes = [P, P, P, P, P, P, P, i32, P, i32, P,
+                                                           i32, i32, i32, i32, i32, dbl, i32, i32]
+        lib.oracle_paged_attention_partitioned.restype = None
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def half_to_double(bits, dtype: str) -> np.ndarray:
+    """Exact value of each 16-bit pattern (elementwise, slow, for pinning)."""
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint16).reshape(-1)
+    out = np.array([lib.oracle_half_to_double(int(b), DTYPE_CODE[dtype]) for b in flat])
+    return out.reshape(np.shape(bits))
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping):
+    """Scatter the step's K/V rows into (copies of) the caches.
+
+    Returns (k_cache_after, v_cache_after, number_of_out_of_range_slots)."""
+    lib = _load()
+    kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    nb, bs, hkv, d = kc.shape
+    bad = lib.oracle_reshape_and_cache(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc), _ptr(sm),
+                                       len(sm), nb, bs, hkv, d)
+    return kc, vc, int(bad)
+
+
+def copy_blocks(k_cache, v_cache, block_mapping):
+    """Copy whole blocks pair by pair (copy-on-write) on copies of the caches."""
+    lib = _load()
+    kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    bm = _c(np.asarray(block_mapping).reshape(-1, 2), np.int64)
+    nb, bs, hkv, d = kc.shape
+    bad = lib.oracle_copy_blocks(_ptr(kc), _ptr(vc), _ptr(bm), len(bm), nb, bs, hkv, d)
+    return kc, vc, int(bad)
+
+
+def paged_attention(q, k_cache, v_cache, dtype: str, block_tables, context_lens, scale,
+                    num_kv_heads: int | None = None) -> np.ndarray:
+    """softmax(q K^T * scale) V over each sequence's paged context, in fp64.
+
+    q: uint16 [B, Hq, D]; caches: uint16 [NB, bs, Hkv, D]; block_tables: int32
+    [B, maxNB]; context_lens: int32 [B].  Returns float64 [B, Hq, D]."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, bs, hkv, d2 = kc.shape
+    assert d2 == D and (num_kv_heads is None or num_kv_heads == hkv)
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    lib.oracle_paged_attention(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), DTYPE_CODE[dtype],
+                               _ptr(bt), bt.shape[1], _ptr(cl), B, Hq, hkv, D, bs, float(scale))
+    return out
+
+
+def paged_attention_partitioned(q, k_cache, v_cache, dtype: str, block_tables, context_lens,
+                                scale, partition_size: int):
+    """Partition-then-merge attention.  Returns (out, part_max, part_sum, part_acc)."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, bs, hkv, _ = kc.shape
+    maxp = max(1, -(-int(cl.max(initial=0)) // int(partition_size)))
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    pm = np.empty((B, Hq, maxp), dtype=np.float64)
+    ps = np.empty((B, Hq, maxp), dtype=np.float64)
+    pa = np.empty((B, Hq, maxp, D), dtype=np.float64)
+    lib.oracle_paged_attention_partitioned(_ptr(out), _ptr(pm), _ptr(ps), _ptr(pa), _ptr(q), _ptr(kc),
+                                           _ptr(vc), DTYPE_CODE[dtype], _ptr(bt), bt.shape[1], _ptr(cl),
+                                           B, Hq, hkv, D, bs, float(scale), int(partition_size), maxp)
+    return out, pm, ps, pa
+
+
+def decode_step(batch):
+    """The whole step on the CPU: copy_blocks, reshape_and_cache, attention.
+
+    ``batch`` is a workloads.Batch.  Returns (out fp64 [B,Hq,D], k_cache_after,
+    v_cache_after)."""
+    kc, vc = batch.k_cache, batch.v_cache
+    if len(batch.block_mapping):
+        kc, vc, _ = copy_blocks(kc, vc, batch.block_mapping)
+    kc, vc, _ = reshape_and_cache(batch.key, batch.value, kc, vc, batch.slot_mapping)
+    out = paged_attention(batch.q, kc, vc, batch.dtype, batch.block_tables, batch.context_lens,
+                          batch.scale)
+    return out, kc, vc
