@@ -1,0 +1,505 @@
+#!/usr/bin/env python
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path over one batch: copy_blocks (copy-on-write
+pairs, if the workload has any), reshape_and_cache of the step's new K/V
+rows, and paged decode attention over every sequence's context - all through
+the C ABI of libpagedattn.so.  The default workload is the LLaMA-13B-shaped
+layer: 256 sequences, 40 heads x 128 dims, block_size 16, long-tailed
+context lengths (lognormal, median 300, clipped to [1, 2048]), bf16.
+
+Metric: KV-read HBM GB/s (and us/step).  One JSON line is printed by rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (fp64 C, all host cores) on a
+bounded sample of the same workload.  Under torchrun (N > 1) every rank runs
+its own replica batch (weak scaling, no collective on the data path);
+``value`` is the KV bytes of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD_TEXT = {
+    "13b": "LLaMA-13B-shaped decode step, one layer: 256 seqs, 40 heads (MHA), head_dim 128, block_size 16, "
+           "context lognormal(median 300, sigma 1) clipped to [1,2048], bf16, reshape_and_cache of each "
+           "sequence's new token via a random slot_mapping",
+    "7b": "LLaMA-7B-shaped decode step, one layer: 64 seqs, 32 heads (MHA), head_dim 128, block_size 16, "
+          "context uniform [32,2048], f16",
+    "gqa": "GQA long-context decode: 16 seqs, 32 q / 8 kv heads, head_dim 128, block_size 16, context "
+           "uniform [16384,32768], 512-token partitions, bf16",
+    "gqa32": "GQA long-context decode: 16 seqs, 32 q / 8 kv heads, head_dim 128, block_size 32, context "
+             "uniform [16384,32768], 512-token partitions, bf16",
+    "prefix": "prefix-sharing decode: 64 prompts x 4 samples sharing a 1000-token prompt, private 0-256 "
+              "token suffix, copy-on-write of the shared partial block, 32 heads, head_dim 128, f16",
+    "tiny": "tiny paged decode: 4 seqs, context {1,17,35,100}, 4 heads, head_dim 64, block_size 16, f16",
+}
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+# --------------------------------------------------------------- accounting
+
+def kv_bytes(b) -> int:
+    """Bytes of K and V a decode step reads: sum_s ctx_s * Hkv * D * 2 (K,V) * 2 B."""
+    return int(b.context_lens.astype("int64").sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+
+
+def decode_bytes(b, partition: int) -> int:
+    """Algorithmic bytes of one pa_decode launch: KV rows, queries, outputs,
+    block-table entries, context lengths and the split-K partial states
+    (written once, read once by the merge)."""
+    import numpy as np
+    ctx = b.context_lens.astype(np.int64)
+    G = b.num_heads // b.num_kv_heads
+    q = b.num_seqs * b.num_heads * b.head_dim * 2
+    out = b.num_seqs * b.num_heads * b.head_dim * 2
+    tables = int(np.ceil(ctx / b.block_size).sum()) * 4 * b.num_kv_heads
+    nparts = np.where(ctx > 0, -(-ctx // partition), 1)
+    split = int(nparts[nparts > 1].sum()) * b.num_kv_heads * G * (b.head_dim + 2) * 4 * 2
+    return kv_bytes(b) + q + out + tables + b.num_seqs * 4 + split
+
+
+def step_bytes(b, partition: int) -> int:
+    rows = len(b.slot_mapping) * b.num_kv_heads * b.head_dim * 2 * 2 * 2  # K,V read + write
+    copies = len(b.block_mapping) * b.block_size * b.num_kv_heads * b.head_dim * 2 * 2 * 2
+    return decode_bytes(b, partition) + rows + copies
+
+
+def hbm_peak():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def aggregate(ms_per_step: float, units: float, world: int):
+    """Slowest rank's time and the units all ranks processed."""
+    if world <= 1:
+        return ms_per_step, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+CLOCK_QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling (every 200 ms) around the timed region."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        if self.uuid:
+            mine = [r for r in rows if len(r) > 1 and r[1].strip() == self.uuid]
+            rows = mine or rows
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                mx.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(REASONS, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def device_tensors(b, device):
+    import numpy as np
+    import torch
+    tdt = torch.float16 if b.dtype == "f16" else torch.bfloat16
+
+    def h(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt)
+
+    host = dict(q=h(b.q), key=h(b.key), value=h(b.value),
+                slot_mapping=torch.from_numpy(b.slot_mapping), block_tables=torch.from_numpy(b.block_tables),
+                context_lens=torch.from_numpy(b.context_lens),
+                block_mapping=torch.from_numpy(np.ascontiguousarray(b.block_mapping)))
+    dev = {k: v.to(device) for k, v in host.items()}
+    dev["k_cache"] = h(b.k_cache).to(device)
+    dev["v_cache"] = h(b.v_cache).to(device)
+    return host, dev
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_140_gb300 as pa
+    from paged_kv_cache_140_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist_init("nccl")
+    pa._lib.load()  # fail loudly before any work if the library is missing
+
+    cfg = W.CONFIGS[args.workload]
+    seed = 140000 + cfg["number"] + 1000 * rank
+    b = W.make_batch(args.workload, seed=seed)
+    host, T = device_tensors(b, device)
+    out = torch.empty(T["q"].shape, dtype=T["q"].dtype, device=device)
+    P = pa.decode_partition_size(b.num_seqs, b.num_heads, b.num_kv_heads, b.head_dim, b.block_size,
+                                 b.max_context_len, b.partition_size)
+    ws = pa.DecodeWorkspace(device)
+    has_pairs = len(b.block_mapping) > 0
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if has_pairs:
+            pa.copy_blocks(T["k_cache"], T["v_cache"], T["block_mapping"])
+        pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"])
+        if ev is not None:
+            ev[0].record(stream)
+        pa.decode(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"],
+                  float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
+                  workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    err = pa.new_err_flag(device)
+    pa.decode(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"],
+              float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
+              workspace=ws, err_flag=err)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    flag = pa.read_err_flag(err)
+    if flag:
+        raise SystemExit(f"device error flag {flag:#x} during warm-up")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    if args.clock_probe_s > 0:  # keep the GPU busy long enough for the sampler
+        t_end = time.time() + args.clock_probe_s
+        while time.time() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for k in range(K):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_step = ms_total / K
+    decode_ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
+
+    # End to end: pinned host inputs -> device, the step, result -> pinned host.
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for k, v in pinned.items() if k != "block_mapping" or has_pairs)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for k, v in pinned.items():
+            if k == "block_mapping" and not has_pairs:
+                continue
+            e2e_in[k].copy_(v, non_blocking=True)
+        if has_pairs:
+            pa.copy_blocks(T["k_cache"], T["v_cache"], e2e_in["block_mapping"])
+        pa.reshape_and_cache(e2e_in["key"], e2e_in["value"], T["k_cache"], T["v_cache"], e2e_in["slot_mapping"])
+        pa.decode(out, e2e_in["q"], T["k_cache"], T["v_cache"], e2e_in["block_tables"], e2e_in["context_lens"],
+                  float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
+                  workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    barrier(world)
+    w0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - w0) * 1e3 / K
+    barrier(world)
+
+    kvb = kv_bytes(b)
+    ms_max, kv_all = aggregate(ms_step, float(kvb), world)
+    e2e_max, _ = aggregate(e2e_ms, float(kvb), world)
+    dec_max, _ = aggregate(decode_ms, 0.0, world)
+    peak, peak_kind = hbm_peak()
+    value = kv_all / (ms_max * 1e-3) / 1e9
+    dbytes = decode_bytes(b, P)
+    achieved = dbytes / (decode_ms * 1e-3) / 1e9
+    traffic = load_traffic(args.workload)
+
+    line = {
+        "metric": "paged decode attention: KV-read HBM GB/s (% of GB300 peak), us/step",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5),
+        "us_per_step": round(ms_max * 1e3, 2),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 1),
+        "peak_kind": peak_kind,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": b.dtype,
+        "data": "synthetic (seeded N(0,1) K/V/Q, seeded block permutation, NaN in unused slots)",
+        "impl": "ours",
+        "config": {
+            "workload": WORKLOAD_TEXT.get(args.workload, args.workload),
+            "name": args.workload,
+            "num_seqs": b.num_seqs, "num_heads": b.num_heads, "num_kv_heads": b.num_kv_heads,
+            "head_dim": b.head_dim, "block_size": b.block_size, "num_blocks": b.num_blocks,
+            "tokens": int(b.context_lens.sum()), "max_context_len": b.max_context_len,
+            "partition_size": P, "kv_bytes_per_step": kvb, "step_bytes": step_bytes(b, P),
+            "seqs_tokens_per_s": round(float(b.context_lens.sum()) * world / (ms_max * 1e-3), 1),
+            "l2": "no flush: each step reads %.2f GB of K/V, far larger than the 126 MB L2" % (kvb / 1e9),
+            "parallelism": f"replicas x{world} (independent batches per GPU)",
+        },
+        "roofline": {
+            "kernel": "paged_decode_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": dbytes,
+            "launch_us": round(decode_ms * 1e3, 2),
+        },
+        "e2e": {"value": round(kv_all / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+                "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens -> device, "
+                        "the step, output -> pinned host, stream sync; the KV cache stays resident"},
+        "gpu_launches": K * (2 + (1 if has_pairs else 0)),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def load_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def _oracle_threads() -> int:
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    os.environ.setdefault("OMP_NUM_THREADS", str(n))
+    return int(os.environ["OMP_NUM_THREADS"])
+
+
+def _post_step_caches(b):
+    import oracle
+    kc, vc = b.k_cache, b.v_cache
+    if len(b.block_mapping):
+        kc, vc, _ = oracle.copy_blocks(kc, vc, b.block_mapping)
+    kc, vc, _ = oracle.reshape_and_cache(b.key, b.value, kc, vc, b.slot_mapping)
+    return kc, vc
+
+
+def _pick_sample(b, target_s, kc, vc):
+    """Sequences (every k-th) whose oracle attention takes about target_s."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_140_gb300 import workloads as W
+    probe = list(range(0, b.num_seqs, max(1, b.num_seqs // 8)))[:8]
+    sub = W.subset_batch(b, probe)
+    t = time.perf_counter()
+    oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
+    dt = max(time.perf_counter() - t, 1e-4)
+    per_tok = dt / max(1, int(sub.context_lens.sum()))
+    want_tok = target_s / per_tok
+    order = np.arange(b.num_seqs)
+    total = int(b.context_lens.sum())
+    if want_tok >= total:
+        return list(order)
+    stride = max(1, int(round(total / want_tok)))
+    return list(order[::stride])
+
+
+def cpu_baseline(b, target_s):
+    threads = _oracle_threads()
+    import oracle
+    from paged_kv_cache_140_gb300 import workloads as W
+    kc, vc = _post_step_caches(b)
+    pick = _pick_sample(b, target_s, kc, vc)
+    sub = W.subset_batch(b, pick)
+    t = time.perf_counter()
+    oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
+    dt = time.perf_counter() - t
+    sb = kv_bytes(sub)
+    return {"value": round(sb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"attention of {len(pick)} of {b.num_seqs} sequences (every "
+                      f"{max(1, b.num_seqs // max(1, len(pick)))}th; {int(sub.context_lens.sum())} tokens, "
+                      f"{sb} KV bytes) over the post-step caches; fp64 C oracle, OpenMP over (seq, head)"}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    threads = _oracle_threads()
+    import oracle
+    from paged_kv_cache_140_gb300 import workloads as W
+    b = W.make_batch(args.workload)
+    kc, vc = _post_step_caches(b)
+    per_step_s = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    pick = _pick_sample(b, per_step_s, kc, vc)
+    sub = W.subset_batch(b, pick)
+
+    def one():
+        oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
+
+    for _ in range(args.warmup):
+        one()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t) / args.steps
+    sb = kv_bytes(sub)
+    value = sb / dt / 1e9
+    line = {
+        "metric": "paged decode attention: KV-read HBM GB/s (% of GB300 peak), us/step",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": b.dtype, "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload), "name": args.workload,
+                   "sample_seqs": len(pick), "sample_tokens": int(sub.context_lens.sum())},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"attention of {len(pick)} of {b.num_seqs} sequences per step "
+                                   f"({int(sub.context_lens.sum())} tokens, {sb} KV bytes)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="13b", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--clock-probe-s", type=float, default=2.0,
+                    help="seconds of steps run under the clock sampler before the timed region")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged decode-attention library.
+ *
+ * The library implements the data-parallel hot path of PagedAttention decode:
+ * every running sequence's single new query token attends over a KV cache
+ * that is split into fixed-size physical blocks reached through a per-sequence
+ * block table.
+ *
+ *   Page A = "LLM推理优化：vLLM PagedAttention深度解析与工程实践"
+ *   Page B = "vLLM 核心：PagedAttention 与 Continuous Batching"
+ *   Page C = nano-vllm walkthrough, lqnn.cn/news/170268
+ *   Page D = "优化大模型推理：PagedAttention 如何实现 GPU 显存高效管理"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All pointers except scalars are DEVICE pointers on the current CUDA
+ *    device.  All tensors are dense, row-major (C order) and start on a 16-byte
+ *    boundary.  The caller owns every buffer, the decode workspace included;
+ *    the library allocates no memory.
+ *  - KV cache layout (one layer, K and V in separate tensors):
+ *        k_cache, v_cache : [num_blocks, block_size, num_kv_heads, head_dim]
+ *    (Page A §4.1; Page C §2.2 gives the per-model form
+ *    [layers, 2, blocks, block_size, heads, head_dim], of which these are
+ *    one layer's K and V slices.)
+ *  - A cache slot is  slot = physical_block * block_size + offset_in_block.
+ *  - Element types: PA_F16 (IEEE binary16) or PA_BF16 for q/K/V; the decode
+ *    output may also be PA_F32.  Arithmetic is fp32 (Page C §6: accumulating
+ *    QK^T in half precision overflowed on long sequences).
+ *  - Supported shapes: head_dim 64 or 128; block_size 8 or a multiple of 16
+ *    up to 256; num_heads a multiple of num_kv_heads with
+ *    num_heads / num_kv_heads in {1, 2, 4, 8}.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work and returns; host-side argument
+ *    checks are synchronous and enqueue nothing when they fail.
+ *  - `err_flag` (nullable, device int) collects problems found on the device.
+ *    Kernels never trap and never spin without bound: a bad index is skipped
+ *    and reported by atomically OR-ing a PA_FLAG_* bit into *err_flag.  The
+ *    caller reads it after synchronising; any non-zero value means the
+ *    affected outputs are not to be trusted (PA_ERR_DEVICE_BOUNDS).
+ *  - Calls are not re-entrant on the same workspace: two pa_decode calls that
+ *    may overlap on the GPU need two workspaces.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned pointer */
+    PA_ERR_UNSUPPORTED = 2,    /* valid request outside the supported shapes */
+    PA_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+    PA_ERR_WORKSPACE = 4,      /* decode workspace missing or too small */
+    PA_ERR_DEVICE_BOUNDS = 5   /* returned by pa_check_err_flag for a non-zero flag */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define PA_FLAG_BAD_SLOT        0x1   /* slot_mapping entry >= num_blocks * block_size */
+#define PA_FLAG_BAD_BLOCK_ID    0x2   /* block table entry outside [0, num_blocks) */
+#define PA_FLAG_BAD_CONTEXT_LEN 0x4   /* context length < 0 or beyond the table/bound */
+#define PA_FLAG_BAD_COPY_PAIR   0x8   /* copy pair id outside [0, num_blocks) */
+#define PA_FLAG_TIMEOUT         0x10  /* a bounded wait on an async copy gave up */
+
+/*
+ * pa_reshape_and_cache -- write this step's new K/V rows into their slots.
+ *
+ * Defined by Page C §2.2 (a new token goes into the current physical block
+ * while it has room, else a new block is taken and the table extended) and
+ * §2.3 step 3 (write back and update the block's token count); Page A §二
+ * (each step appends the new token's K and V to the cache).
+ *
+ *   key, value   : [num_tokens, num_kv_heads, head_dim], dtype
+ *   k_cache/v_cache : [num_blocks, block_size, num_kv_heads, head_dim], dtype
+ *   slot_mapping : [num_tokens] int64.  For token t with slot >= 0:
+ *                    k_cache[slot / bs][slot % bs][h][:] = key[t][h][:]
+ *                    v_cache[slot / bs][slot % bs][h][:] = value[t][h][:]
+ *                  slot < 0 means "no write" (padding token).
+ * The copy is bit-exact.  Slots must be distinct (else the surviving row is
+ * unspecified).  slot >= num_blocks * block_size: skipped, PA_FLAG_BAD_SLOT.
+ * num_tokens == 0 is a no-op.
+ */
+pa_status pa_reshape_and_cache(const void *key, const void *value,
+                               void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping, int64_t num_tokens,
+                               int64_t num_blocks, int block_size,
+                               int num_kv_heads, int head_dim, pa_dtype dtype,
+                               int *err_flag, void *stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of workspace pa_decode needs.
+ *
+ * Returns 0 when no sequence can be split (max_context_len fits in one
+ * partition).  The workspace holds per-partition partial results (running
+ * max, sum of exponentials, unnormalised weighted V sum, fp32) and one
+ * completion counter per (sequence, KV head).  It must be ZERO-FILLED before
+ * its first use (pa_decode_workspace_init does that); every pa_decode that
+ * completes leaves the counters at zero again, so later calls need no reset.
+ * `partition_size` is the same value later passed to pa_decode (0 = auto).
+ * Returns (size_t)-1 for arguments pa_decode would reject.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size, int max_context_len,
+                                int partition_size);
+
+/* Zero-fill a decode workspace (stream-ordered memset). */
+pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/* The partition length, in tokens, pa_decode uses for these arguments. */
+int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads,
+                             int head_dim, int block_size, int max_context_len,
+                             int partition_size);
+
+/*
+ * pa_decode -- paged decode attention for one query token per sequence.
+ *
+ * For sequence s and query head h, with G = num_heads / num_kv_heads and the
+ * KV head kvh = h / G (consecutive grouping; Page D's size formula counts
+ * H_kv KV heads):
+ *     x_p   = scale * <query[s][h][:], K_p>,  p = 0 .. context_lens[s]-1
+ *     K_p   = k_cache[block_tables[s][p / bs]][p % bs][kvh][:]   (V_p alike)
+ *     out[s][h][:] = sum_p softmax(x)_p * V_p
+ * i.e. softmax(q K^T * scale) V (Page A §二) over the sequence's logical
+ * context, gathered through its block table (Page A §3.1, §4.1; Page B §3;
+ * Page C §2.3 steps 1-2).  Slots at positions >= context_lens[s] are never
+ * read, so stale data there cannot leak in (Page C §6).
+ *
+ * Long contexts are cut into partitions of `partition_size` tokens (0 = auto)
+ * whose partial results (max, sum, weighted V sum) are merged in partition
+ * order -- the "partial accumulate, then merge" kernel of Page A §4.1.  The
+ * result does not depend on the physical block ids or on the GPU schedule
+ * and is bitwise reproducible run to run for a given partition size.
+ *
+ *   out          : [num_seqs, num_heads, head_dim], out_dtype (F16/BF16/F32)
+ *   query        : [num_seqs, num_heads, head_dim], kv_dtype
+ *   k_cache/v_cache : [num_blocks, block_size, num_kv_heads, head_dim], kv_dtype
+ *   block_tables : [num_seqs, max_blocks_per_seq] int32; only the first
+ *                  ceil(context_lens[s] / bs) entries of row s are read
+ *   context_lens : [num_seqs] int32, each in [0, max_context_len]; 0 gives a
+ *                  zero output row
+ *   max_context_len : host-known upper bound of context_lens (sizes the
+ *                  workspace); must be <= max_blocks_per_seq * block_size
+ *   scale        : softmax scale, usually 1/sqrt(head_dim)
+ *   partition_size : 0 (auto) or a multiple of 16 tokens, at most
+ *                  32 * block_size
+ *   workspace    : device buffer of pa_decode_workspace_size(...) bytes,
+ *                  zero-filled before first use (may be NULL if that size is 0)
+ * Device-side problems: a block id outside [0, num_blocks) is not read, its
+ * tokens are left out of the softmax and PA_FLAG_BAD_BLOCK_ID is set; a
+ * context length outside [0, max_context_len] gives a zero row and
+ * PA_FLAG_BAD_CONTEXT_LEN.
+ */
+pa_status pa_decode(void *out, pa_dtype out_dtype,
+                    const void *query,
+                    const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int max_context_len,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, int64_t num_blocks, float scale,
+                    int partition_size,
+                    void *workspace, size_t workspace_bytes,
+                    int *err_flag, void *stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write of shared blocks.
+ *
+ * A block referenced by several sequences is read-only; before one of them
+ * writes into it, the block is copied to a fresh one (Page D, copy-on-write
+ * section: parallel sampling of one prompt; Page A §3.1; Page B §3 prefix
+ * sharing).  For every pair p:
+ *     k_cache[dst_p] = k_cache[src_p],  v_cache[dst_p] = v_cache[src_p]
+ * (whole blocks: block_size * num_kv_heads * head_dim elements each), bit-exact.
+ *
+ *   block_mapping : [num_pairs, 2] int64 (src, dst), device memory
+ * Destinations must be distinct and no destination may also be a source
+ * (else the result depends on order and is unspecified).  A pair with an id
+ * outside [0, num_blocks) is skipped and sets PA_FLAG_BAD_COPY_PAIR.
+ * num_pairs == 0 is a no-op.
+ */
+pa_status pa_copy_blocks(void *k_cache, void *v_cache,
+                         const int64_t *block_mapping, int64_t num_pairs,
+                         int64_t num_blocks, int block_size, int num_kv_heads,
+                         int head_dim, pa_dtype dtype, int *err_flag, void *stream);
+
+/* Host helper: synchronously read *err_flag (device), optionally clear it,
+ * and map it to PA_OK / PA_ERR_DEVICE_BOUNDS.  `flag_out` (nullable, host)
+ * receives the raw bits. */
+pa_status pa_check_err_flag(int *err_flag, int clear, int *flag_out, void *stream);
+
+/* A short, static description of a status code. */
+const char *pa_status_string(pa_status status);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

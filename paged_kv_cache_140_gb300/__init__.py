@@ -1,0 +1,193 @@
+"""GB300-native (sm_103a) paged decode attention.
+
+The computation lives in the CUDA library ``lib/libpagedattn.so`` behind the
+C ABI of ``include/pa.h``.  This module only marshals PyTorch tensors (device
+memory and the current CUDA stream) into those calls; there is no CPU or
+PyTorch fallback - a missing library raises.
+
+    reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)
+    decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, ...)
+    copy_blocks(k_cache, v_cache, block_mapping)
+
+Cache layout: ``[num_blocks, block_size, num_kv_heads, head_dim]`` per layer
+for K and for V ("LLM推理优化：vLLM PagedAttention深度解析与工程实践", §4.1).
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import (FLAG_BAD_BLOCK_ID, FLAG_BAD_CONTEXT_LEN, FLAG_BAD_COPY_PAIR, FLAG_BAD_SLOT,
+                   FLAG_TIMEOUT, PA_BF16, PA_F16, PA_F32, PagedAttentionError)
+
+__all__ = ["reshape_and_cache", "decode", "copy_blocks", "decode_workspace_size",
+           "decode_partition_size", "DecodeWorkspace", "new_err_flag", "read_err_flag",
+           "PagedAttentionError", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK_ID", "FLAG_BAD_CONTEXT_LEN",
+           "FLAG_BAD_COPY_PAIR", "FLAG_TIMEOUT", "library_path"]
+
+
+def library_path() -> str:
+    return _lib.lib_path()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t, allow_f32=False) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    if allow_f32 and t.dtype == torch.float32:
+        return PA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(name, t):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _stream(device) -> ctypes.c_void_p:
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def new_err_flag(device=None):
+    """A zeroed device int32 that kernels OR their PA_FLAG_* bits into."""
+    torch = _torch()
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_err_flag(err_flag, clear: bool = True) -> int:
+    """Synchronise the current stream and return (optionally clearing) the flag bits."""
+    lib = _lib.load()
+    out = ctypes.c_int(0)
+    st = lib.pa_check_err_flag(_ptr(err_flag), int(clear), ctypes.byref(out), _stream(err_flag.device))
+    if st not in (_lib.PA_OK, _lib.PA_ERR_DEVICE_BOUNDS):
+        _lib.check(st, "pa_check_err_flag")
+    return int(out.value)
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, err_flag=None) -> None:
+    """Write key/value rows [T, Hkv, D] into cache slots (slot < 0: skip)."""
+    for n, t in (("key", key), ("value", value), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("slot_mapping", slot_mapping)):
+        _cuda_contig(n, t)
+    torch = _torch()
+    _need(key.dim() == 3 and value.shape == key.shape, "key/value must be [T, Hkv, D]")
+    _need(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [NB, bs, Hkv, D]")
+    _need(k_cache.shape[2:] == key.shape[1:], "cache and key head shapes differ")
+    _need(key.dtype == value.dtype == k_cache.dtype == v_cache.dtype, "dtype mismatch")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == key.shape[0],
+          "slot_mapping must be int64 [T]")
+    nb, bs, hkv, d = k_cache.shape
+    st = _lib.load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d,
+                                          _dtype_code(key), _ptr(err_flag), _stream(key.device))
+    _lib.check(st, "pa_reshape_and_cache")
+
+
+def copy_blocks(k_cache, v_cache, block_mapping, err_flag=None) -> None:
+    """Copy whole blocks for each (src, dst) row of block_mapping [P, 2] int64."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("block_mapping", block_mapping)):
+        _cuda_contig(n, t)
+    torch = _torch()
+    _need(block_mapping.dtype == torch.int64 and block_mapping.dim() == 2 and block_mapping.shape[1] == 2,
+          "block_mapping must be int64 [P, 2]")
+    _need(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype, "cache mismatch")
+    nb, bs, hkv, d = k_cache.shape
+    st = _lib.load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_mapping),
+                                    block_mapping.shape[0], nb, bs, hkv, d, _dtype_code(k_cache),
+                                    _ptr(err_flag), _stream(k_cache.device))
+    _lib.check(st, "pa_copy_blocks")
+
+
+def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          max_context_len, partition_size=0) -> int:
+    n = _lib.load().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                             max_context_len, partition_size)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("arguments rejected by pa_decode_workspace_size")
+    return int(n)
+
+
+def decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          max_context_len, partition_size=0) -> int:
+    return int(_lib.load().pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                    block_size, max_context_len, partition_size))
+
+
+class DecodeWorkspace:
+    """A zero-initialised device workspace for pa_decode, grown on demand.
+
+    One instance must not serve two decode calls that can overlap on the GPU
+    (the default per-(device, stream) instances used by :func:`decode` never do).
+    """
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        torch = _torch()
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device or "cuda")
+            st = _lib.load().pa_decode_workspace_init(_ptr(self.buf), nbytes, _stream(self.buf.device))
+            _lib.check(st, "pa_decode_workspace_init")
+        return self.buf
+
+
+_default_ws: dict = {}
+
+
+def decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: float,
+           max_context_len: int | None = None, partition_size: int = 0, workspace=None,
+           err_flag=None) -> None:
+    """Paged decode attention into ``out`` [B, Hq, D] (f16, bf16 or f32).
+
+    ``max_context_len`` is a host-side bound on ``context_lens`` (defaults to
+    the block-table width times the block size)."""
+    torch = _torch()
+    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(query.dim() == 3 and out.shape == query.shape, "query/out must be [B, Hq, D]")
+    _need(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [NB, bs, Hkv, D]")
+    _need(query.dtype == k_cache.dtype == v_cache.dtype, "query and caches must share a dtype")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.shape[0] == query.shape[0], "block_tables must be int32 [B, maxNB]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == query.shape[0],
+          "context_lens must be int32 [B]")
+    B, Hq, D = query.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    _need(d2 == D, "head_dim mismatch")
+    maxnb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = maxnb * bs
+    ws_bytes = decode_workspace_size(B, Hq, hkv, D, bs, max_context_len, partition_size)
+    if workspace is None:
+        key = (query.device.index, torch.cuda.current_stream(query.device).cuda_stream)
+        workspace = _default_ws.setdefault(key, DecodeWorkspace(query.device))
+    buf = workspace.get(ws_bytes) if isinstance(workspace, DecodeWorkspace) else workspace
+    nbytes = 0 if buf is None else buf.numel() * buf.element_size()
+    st = _lib.load().pa_decode(_ptr(out), _dtype_code(out, allow_f32=True), _ptr(query),
+                               _ptr(k_cache), _ptr(v_cache), _dtype_code(query), _ptr(block_tables),
+                               maxnb, _ptr(context_lens), int(max_context_len), B, Hq, hkv, D, bs, nb,
+                               float(scale), int(partition_size), _ptr(buf), nbytes, _ptr(err_flag),
+                               _stream(query.device))
+    _lib.check(st, "pa_decode")

@@ -1,0 +1,300 @@
+// The exported C ABI (declared in include/pa.h): argument validation,
+// partition and workspace planning, TMA descriptor encoding and launches.
+// The library allocates no memory and keeps no state between calls beyond
+// cached device attributes and the driver entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+#define PA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool half_dtype(pa_dtype d) { return d == PA_F16 || d == PA_BF16; }
+bool supported_head_dim(int d) { return d == 64 || d == 128; }
+bool supported_block_size(int bs) { return bs == 8 || (bs >= 16 && bs <= 256 && bs % 16 == 0); }
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+bool device_info(DeviceInfo &info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    if (cudaDeviceGetAttribute(&info.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+        return false;
+    return true;
+}
+
+// Partition length in tokens for pa_decode; 0 when the request is invalid.
+int resolve_partition(int max_context_len, int block_size, int requested) {
+    const int cap = 32 * block_size;
+    if (requested != 0) {
+        if (requested < 16 || requested % 16 != 0 || requested > cap) return 0;
+        return requested;
+    }
+    int P;
+    if (max_context_len <= 256)
+        P = static_cast<int>(std::max<int64_t>(16, round_up(max_context_len, 16)));
+    else if (max_context_len <= 8192)
+        P = 256;
+    else
+        P = 512;
+    return std::min(P, cap);
+}
+
+struct WorkspacePlan {
+    int partition = 0;
+    int max_partitions = 1;
+    size_t counters_off = 0, ml_off = 0, acc_off = 0, bytes = 0;
+};
+
+bool plan_workspace(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                    int max_context_len, int partition_size, WorkspacePlan &w) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads != 0)
+        return false;
+    if (!supported_group(num_heads / num_kv_heads) || !supported_head_dim(head_dim) ||
+        !supported_block_size(block_size) || max_context_len < 0)
+        return false;
+    w.partition = resolve_partition(max_context_len, block_size, partition_size);
+    if (w.partition == 0) return false;
+    w.max_partitions = std::max(1, (max_context_len + w.partition - 1) / w.partition);
+    if (w.max_partitions <= 1) {
+        w.bytes = 0;
+        return true;
+    }
+    const int G = num_heads / num_kv_heads;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    const int64_t slots = pairs * w.max_partitions;
+    w.counters_off = 0;
+    w.ml_off = round_up(pairs * 4, 256);
+    w.acc_off = w.ml_off + round_up(slots * G * 2 * 4, 256);
+    w.bytes = w.acc_off + static_cast<size_t>(slots) * G * head_dim * 4;
+    return true;
+}
+
+bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int block_size,
+                      int num_kv_heads, int head_dim) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
+                                static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(num_blocks) * block_size};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                   static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+    const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(std::min(block_size, 16))};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(cache), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+PA_EXPORT const char *pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_WORKSPACE: return "decode workspace missing or too small";
+        case PA_ERR_DEVICE_BOUNDS: return "device-side index out of bounds (see err_flag bits)";
+    }
+    return "unknown status";
+}
+
+PA_EXPORT int pa_version(void) { return 100; }
+
+PA_EXPORT pa_status pa_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                         void *v_cache, const int64_t *slot_mapping,
+                                         int64_t num_tokens, int64_t num_blocks, int block_size,
+                                         int num_kv_heads, int head_dim, pa_dtype dtype,
+                                         int *err_flag, void *stream) {
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || !half_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    if ((static_cast<int64_t>(num_kv_heads) * head_dim * 2) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
+    cudaError_t e = pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping,
+                                                 num_tokens, num_blocks * block_size, row_bytes,
+                                                 err_flag, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                                   int64_t num_pairs, int64_t num_blocks, int block_size,
+                                   int num_kv_heads, int head_dim, pa_dtype dtype, int *err_flag,
+                                   void *stream) {
+    if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || !half_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, num_blocks,
+                                           block_bytes, err_flag,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int max_context_len,
+                                          int partition_size) {
+    WorkspacePlan w;
+    if (!plan_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                        partition_size, w))
+        return static_cast<size_t>(-1);
+    return w.bytes;
+}
+
+PA_EXPORT int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int max_context_len,
+                                       int partition_size) {
+    WorkspacePlan w;
+    if (!plan_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                        partition_size, w))
+        return 0;
+    return w.partition;
+}
+
+PA_EXPORT pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes,
+                                             void *stream) {
+    if (workspace_bytes == 0) return PA_OK;
+    if (workspace == nullptr) return PA_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
+                              const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int max_context_len, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, float scale, int partition_size,
+                              void *workspace, size_t workspace_bytes, int *err_flag,
+                              void *stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
+        return PA_ERR_INVALID_ARG;
+    if (!half_dtype(kv_dtype) || (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!supported_group(num_heads / num_kv_heads) || !supported_head_dim(head_dim) ||
+        !supported_block_size(block_size))
+        return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+        return PA_ERR_INVALID_ARG;
+    if (num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    WorkspacePlan w;
+    if (!plan_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                        partition_size, w))
+        return PA_ERR_INVALID_ARG;
+    // Work is counted in 16-token stages in 32-bit arithmetic on the device.
+    const int64_t max_units = static_cast<int64_t>(num_seqs) * num_kv_heads *
+                              std::max<int64_t>(1, (max_context_len + 15) / 16);
+    if (max_units >= (int64_t{1} << 31)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    if (w.bytes > 0 && (workspace == nullptr || workspace_bytes < w.bytes || !aligned16(workspace)))
+        return PA_ERR_WORKSPACE;
+
+    DeviceInfo dev;
+    if (!device_info(dev)) return PA_ERR_CUDA;
+    const int G = num_heads / num_kv_heads;
+    int warps = head_dim == 128 ? 8 : 16;
+    while (warps > 1 && pa::decode_smem_bytes(head_dim, G, warps, num_seqs) >
+                            static_cast<size_t>(dev.smem_optin))
+        --warps;
+    const size_t smem = pa::decode_smem_bytes(head_dim, G, warps, num_seqs);
+    if (smem > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
+    const size_t smem_used = smem;
+
+    CUtensorMap tk, tv;
+    if (!encode_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !encode_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim))
+        return PA_ERR_CUDA;
+
+    pa::DecodeParams p{};
+    p.out = out;
+    p.out_dtype = static_cast<int>(out_dtype);
+    p.q = query;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_context_len = max_context_len;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.partition_size = w.partition;
+    p.max_partitions = w.max_partitions;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.counters = w.bytes ? reinterpret_cast<uint32_t *>(ws + w.counters_off) : nullptr;
+    p.ws_ml = w.bytes ? reinterpret_cast<float *>(ws + w.ml_off) : nullptr;
+    p.ws_acc = w.bytes ? reinterpret_cast<float *>(ws + w.acc_off) : nullptr;
+    p.err_flag = err_flag;
+
+    cudaError_t e = pa::launch_decode(p, head_dim, G, kv_dtype == PA_BF16, tk, tv, dev.sms, warps,
+                                      smem_used, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT pa_status pa_check_err_flag(int *err_flag, int clear, int *flag_out, void *stream) {
+    if (err_flag == nullptr) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    if (cudaMemcpyAsync(&host, err_flag, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    if (clear && cudaMemsetAsync(err_flag, 0, sizeof(int), s) != cudaSuccess) return PA_ERR_CUDA;
+    if (flag_out) *flag_out = host;
+    return host == 0 ? PA_OK : PA_ERR_DEVICE_BOUNDS;
+}

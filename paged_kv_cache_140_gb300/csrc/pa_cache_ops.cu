@@ -1,0 +1,134 @@
+// reshape_and_cache and copy_blocks for sm_103a: bit-exact row and block
+// copies with 16-byte vector accesses.
+//
+// reshape_and_cache writes each new token's K/V row ([Hkv, D], contiguous in
+// both the source and the cache) into its slot, slot = block * bs + offset
+// (nano-vllm walkthrough lqnn.cn/news/170268, §2.2 and §2.3 step 3).
+// copy_blocks duplicates whole physical blocks for copy-on-write
+// ("优化大模型推理：PagedAttention 如何实现 GPU 显存高效管理", copy-on-write
+// section).  Both are pure data movement bound by HBM bandwidth; grids are
+// sized in multiples of the SM count by the host.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+// One CTA per token (grid-stride over tokens); threads stride over the row's
+// 16-byte chunks, K and V interleaved for memory-level parallelism.
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                             uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                             const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                             int64_t num_slots, int64_t row16, int *err_flag) {
+    for (int64_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (threadIdx.x == 0) report(err_flag, 0x1 /* PA_FLAG_BAD_SLOT */);
+            continue;
+        }
+        const uint4 *ks = key + t * row16;
+        const uint4 *vs = value + t * row16;
+        uint4 *kd = k_cache + slot * row16;
+        uint4 *vd = v_cache + slot * row16;
+        int64_t i = threadIdx.x;
+        for (; i + blockDim.x < row16; i += 2 * blockDim.x) {
+            const uint4 a = __ldg(ks + i), b = __ldg(ks + i + blockDim.x);
+            const uint4 c = __ldg(vs + i), d = __ldg(vs + i + blockDim.x);
+            kd[i] = a; kd[i + blockDim.x] = b;
+            vd[i] = c; vd[i + blockDim.x] = d;
+        }
+        for (; i < row16; i += blockDim.x) {
+            kd[i] = __ldg(ks + i);
+            vd[i] = __ldg(vs + i);
+        }
+    }
+}
+
+// grid.x: copy pairs (grid-stride), grid.y: slices of the block; each thread
+// moves 4 chunks of 16 bytes of K and of V per iteration.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                       const int64_t *__restrict__ block_mapping, int64_t num_pairs,
+                       int64_t num_blocks, int64_t block16, int *err_flag) {
+    const int64_t slice = (block16 + gridDim.y - 1) / gridDim.y;
+    const int64_t beg = blockIdx.y * slice;
+    const int64_t end = min(block16, beg + slice);
+    for (int64_t pr = blockIdx.x; pr < num_pairs; pr += gridDim.x) {
+        const int64_t src = block_mapping[2 * pr];
+        const int64_t dst = block_mapping[2 * pr + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (threadIdx.x == 0 && blockIdx.y == 0) report(err_flag, 0x8 /* PA_FLAG_BAD_COPY_PAIR */);
+            continue;
+        }
+        const uint4 *ks = k_cache + src * block16;
+        const uint4 *vs = v_cache + src * block16;
+        uint4 *kd = k_cache + dst * block16;
+        uint4 *vd = v_cache + dst * block16;
+        int64_t i = beg + threadIdx.x;
+        const int64_t step = blockDim.x;
+        for (; i + 3 * step < end; i += 4 * step) {
+            uint4 a[4], b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) { a[u] = ks[i + u * step]; b[u] = vs[i + u * step]; }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) { kd[i + u * step] = a[u]; vd[i + u * step] = b[u]; }
+        }
+        for (; i < end; i += step) {
+            kd[i] = ks[i];
+            vd[i] = vs[i];
+        }
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return n > 0 ? n : 148;
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                     void *v_cache, const int64_t *slot_mapping,
+                                     int64_t num_tokens, int64_t num_slots, int64_t row_bytes,
+                                     int *err_flag, cudaStream_t stream) {
+    const int64_t row16 = row_bytes / 16;
+    const int threads = row16 >= 256 ? 256 : (row16 >= 128 ? 128 : 64);
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+    const int grid = static_cast<int>(num_tokens < cap ? num_tokens : cap);
+    reshape_and_cache_kernel<<<grid, threads, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
+        num_slots, row16, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                               int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
+                               int *err_flag, cudaStream_t stream) {
+    const int64_t block16 = block_bytes / 16;
+    const int threads = 256;
+    const int sms = sm_count();
+    // Enough CTAs to cover the SMs a few times over, each slice >= 4 chunks/thread.
+    int64_t slices = (block16 + 4 * threads - 1) / (4 * threads);
+    const int64_t want = 4LL * sms;
+    if (num_pairs * slices < want) {
+        const int64_t more = (want + num_pairs - 1) / num_pairs;
+        const int64_t maxs = (block16 + threads - 1) / threads;
+        slices = more < maxs ? more : maxs;
+    }
+    if (slices < 1) slices = 1;
+    if (slices > 65535) slices = 65535;
+    const int64_t gx = num_pairs < 65535LL * 16 ? num_pairs : 65535LL * 16;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(slices));
+    copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4 *>(k_cache),
+                                                     static_cast<uint4 *>(v_cache), block_mapping,
+                                                     num_pairs, num_blocks, block16, err_flag);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,55 @@
+// Host-side interface between the C ABI (pa_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Tokens per pipeline stage of the decode kernel: one stage brings 16 K rows
+// and 16 V rows of one KV head into shared memory.
+constexpr int kStageTokens = 16;
+// Stages in flight per warp (ring depth).
+constexpr int kStages = 3;
+
+struct DecodeParams {
+    void *out;
+    int out_dtype;               // pa_dtype value
+    const void *q;               // [B, Hq, D]
+    const int32_t *block_tables; // [B, max_blocks_per_seq]
+    const int32_t *context_lens; // [B]
+    int max_blocks_per_seq;
+    int max_context_len;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int block_size;
+    int64_t num_blocks;
+    float scale_log2;            // softmax scale * log2(e)
+    int partition_size;          // tokens per partition, multiple of 16
+    int max_partitions;          // partition slots per (seq, KV head) in the workspace
+    uint32_t *counters;          // [B * Hkv] completion tickets (zero between calls)
+    float *ws_ml;                // [B * Hkv * max_partitions, G, 2]  (max, sum)
+    float *ws_acc;               // [B * Hkv * max_partitions, G, D]
+    int *err_flag;
+};
+
+// Shared memory the decode kernel needs for `warps` warps and `num_seqs`
+// sequences (including alignment slack).
+size_t decode_smem_bytes(int head_dim, int group, int warps, int num_seqs);
+
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, bool bf16,
+                          const CUtensorMap &tmap_k, const CUtensorMap &tmap_v, int grid,
+                          int warps, size_t smem, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                     void *v_cache, const int64_t *slot_mapping,
+                                     int64_t num_tokens, int64_t num_slots, int64_t row_bytes,
+                                     int *err_flag, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                               int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
+                               int *err_flag, cudaStream_t stream);
+
+}  // namespace pa

@@ -209,15 +209,21 @@ def make_context_lens(name: str, num_seqs: int | None = None, seed: int | None =
 
 def make_batch(name: str, *, num_seqs: int | None = None, groups: int | None = None,
                seed: int | None = None, ctx_cap: int | None = None,
-               block_size: int | None = None, context_lens=None) -> Batch:
+               block_size: int | None = None, context_lens=None, **overrides) -> Batch:
     """Build the inputs of workload ``name`` (a key of :data:`CONFIGS`).
 
     ``num_seqs`` (or ``groups`` for "prefix") shrinks the batch while keeping
     every other property of the workload; ``ctx_cap`` clips the context law to
     a shorter maximum (for oracle-sized cases); ``context_lens`` replaces the
-    drawn lengths outright (edge-case tests).
+    drawn lengths outright (edge-case tests); other keywords (``num_heads``,
+    ``num_kv_heads``, ``head_dim``, ``dtype``, ``partition_size``) override the
+    workload's entries.
     """
     cfg = dict(CONFIGS[name])
+    for k, v in overrides.items():
+        if k not in ("num_heads", "num_kv_heads", "head_dim", "dtype", "partition_size"):
+            raise TypeError(f"unknown override {k}")
+        cfg[k] = v
     if seed is None:
         seed = 140000 + cfg["number"]
     rng = np.random.Generator(np.random.PCG64(seed))
