@@ -374,12 +374,27 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def decode_source_hash() -> str:
+    """Hash of the decode kernel's sources; a traffic figure taken from an
+    older kernel is not reported."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("pa_decode.cu", "pa_device.cuh", "pa_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_140_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(workload):
-    """DRAM bytes per decode launch from the committed ncu summary, if current."""
+    """DRAM bytes per decode launch (ncu dram__bytes_read.sum + write.sum),
+    scaled to this workload, from the committed profile summary - or None
+    when the summary was taken on a different kernel source."""
     path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        if d.get("kernel_source_hash") != decode_source_hash():
+            return None
         return d.get("dram_bytes_per_launch")
     except Exception:
         return None
@@ -430,15 +445,21 @@ def cpu_baseline(b, target_s):
     kc, vc = _post_step_caches(b)
     pick = _pick_sample(b, target_s, kc, vc)
     sub = W.subset_batch(b, pick)
+    runs = 0
     t = time.perf_counter()
-    oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
-    dt = time.perf_counter() - t
+    while True:  # repeat a sample that is the whole batch until ~target_s of CPU work
+        oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
+        runs += 1
+        if time.perf_counter() - t >= target_s or len(pick) < b.num_seqs:
+            break
+    dt = (time.perf_counter() - t) / runs
     sb = kv_bytes(sub)
     return {"value": round(sb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "seconds": round(dt, 2),
+            "seconds": round(dt * runs, 2),
             "sample": f"attention of {len(pick)} of {b.num_seqs} sequences (every "
                       f"{max(1, b.num_seqs // max(1, len(pick)))}th; {int(sub.context_lens.sum())} tokens, "
-                      f"{sb} KV bytes) over the post-step caches; fp64 C oracle, OpenMP over (seq, head)"}
+                      f"{sb} KV bytes) over the post-step caches, run {runs}x; fp64 C oracle, "
+                      f"OpenMP over (seq, head)"}
 
 
 def run_reference(args, world, rank):

@@ -101,7 +101,11 @@ pa_status pa_reshape_and_cache(const void *key, const void *value,
  * max, sum of exponentials, unnormalised weighted V sum, fp32) and one
  * completion counter per (sequence, KV head).  It must be ZERO-FILLED before
  * its first use (pa_decode_workspace_init does that); every pa_decode that
- * completes leaves the counters at zero again, so later calls need no reset.
+ * completes leaves the counters at zero again, so later calls with the same
+ * arguments to this function need no reset.  A workspace reused for a call
+ * whose arguments here differ must be zero-filled again first (the counter
+ * region of one layout overlaps the partial-result region of another), as
+ * must one whose last call reported PA_FLAG_TIMEOUT.
  * `partition_size` is the same value later passed to pa_decode (0 = auto).
  * Returns (size_t)-1 for arguments pa_decode would reject.
  */

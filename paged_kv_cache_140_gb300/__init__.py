@@ -140,15 +140,24 @@ class DecodeWorkspace:
     def __init__(self, device=None):
         self.device = device
         self.buf = None
+        self.layout = None
 
-    def get(self, nbytes: int):
+    def get(self, nbytes: int, layout=None):
+        """The buffer for a call needing ``nbytes`` with workspace ``layout``
+        (the arguments of pa_decode_workspace_size).  It is zero-filled when
+        first allocated and again whenever the layout changes, because the
+        completion tickets of one layout overlap other regions of another."""
         torch = _torch()
         if nbytes == 0:
             return None
-        if self.buf is None or self.buf.numel() < nbytes:
+        fresh = self.buf is None or self.buf.numel() < nbytes
+        if fresh:
             self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device or "cuda")
-            st = _lib.load().pa_decode_workspace_init(_ptr(self.buf), nbytes, _stream(self.buf.device))
+        if fresh or layout != self.layout:
+            st = _lib.load().pa_decode_workspace_init(_ptr(self.buf), self.buf.numel(),
+                                                      _stream(self.buf.device))
             _lib.check(st, "pa_decode_workspace_init")
+            self.layout = layout
         return self.buf
 
 
@@ -183,7 +192,8 @@ def decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: floa
     if workspace is None:
         key = (query.device.index, torch.cuda.current_stream(query.device).cuda_stream)
         workspace = _default_ws.setdefault(key, DecodeWorkspace(query.device))
-    buf = workspace.get(ws_bytes) if isinstance(workspace, DecodeWorkspace) else workspace
+    layout = (B, Hq, hkv, D, bs, int(max_context_len), int(partition_size))
+    buf = workspace.get(ws_bytes, layout) if isinstance(workspace, DecodeWorkspace) else workspace
     nbytes = 0 if buf is None else buf.numel() * buf.element_size()
     st = _lib.load().pa_decode(_ptr(out), _dtype_code(out, allow_f32=True), _ptr(query),
                                _ptr(k_cache), _ptr(v_cache), _dtype_code(query), _ptr(block_tables),
