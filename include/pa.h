@@ -172,6 +172,45 @@ pa_status pa_decode(void *out, pa_dtype out_dtype,
                     int *err_flag, void *stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for callers of this
+ * library that cannot allocate, and so cannot supply pa_decode's workspace:
+ * code running inside a host framework that owns all device memory and
+ * forbids allocation while it executes (an inference engine plugin's execute
+ * step, for example), or a deployment whose device-memory budget is fixed
+ * when the library loads.
+ *
+ * Arguments and results are those of pa_decode without the workspace.  The
+ * workspace is instead a scratch array of PA_NOALLOC_SCRATCH_BYTES inside the
+ * library (a static __device__ array): every GPU that loads the library holds
+ * that memory until the process exits.  The call allocates nothing - no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *  - Returns PA_ERR_WORKSPACE, enqueuing nothing, when
+ *    pa_decode_workspace_size(...) for these arguments exceeds
+ *    PA_NOALLOC_SCRATCH_BYTES (use a larger partition_size, fewer sequences,
+ *    or pa_decode with a workspace of your own).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents; each call clears the part that must start at zero (its
+ *    completion counters) with a stream-ordered memset before its kernel.
+ *    Calls that may overlap on the GPU - different streams, threads or
+ *    processes' shared contexts - race on the array and corrupt each other's
+ *    results: order them (one stream, or events).
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype,
+                            const void *query,
+                            const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int max_context_len,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale,
+                            int partition_size, int *err_flag, void *stream);
+
+/*
  * pa_copy_blocks -- copy-on-write of shared blocks.
  *
  * A block referenced by several sequences is read-only; before one of them

@@ -1,0 +1,105 @@
+"""pa_decode_noalloc, the decode entry point for callers that cannot allocate.
+
+Some users of this library cannot allocate device memory while they run - for
+example a plugin executing inside an inference engine that owns all device
+memory, or a deployment with a device-memory budget fixed at load time - so
+they cannot hand pa_decode a workspace.  pa_decode_noalloc keeps that
+workspace in a fixed scratch array inside the library instead.  These tests
+call it through the C ABI and check it against pa_decode on consecutive calls
+(the array keeps the previous call's contents, so each call must clear what
+has to start at zero), including calls whose workspace layouts differ.
+
+This file is named to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_140_gb300 import _build, _lib
+    _build.build()
+    return torch, _lib.load()
+
+
+def _dev_batch(torch, b):
+    from pa_harness import to_device
+    T = to_device(b)
+    import paged_kv_cache_140_gb300 as pa
+    pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"])
+    torch.cuda.synchronize()
+    return T
+
+
+def _reference(torch, b, T):
+    """Output of the existing entry point, pa_decode (caller-provided workspace)."""
+    import paged_kv_cache_140_gb300 as pa
+    out = torch.empty(T["q"].shape, dtype=torch.float32, device="cuda")
+    err = pa.new_err_flag()
+    pa.decode(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"],
+              float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
+              workspace=pa.DecodeWorkspace("cuda"), err_flag=err)
+    assert pa.read_err_flag(err) == 0
+    return out
+
+
+def _noalloc(torch, lib, b, T):
+    import paged_kv_cache_140_gb300 as pa
+    out = torch.full(T["q"].shape, float("nan"), dtype=torch.float32, device="cuda")
+    err = pa.new_err_flag()
+    P = ctypes.c_void_p
+    st = lib.pa_decode_noalloc(
+        P(out.data_ptr()), 2, P(T["q"].data_ptr()), P(T["k_cache"].data_ptr()), P(T["v_cache"].data_ptr()),
+        1 if b.dtype == "bf16" else 0, P(T["block_tables"].data_ptr()), T["block_tables"].shape[1],
+        P(T["context_lens"].data_ptr()), b.max_context_len, b.num_seqs, b.num_heads, b.num_kv_heads,
+        b.head_dim, b.block_size, b.num_blocks, float(b.scale), b.partition_size, P(err.data_ptr()),
+        P(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, f"pa_decode_noalloc returned {st}"
+    torch.cuda.synchronize()
+    assert pa.read_err_flag(err) == 0
+    return out
+
+
+def _close(torch, a, b):
+    from pa_harness import ATOL
+    d = (a - b).abs().max().item()
+    assert torch.isfinite(a).all() and d <= ATOL, f"max abs difference {d:.3e}"
+
+
+def test_noalloc_matches_pa_decode_on_consecutive_calls(env):
+    torch, lib = env
+    from paged_kv_cache_140_gb300 import workloads as W
+    b1 = W.make_batch("13b", num_seqs=24)                 # split sequences: scratch in use
+    b2 = W.make_batch("gqa", num_seqs=2, ctx_cap=12000)   # another workspace layout
+    T1, T2 = _dev_batch(torch, b1), _dev_batch(torch, b2)
+    r1, r2 = _reference(torch, b1, T1), _reference(torch, b2, T2)
+    for b, T, r in ((b1, T1, r1), (b1, T1, r1), (b2, T2, r2), (b1, T1, r1)):
+        _close(torch, _noalloc(torch, lib, b, T), r)
+
+
+def test_noalloc_without_split_sequences(env):
+    torch, lib = env
+    from paged_kv_cache_140_gb300 import workloads as W
+    b = W.make_batch("tiny")
+    T = _dev_batch(torch, b)
+    r = _reference(torch, b, T)
+    for _ in range(2):
+        _close(torch, _noalloc(torch, lib, b, T), r)
+
+
+def test_noalloc_rejects_requests_beyond_the_scratch_limit(env):
+    torch, lib = env
+    from paged_kv_cache_140_gb300 import _lib as L
+    need = lib.pa_decode_workspace_size(256, 40, 40, 128, 16, 2048, 16)
+    assert need > 32 * 1024 * 1024
+    nul = ctypes.c_void_p(0)
+    st = lib.pa_decode_noalloc(nul, 2, nul, nul, nul, 1, nul, 128, nul, 2048, 256, 40, 40, 128, 16,
+                               10000, 0.088, 16, nul, nul)
+    assert st == L.PA_ERR_WORKSPACE
