@@ -224,6 +224,9 @@ def run_ours(args, world, rank, local):
                                  b.max_context_len, b.partition_size)
     ws = pa.DecodeWorkspace(device)
     has_pairs = len(b.block_mapping) > 0
+    # pa_decode adds a merge launch when some sequence spans several partitions.
+    split = pa.decode_workspace_size(b.num_seqs, b.num_heads, b.num_kv_heads, b.head_dim, b.block_size,
+                                     b.max_context_len, b.partition_size) > 0
     stream = torch.cuda.current_stream(device)
 
     def step(ev=None):
@@ -365,7 +368,7 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": int(d2h),
                 "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens -> device, "
                         "the step, output -> pinned host, stream sync; the KV cache stays resident"},
-        "gpu_launches": K * (2 + (1 if has_pairs else 0)),
+        "gpu_launches": K * (2 + (1 if has_pairs else 0) + (1 if split else 0)),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

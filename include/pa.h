@@ -97,15 +97,10 @@ pa_status pa_reshape_and_cache(const void *key, const void *value,
  * pa_decode_workspace_size -- bytes of workspace pa_decode needs.
  *
  * Returns 0 when no sequence can be split (max_context_len fits in one
- * partition).  The workspace holds per-partition partial results (running
- * max, sum of exponentials, unnormalised weighted V sum, fp32) and one
- * completion counter per (sequence, KV head).  It must be ZERO-FILLED before
- * its first use (pa_decode_workspace_init does that); every pa_decode that
- * completes leaves the counters at zero again, so later calls with the same
- * arguments to this function need no reset.  A workspace reused for a call
- * whose arguments here differ must be zero-filled again first (the counter
- * region of one layout overlaps the partial-result region of another), as
- * must one whose last call reported PA_FLAG_TIMEOUT.
+ * partition).  The workspace holds the per-partition partial results of split
+ * sequences (running max, sum of exponentials, unnormalised weighted V sum,
+ * fp32).  It needs no initial contents: every partial is written before it is
+ * read, within the same call.
  * `partition_size` is the same value later passed to pa_decode (0 = auto).
  * Returns (size_t)-1 for arguments pa_decode would reject.
  */
@@ -113,7 +108,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                 int head_dim, int block_size, int max_context_len,
                                 int partition_size);
 
-/* Zero-fill a decode workspace (stream-ordered memset). */
+/* Zero-fill a decode workspace (stream-ordered memset); optional, since the
+ * workspace needs no initial contents. */
 pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /* The partition length, in tokens, pa_decode uses for these arguments. */
@@ -153,8 +149,8 @@ int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads,
  *   scale        : softmax scale, usually 1/sqrt(head_dim)
  *   partition_size : 0 (auto) or a multiple of 16 tokens, at most
  *                  32 * block_size
- *   workspace    : device buffer of pa_decode_workspace_size(...) bytes,
- *                  zero-filled before first use (may be NULL if that size is 0)
+ *   workspace    : device buffer of pa_decode_workspace_size(...) bytes
+ *                  (may be NULL if that size is 0)
  * Device-side problems: a block id outside [0, num_blocks) is not read, its
  * tokens are left out of the softmax and PA_FLAG_BAD_BLOCK_ID is set; a
  * context length outside [0, max_context_len] gives a zero row and
@@ -194,11 +190,11 @@ pa_status pa_decode(void *out, pa_dtype out_dtype,
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture on the device.
  *  - Every call on a device shares the one array, which keeps the previous
- *    call's contents; each call clears the part that must start at zero (its
- *    completion counters) with a stream-ordered memset before its kernel.
- *    Calls that may overlap on the GPU - different streams, threads or
- *    processes' shared contexts - race on the array and corrupt each other's
- *    results: order them (one stream, or events).
+ *    call's contents; nothing in it needs clearing between calls (every
+ *    partial result is written before it is read within a call).  Calls that
+ *    may overlap on the GPU - different streams, threads or processes' shared
+ *    contexts - race on the array and corrupt each other's results: order
+ *    them (one stream, or events).
  */
 #define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype,

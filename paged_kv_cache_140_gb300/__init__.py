@@ -131,7 +131,8 @@ def decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, block_siz
 
 
 class DecodeWorkspace:
-    """A zero-initialised device workspace for pa_decode, grown on demand.
+    """A device workspace for pa_decode, grown on demand (no initial contents
+    are needed).
 
     One instance must not serve two decode calls that can overlap on the GPU
     (the default per-(device, stream) instances used by :func:`decode` never do).
@@ -140,24 +141,14 @@ class DecodeWorkspace:
     def __init__(self, device=None):
         self.device = device
         self.buf = None
-        self.layout = None
 
     def get(self, nbytes: int, layout=None):
-        """The buffer for a call needing ``nbytes`` with workspace ``layout``
-        (the arguments of pa_decode_workspace_size).  It is zero-filled when
-        first allocated and again whenever the layout changes, because the
-        completion tickets of one layout overlap other regions of another."""
+        """A buffer of at least ``nbytes`` bytes (None when nothing is needed)."""
         torch = _torch()
         if nbytes == 0:
             return None
-        fresh = self.buf is None or self.buf.numel() < nbytes
-        if fresh:
+        if self.buf is None or self.buf.numel() < nbytes:
             self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device or "cuda")
-        if fresh or layout != self.layout:
-            st = _lib.load().pa_decode_workspace_init(_ptr(self.buf), self.buf.numel(),
-                                                      _stream(self.buf.device))
-            _lib.check(st, "pa_decode_workspace_init")
-            self.layout = layout
         return self.buf
 
 

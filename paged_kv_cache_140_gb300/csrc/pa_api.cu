@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <stdlib.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -59,6 +61,28 @@ bool device_info(DeviceInfo &info) {
     return true;
 }
 
+struct Tuning {
+    int stages = 0;  // 0: default
+    int warps = 0;
+};
+
+int env_int(const char *name, int lo, int hi) {
+    const char *v = getenv(name);
+    if (v == nullptr) return 0;
+    const int x = atoi(v);
+    return (x >= lo && x <= hi) ? x : 0;
+}
+
+const Tuning &tuning() {
+    static const Tuning t = [] {
+        Tuning r;
+        r.stages = env_int("PA_DECODE_STAGES", 2, 8);
+        r.warps = env_int("PA_DECODE_WARPS", 1, 16);
+        return r;
+    }();
+    return t;
+}
+
 // Partition length in tokens for pa_decode; 0 when the request is invalid.
 int resolve_partition(int max_context_len, int block_size, int requested) {
     const int cap = 32 * block_size;
@@ -79,7 +103,7 @@ int resolve_partition(int max_context_len, int block_size, int requested) {
 struct WorkspacePlan {
     int partition = 0;
     int max_partitions = 1;
-    size_t counters_off = 0, ml_off = 0, acc_off = 0, bytes = 0;
+    size_t ml_off = 0, acc_off = 0, bytes = 0;
 };
 
 bool plan_workspace(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
@@ -97,11 +121,9 @@ bool plan_workspace(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
         return true;
     }
     const int G = num_heads / num_kv_heads;
-    const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
-    const int64_t slots = pairs * w.max_partitions;
-    w.counters_off = 0;
-    w.ml_off = round_up(pairs * 4, 256);
-    w.acc_off = w.ml_off + round_up(slots * G * 2 * 4, 256);
+    const int64_t slots = static_cast<int64_t>(num_seqs) * num_kv_heads * w.max_partitions;
+    w.ml_off = 0;
+    w.acc_off = round_up(slots * G * 2 * 4, 256);
     w.bytes = w.acc_off + static_cast<size_t>(slots) * G * head_dim * 4;
     return true;
 }
@@ -247,13 +269,18 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
     DeviceInfo dev;
     if (!device_info(dev)) return PA_ERR_CUDA;
     const int G = num_heads / num_kv_heads;
-    int warps = head_dim == 128 ? 8 : 16;
-    while (warps > 1 && pa::decode_smem_bytes(head_dim, G, warps, num_seqs) >
+    // Ring depth and warps per CTA (PA_DECODE_STAGES / PA_DECODE_WARPS override
+    // the defaults for tuning); fewer warps are used if shared memory is short.
+    const Tuning &tune = tuning();
+    const int stages = tune.stages > 0 ? tune.stages : pa::kDefaultStages;
+    const int max_warps = head_dim == 128 ? 12 : 16;
+    const int def_warps = head_dim == 128 ? pa::kDefaultWarps128 : 16;
+    int warps = tune.warps > 0 ? std::min(tune.warps, max_warps) : def_warps;
+    while (warps > 1 && pa::decode_smem_bytes(head_dim, G, warps, stages, num_seqs) >
                             static_cast<size_t>(dev.smem_optin))
         --warps;
-    const size_t smem = pa::decode_smem_bytes(head_dim, G, warps, num_seqs);
-    if (smem > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
-    const size_t smem_used = smem;
+    const size_t smem_used = pa::decode_smem_bytes(head_dim, G, warps, stages, num_seqs);
+    if (smem_used > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
     CUtensorMap tk, tv;
     if (!encode_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim) ||
@@ -277,10 +304,10 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
     p.partition_size = w.partition;
     p.max_partitions = w.max_partitions;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    p.counters = w.bytes ? reinterpret_cast<uint32_t *>(ws + w.counters_off) : nullptr;
     p.ws_ml = w.bytes ? reinterpret_cast<float *>(ws + w.ml_off) : nullptr;
     p.ws_acc = w.bytes ? reinterpret_cast<float *>(ws + w.acc_off) : nullptr;
     p.err_flag = err_flag;
+    p.stages = stages;
 
     cudaError_t e = pa::launch_decode(p, head_dim, G, kv_dtype == PA_BF16, tk, tv, dev.sms, warps,
                                       smem_used, static_cast<cudaStream_t>(stream));

@@ -14,24 +14,30 @@
 //    Work items are (sequence, partition, KV head); the item list is split
 //    into contiguous ranges of equal token weight, one per warp, so a
 //    long-tailed length mix cannot leave SMs idle at the end.
-//  * Each warp owns a ring of kStages shared-memory slots.  A slot holds one
-//    16-token stage: the K and V rows of one KV head, brought in by TMA
-//    (3-D tensor map over [blocks*block_size, Hkv, D], 64-element boxes with
-//    128-byte swizzle) straight from the physical block the table names,
-//    plus the item's query rows (bulk copy) on its first stage.  Loads for
-//    the next stages - across item boundaries - are in flight while the warp
-//    computes on the current one.
-//  * QK: lane (t, half) dots token t's half row with the fp32 query held in
-//    shared memory (broadcast reads; the swizzle makes the 16 row reads
-//    conflict-free); one shuffle joins the halves.  Online softmax in base 2
-//    with fp32 state (nano-vllm §6: fp32 accumulation).  PV: each lane owns
-//    D/32 output dims and walks the stage's tokens.
-//  * Positions at or beyond the context length are masked by select, never
-//    multiplied, so NaN in stale slots cannot leak (nano-vllm §6).
-//  * Partial states of split sequences go to a caller-owned workspace; the
-//    last warp to finish a (sequence, KV head) - found with an atomic ticket
-//    - merges them in partition order and resets the ticket.  No warp ever
-//    waits on another.
+//  * Each warp owns a ring of shared-memory slots.  A slot holds one 16-token
+//    stage: the K and V rows of one KV head, brought in by TMA (3-D tensor map
+//    over [blocks*block_size, Hkv, D], 64-element boxes with 128-byte swizzle)
+//    straight from the physical block the table names, plus the item's query
+//    rows (bulk copy) on its first stage.  Loads for the next stages - across
+//    item boundaries - are in flight while the warp computes on the current
+//    one; the block-table slice of the next item is prefetched into registers.
+//  * QK and PV run on warp-level tensor-core MMA (m16n8k16, fp32 accumulate):
+//    the query heads of one KV group are the N = 8 columns (a dense tile for
+//    G = 8, padded for smaller groups).  Decode is bound by reading K/V; the
+//    MMA is there to keep each warp's instruction count per byte low enough
+//    that 8 warps per SM keep HBM busy.  ldmatrix reads the swizzled tiles
+//    conflict-free.  The softmax weights enter PV as a 16-bit high part plus
+//    a 16-bit residual, keeping ~16 significant bits.
+//  * Online softmax in base 2 with fp32 state (nano-vllm §6: fp32
+//    accumulation) and lazy rescaling (the reference max only moves when a
+//    logit exceeds it by more than 2^8).
+//  * Positions at or beyond the context length are masked by select, and
+//    their V rows are zeroed in shared memory before PV, so NaN in stale slots
+//    cannot leak (nano-vllm §6).
+//  * Split sequences write their partial states (max, sum, weighted V sum) to
+//    a caller-owned workspace; a small merge kernel, chained with
+//    programmatic dependent launch, combines them in partition order.  No
+//    warp ever waits on another.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -40,7 +46,7 @@ namespace pa {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kRowBytes = 128;                        // one swizzled 64-element half row
+constexpr int kRowBytes = 128;                          // one swizzled 64-element half row
 constexpr int kRegionBytes = kStageTokens * kRowBytes;  // 16 rows x 128 B = 2 KB
 
 template <int D, int G>
@@ -51,10 +57,10 @@ struct Layout {
     static constexpr int kQOffset = 2 * kTileBytes;
     static constexpr int kQBytes = G * D * 2;
     static constexpr int kSlotBytes = ((2 * kTileBytes + kQBytes + 1023) / 1024) * 1024;
-    static constexpr int kQStride = D + 8;                 // floats per fp32 query row
-    static constexpr int kQ32Bytes = G * kQStride * 4;
-    static constexpr int kChunksPerLane = D / 16;          // 16-byte K chunks per lane in QK
-    static constexpr int kDimsPerLane = D / 32;            // output dims per lane in PV
+    static constexpr int kOStride = D + 4;                 // floats per staged output row
+    static constexpr int kOBytes = G * kOStride * 4;       // per-warp output staging
+    static constexpr int kSteps = D / 16;                  // MMA steps over the head dim
+    static constexpr int kDimsPerLane = D / 32;            // output dims per lane in the store
 };
 
 struct StageMeta {
@@ -70,6 +76,20 @@ constexpr int kMetaBytes = sizeof(StageMeta);
 __device__ __forceinline__ uint32_t seq_weight(int ctx, int hkv) {
     int st = ctx > 0 ? (ctx + kStageTokens - 1) / kStageTokens : 1;
     return static_cast<uint32_t>(st) * static_cast<uint32_t>(hkv);
+}
+
+// Maximum over the warp of a float, via an order-preserving integer image.
+__device__ __forceinline__ float warp_max(float x) {
+    int k = __float_as_int(x);
+    k = k >= 0 ? k : k ^ 0x7fffffff;
+    k = __reduce_max_sync(kFull, k);
+    return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
 }
 
 // Cursor over the ordered work items (s, part, kvh) of one warp.
@@ -105,10 +125,46 @@ struct Cursor {
     }
 };
 
-// 128-dim heads run at most 8 warps per CTA (the slot ring fills shared
-// memory), so they get 255 registers per thread; 64-dim heads run up to 16.
+// Block ids of one item's partition, one per lane (lane i: logical block
+// first + i), or -1 past the item's last block.
+__device__ __forceinline__ int32_t load_item_blocks(const DecodeParams &p, const Cursor &c,
+                                                    int P, int lane) {
+    if (c.ntok <= 0) return -1;
+    const int fb = (c.part * P) / p.block_size;
+    const int lb = (c.part * P + c.ntok - 1) / p.block_size;
+    return lane <= lb - fb
+               ? __ldg(p.block_tables + static_cast<int64_t>(c.s) * p.max_blocks_per_seq + fb + lane)
+               : -1;
+}
+
+// Store D/32 consecutive floats of a row (this lane's slice) as f32, bf16 or
+// f16 (pa_dtype codes 2, 1, 0), rounding to nearest even.
 template <int D>
-constexpr int kMaxThreads = D == 128 ? 256 : 512;
+__device__ __forceinline__ void store_row(void *base, int dtype, int64_t off, const float *o) {
+    constexpr int DPL = D / 32;
+    if (dtype == 2) {
+        float *dst = static_cast<float *>(base) + off;
+        if constexpr (DPL == 4)
+            *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        else
+            *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
+    } else {
+        uint16_t h[DPL];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) h[i] = dtype == 1 ? float_to_bf16_bits(o[i]) : float_to_f16_bits(o[i]);
+        uint16_t *dst = static_cast<uint16_t *>(base) + off;
+        if constexpr (DPL == 4)
+            *reinterpret_cast<uint2 *>(dst) =
+                make_uint2(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16));
+        else
+            *reinterpret_cast<uint32_t *>(dst) = h[0] | (uint32_t(h[1]) << 16);
+    }
+}
+
+// 128-dim heads run at most 12 warps per CTA (the slot ring fills shared
+// memory); 64-dim heads run up to 16.
+template <int D>
+constexpr int kMaxThreads = D == 128 ? 384 : 512;
 
 template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(kMaxThreads<D>, 1)
@@ -117,6 +173,9 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
                         const __grid_constant__ CUtensorMap tmap_v) {
     using L = Layout<D, G>;
     using Cvt = Half2x<BF16>;
+    constexpr int KS = L::kSteps;   // QK steps over the head dim
+    constexpr int MT = L::kSteps;   // PV tiles over the head dim
+    constexpr int DPL = L::kDimsPerLane;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -124,18 +183,19 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nw = blockDim.x >> 5;
+    const int S = p.stages;
     const int B = p.num_seqs;
     const int Hkv = p.num_kv_heads;
     const int P = p.partition_size;
 
-    uint8_t *slots = smem + static_cast<size_t>(warp) * kStages * L::kSlotBytes;
-    uint8_t *misc = smem + static_cast<size_t>(nw) * kStages * L::kSlotBytes;
-    float *q32 = reinterpret_cast<float *>(misc + warp * L::kQ32Bytes);
-    misc += nw * L::kQ32Bytes;
-    StageMeta *meta = reinterpret_cast<StageMeta *>(misc) + warp * kStages;
-    misc += nw * kStages * kMetaBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(misc) + warp * kStages;
-    misc += nw * kStages * 8;
+    uint8_t *slots = smem + static_cast<size_t>(warp) * S * L::kSlotBytes;
+    uint8_t *misc = smem + static_cast<size_t>(nw) * S * L::kSlotBytes;
+    float *obuf = reinterpret_cast<float *>(misc + warp * L::kOBytes);
+    misc += nw * L::kOBytes;
+    StageMeta *meta = reinterpret_cast<StageMeta *>(misc) + warp * S;
+    misc += nw * S * kMetaBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(misc) + warp * S;
+    misc += nw * S * 8;
     uint32_t *warp_tot = reinterpret_cast<uint32_t *>(misc);
     misc += 32 * 4;
     int *ctx_s = reinterpret_cast<int *>(misc);
@@ -151,13 +211,16 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         ctx_s[i] = c;
     }
     if (lane == 0) {
-        for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
     }
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
+    // The merge kernel (if launched) may start launching now; it waits for
+    // this grid's completion before reading any partial state.
+    pdl_launch_dependents();
     __syncthreads();
     {
         const int nthr = blockDim.x;
@@ -227,46 +290,52 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     const uint64_t policy = l2_policy_evict_first();
     const int bs = p.block_size;
     const int Hq = p.num_heads;
+    const int rows = min(bs, kStageTokens);          // rows per TMA box
+    const int nsub = bs >= kStageTokens ? 1 : kStageTokens / bs;  // blocks per stage
 
     // ---- issuer state ----
-    int ij = 0;                  // stage within the issuer's current item
-    int32_t bid = -1;            // lane i: block id i of the issuer's item
-    int fb = 0;                  // first logical block of the issuer's item
+    int ij = 0;                                       // stage within the issuer's item
+    int32_t bid = load_item_blocks(p, ic, P, lane);   // block ids of the issuer's item
+    int32_t bid_next = -1;                            // prefetched ids of the following item
+    bool next_ready = false;
+    int fb = 0;                                       // first logical block of the issuer's item
     bool more = true;
-    uint32_t issued = 0;
+    int islot = 0;
 
     auto issue = [&]() {
-        const int slot = static_cast<int>(issued % kStages);
+        const int slot = islot;
+        islot = (islot + 1 == S) ? 0 : islot + 1;
         uint8_t *sp = slots + slot * L::kSlotBytes;
-        if (ij == 0 && ic.ntok > 0) {
+        if (ij == 0) {
+            if (next_ready) bid = bid_next;
+            next_ready = false;
             fb = (ic.part * P) / bs;
-            const int lb = (ic.part * P + ic.ntok - 1) / bs;
-            bid = (lane <= lb - fb)
-                      ? p.block_tables[static_cast<int64_t>(ic.s) * p.max_blocks_per_seq + fb + lane]
-                      : -1;
+            // Prefetch the next item's block ids; they are used one item later.
+            Cursor nx = ic;
+            nx.advance(ctx_s, prefix, Hkv, P, B);
+            if (nx.start < hi) {
+                bid_next = load_item_blocks(p, nx, P, lane);
+                next_ready = true;
+            }
         }
         const int tok0 = ic.part * P + ij * kStageTokens;
         const int n = ic.ntok > 0 ? min(kStageTokens, ic.ntok - ij * kStageTokens) : 0;
         int mask = n > 0 ? static_cast<int>((1u << n) - 1u) : 0;
-        // Physical blocks of this stage: one when block_size >= 16, two when 8.
-        const int nsub = bs >= kStageTokens ? 1 : kStageTokens / bs;
         int ids[2] = {-1, -1};
         uint32_t bytes = 0;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             if (b < nsub) {
-                const int first = tok0 + b * bs;
                 const bool used = n > b * bs;
-                const int idx = used ? first / bs - fb : 0;
+                const int idx = used ? (tok0 + b * bs) / bs - fb : 0;
                 const int id = __shfl_sync(kFull, bid, idx & 31);
                 if (used) {
                     if (id < 0 || static_cast<int64_t>(id) >= p.num_blocks) {
-                        const int rows = min(bs, kStageTokens);
                         mask &= ~(((1 << rows) - 1) << (b * bs));
                         if (lane == 0) report(p.err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
                     } else {
                         ids[b] = id;
-                        bytes += 2u * L::kHalves * min(bs, kStageTokens) * kRowBytes;
+                        bytes += 2u * L::kHalves * rows * kRowBytes;
                     }
                 }
             }
@@ -279,7 +348,6 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
             m.nst = ic.nst; m.nparts = ic.nparts; m.mask = mask; m.pad = 0;
             meta[slot] = m;
             mbar_arrive_expect_tx(&bars[slot], bytes);
-            const int rows = min(bs, kStageTokens);
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 if (ids[b] >= 0) {
@@ -299,7 +367,6 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
                 bulk_load(sp + L::kQOffset, qsrc, L::kQBytes, &bars[slot]);
             }
         }
-        ++issued;
         if (++ij == ic.nst) {
             ij = 0;
             ic.advance(ctx_s, prefix, Hkv, P, B);
@@ -307,239 +374,280 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         }
     };
 
-    // ---- consumer state ----
-    const int t = lane & 15;      // QK: token of this lane
-    const int hh = lane >> 4;     // QK: which half of the dims
-    float m_run[G], l_lane[G], acc[G][L::kDimsPerLane];
+    // ---- consumer state (mma.sync fragments; g = lane / 4, t = lane % 4) ----
+    // QK:  C[token][head] = K[token][:] . q[head][:]   (M = 16 tokens, N = 8 heads,
+    //      K = 16 dims per step); lane holds tokens g, g+8 of heads 2t, 2t+1.
+    // PV:  O^T[dim][head] += V^T[dim][token] p[token][head] (M = 16 dims per tile,
+    //      N = 8 heads, K = 16 tokens); lane holds dims g, g+8 of heads 2t, 2t+1.
+    // Heads >= G are padding: their query fragments are zero and their logits
+    // are masked, so they never contribute.
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t sm_base = smem_addr(slots);
+    uint32_t qf[KS][2];          // query B fragments for the item
+    float acc[MT][4];            // O^T accumulators
+    float m_run[2], l_run[2];    // running max (log2 domain) and sum, heads 2t, 2t+1
 
-    for (int k = 0; k < kStages && more; ++k) issue();
+    int inflight = 0;
+    for (int k = 0; k < S && more; ++k) {
+        issue();
+        ++inflight;
+    }
 
-    uint32_t consumed = 0;
-    while (consumed < issued) {
-        const int slot = static_cast<int>(consumed % kStages);
-        const uint8_t *sp = slots + slot * L::kSlotBytes;
-        if (!mbar_wait_bounded(&bars[slot], (consumed / kStages) & 1u)) {
+    int cslot = 0;
+    uint32_t cphase = 0;
+    while (inflight > 0) {
+        const int slot = cslot;
+        uint8_t *sp = slots + slot * L::kSlotBytes;
+        const uint32_t sa = sm_base + slot * L::kSlotBytes;
+        if (!mbar_try_wait(&bars[slot], cphase) && !mbar_wait_bounded(&bars[slot], cphase)) {
             if (lane == 0) report(p.err_flag, 0x10 /* PA_FLAG_TIMEOUT */);
             return;
+        }
+        if (++cslot == S) {
+            cslot = 0;
+            cphase ^= 1u;
         }
         const StageMeta m = meta[slot];
 
         if (m.j == 0) {
-            // New item: widen the query to fp32, pre-scaled into the log2 domain.
-            const uint16_t *qh = reinterpret_cast<const uint16_t *>(sp + L::kQOffset);
+            // New item: the query's B fragments straight from the slot (16-bit).
+            const uint32_t *qw = reinterpret_cast<const uint32_t *>(sp + L::kQOffset);
 #pragma unroll
-            for (int k = 0; k < G * D / 64; ++k) {
-                const int e = 2 * (lane + 32 * k);  // element pair (e, e+1)
-                const int g = e / D, d = e % D;
-                const float2 f = Cvt::to_float2(*reinterpret_cast<const uint32_t *>(qh + e));
-                float *dst = q32 + g * L::kQStride + d + (d >= 64 ? 4 : 0);
-                dst[0] = f.x * p.scale_log2;
-                dst[1] = f.y * p.scale_log2;
+            for (int ks = 0; ks < KS; ++ks) {
+                qf[ks][0] = g < G ? qw[(g * D + ks * 16 + 2 * t) >> 1] : 0u;
+                qf[ks][1] = g < G ? qw[(g * D + ks * 16 + 2 * t + 8) >> 1] : 0u;
             }
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                m_run[g] = -INFINITY;
-                l_lane[g] = 0.f;
+            for (int e = 0; e < 2; ++e) {
+                m_run[e] = -INFINITY;
+                l_run[e] = 0.f;
+            }
 #pragma unroll
-                for (int i = 0; i < L::kDimsPerLane; ++i) acc[g][i] = 0.f;
+            for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        }
+
+        // ---- QK^T: 16 tokens x 8 heads, two accumulators over the dim steps ----
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int j = lane >> 3, r = lane & 7;
+            const int tok = r + 8 * (j & 1);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int ch = 2 * ks + (j >> 1);
+                uint32_t a[4];
+                ldsm_x4(a, sa + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
+                mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
+            }
+        }
+        // x[i]: i = 0 (token g, head 2t), 1 (g, 2t+1), 2 (g+8, 2t), 3 (g+8, 2t+1)
+        float x[4];
+        {
+            const bool v_lo = (m.mask >> g) & 1, v_hi = (m.mask >> (g + 8)) & 1;
+            const bool h0 = 2 * t < G, h1 = 2 * t + 1 < G;
+            const float sc = p.scale_log2;
+            x[0] = (v_lo && h0) ? (c[0][0] + c[1][0]) * sc : -INFINITY;
+            x[1] = (v_lo && h1) ? (c[0][1] + c[1][1]) * sc : -INFINITY;
+            x[2] = (v_hi && h0) ? (c[0][2] + c[1][2]) * sc : -INFINITY;
+            x[3] = (v_hi && h1) ? (c[0][3] + c[1][3]) * sc : -INFINITY;
+        }
+        float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx[0] = fmaxf(mx[0], __shfl_xor_sync(kFull, mx[0], o));
+            mx[1] = fmaxf(mx[1], __shfl_xor_sync(kFull, mx[1], o));
+        }
+        // Lazy rescaling: keep the running reference max unless a new logit
+        // exceeds it by more than 2^8 (weights stay <= 256, exact in fp32).
+        const bool need = mx[0] > m_run[0] + 8.f || mx[1] > m_run[1] + 8.f;
+        if (__any_sync(kFull, need)) {
+            float alpha[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float m_new = fmaxf(m_run[e], mx[e]);
+                alpha[e] = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run[e] - m_new);
+                m_run[e] = m_new;
+                l_run[e] *= alpha[e];
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[mt][0] *= alpha[0];
+                acc[mt][1] *= alpha[1];
+                acc[mt][2] *= alpha[0];
+                acc[mt][3] *= alpha[1];
+            }
+        }
+        const float mu0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+        const float mu1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
+        const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
+        const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
+        l_run[0] += p0 + p2;
+        l_run[1] += p1 + p3;
+
+        // ---- P as the PV B fragment: lane needs p(token 2t|2t+1|2t+8|2t+9, head g) ----
+        uint32_t bhi[2], blo[2];
+        {
+            const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
+            const bool odd = g & 1;
+            const float a0 = __shfl_sync(kFull, p0, srcA), a1 = __shfl_sync(kFull, p1, srcA);
+            const float a2 = __shfl_sync(kFull, p2, srcA), a3 = __shfl_sync(kFull, p3, srcA);
+            const float b0 = __shfl_sync(kFull, p0, srcB), b1 = __shfl_sync(kFull, p1, srcB);
+            const float b2 = __shfl_sync(kFull, p2, srcB), b3 = __shfl_sync(kFull, p3, srcB);
+            const float w[4] = {odd ? a1 : a0, odd ? b1 : b0, odd ? a3 : a2, odd ? b3 : b2};
+            // Split each weight into a 16-bit high part and a 16-bit residual,
+            // so the tensor-core product keeps ~16 significant bits of p.
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                bhi[k] = pack2<BF16>(w[2 * k], w[2 * k + 1]);
+                const float2 h = Cvt::to_float2(bhi[k]);
+                blo[k] = pack2<BF16>(w[2 * k] - h.x, w[2 * k + 1] - h.y);
+            }
+        }
+
+        // ---- PV over the stage; rows past the context are zeroed first ----
+        const uint32_t va = sa + L::kVOffset;
+        if (m.mask != 0xffff) {
+            // Stale rows (past the context, or of a skipped block) may hold
+            // NaN; 0 * NaN would poison the tensor-core sums, so clear them.
+            uint8_t *vt = sp + L::kVOffset;
+#pragma unroll
+            for (int k = 0; k < kStageTokens * L::kHalves * 8 / 32; ++k) {
+                const int q16 = lane + 32 * k;                // 16-byte chunk index
+                const int row = (q16 >> 3) % kStageTokens;    // 8 chunks per 128-byte row
+                if (!((m.mask >> row) & 1))
+                    *reinterpret_cast<uint4 *>(vt + q16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+        {
+            const int j = lane >> 3, r = lane & 7;
+            const int tok = r + 8 * (j >> 1);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int ch = 2 * mt + (j & 1);
+                uint32_t a[4];
+                ldsm_x4_trans(a, va + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
+                mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
+                mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+            }
+        }
+
+        // ---- item end: output (or partial state) staged through shared memory ----
+        if (m.j == m.nst - 1) {
+            float lt[2] = {l_run[0], l_run[1]};
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                lt[0] += __shfl_xor_sync(kFull, lt[0], o);
+                lt[1] += __shfl_xor_sync(kFull, lt[1], o);
+            }
+            const bool final_out = m.nparts == 1;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = 2 * t + e;
+                if (h < G) {
+                    const float s = final_out ? (lt[e] > 0.f ? 1.f / lt[e] : 0.f) : 1.f;
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        obuf[h * L::kOStride + mt * 16 + g] = acc[mt][e] * s;
+                        obuf[h * L::kOStride + mt * 16 + g + 8] = acc[mt][2 + e] * s;
+                    }
+                }
+            }
+            __syncwarp();
+            const int d0 = lane * DPL;
+            if (final_out) {
+                const int64_t orow0 = static_cast<int64_t>(m.s) * Hq + m.kvh * G;
+#pragma unroll
+                for (int h = 0; h < G; ++h) store_row<D>(p.out, p.out_dtype, (orow0 + h) * D + d0, obuf + h * L::kOStride + d0);
+            } else {
+                const int64_t slot_id = (static_cast<int64_t>(m.s) * Hkv + m.kvh) * p.max_partitions + m.part;
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    store_row<D>(p.ws_acc, 2, (slot_id * G + h) * D + d0, obuf + h * L::kOStride + d0);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int h = 2 * t + e;
+                    if (g == 0 && h < G)
+                        *reinterpret_cast<float2 *>(p.ws_ml + (slot_id * G + h) * 2) = make_float2(m_run[e], lt[e]);
+                }
             }
             __syncwarp();
         }
 
-        // ---- QK^T for the stage's 16 tokens ----
-        float x[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) x[g] = 0.f;
-#pragma unroll
-        for (int i = 0; i < L::kChunksPerLane; ++i) {
-            const int c = hh * L::kChunksPerLane + i;
-            const int hr = c >> 3, cc = c & 7;
-            const uint4 kw = *reinterpret_cast<const uint4 *>(sp + hr * kRegionBytes + t * kRowBytes +
-                                                              ((cc ^ (t & 7)) << 4));
-            const float2 k0 = Cvt::to_float2(kw.x), k1 = Cvt::to_float2(kw.y);
-            const float2 k2 = Cvt::to_float2(kw.z), k3 = Cvt::to_float2(kw.w);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float *qp = q32 + g * L::kQStride + c * 8 + (hr ? 4 : 0);
-                const float4 qa = *reinterpret_cast<const float4 *>(qp);
-                const float4 qb = *reinterpret_cast<const float4 *>(qp + 4);
-                float a = x[g];
-                a = fmaf(qa.x, k0.x, a); a = fmaf(qa.y, k0.y, a);
-                a = fmaf(qa.z, k1.x, a); a = fmaf(qa.w, k1.y, a);
-                a = fmaf(qb.x, k2.x, a); a = fmaf(qb.y, k2.y, a);
-                a = fmaf(qb.z, k3.x, a); a = fmaf(qb.w, k3.y, a);
-                x[g] = a;
-            }
-        }
-        const bool valid = (m.mask >> t) & 1;
-        float pr[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            if (L::kHalves * 8 > L::kChunksPerLane) x[g] += __shfl_xor_sync(kFull, x[g], 16);
-            const float xv = valid ? x[g] : -INFINITY;
-            float mt = xv;
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
-            const float m_new = fmaxf(m_run[g], mt);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = fast_exp2(m_run[g] - m_use);
-            pr[g] = fast_exp2(xv - m_use);
-            l_lane[g] = l_lane[g] * alpha + pr[g];
-#pragma unroll
-            for (int i = 0; i < L::kDimsPerLane; ++i) acc[g][i] *= alpha;
-            m_run[g] = m_new;
-        }
-
-        // ---- PV: lane owns kDimsPerLane consecutive output dims ----
-        const uint8_t *vt = sp + L::kVOffset;
-#pragma unroll
-        for (int tt = 0; tt < kStageTokens; ++tt) {
-            if (!((m.mask >> tt) & 1)) continue;
-            float pt[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) pt[g] = __shfl_sync(kFull, pr[g], tt);
-            if constexpr (D == 128) {
-                const int hr = lane >> 4, cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
-                const uint2 vw = *reinterpret_cast<const uint2 *>(
-                    vt + hr * kRegionBytes + tt * kRowBytes + ((cc ^ (tt & 7)) << 4) + sub);
-                const float2 v0 = Cvt::to_float2(vw.x), v1 = Cvt::to_float2(vw.y);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    acc[g][0] = fmaf(pt[g], v0.x, acc[g][0]);
-                    acc[g][1] = fmaf(pt[g], v0.y, acc[g][1]);
-                    acc[g][2] = fmaf(pt[g], v1.x, acc[g][2]);
-                    acc[g][3] = fmaf(pt[g], v1.y, acc[g][3]);
-                }
-            } else {
-                const int cc = lane >> 2, sub = (lane & 3) * 4;
-                const uint32_t vw = *reinterpret_cast<const uint32_t *>(
-                    vt + tt * kRowBytes + ((cc ^ (tt & 7)) << 4) + sub);
-                const float2 v0 = Cvt::to_float2(vw);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    acc[g][0] = fmaf(pt[g], v0.x, acc[g][0]);
-                    acc[g][1] = fmaf(pt[g], v0.y, acc[g][1]);
-                }
-            }
-        }
-
-        // ---- item end: write the output or the partial state ----
-        if (m.j == m.nst - 1) {
-            float l_tot[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float v = l_lane[g];
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
-                l_tot[g] = v;
-            }
-            const int d0 = lane * L::kDimsPerLane;
-            const int64_t orow0 = static_cast<int64_t>(m.s) * Hq + m.kvh * G;
-            auto store_out = [&](int g, const float *o) {
-                const int64_t off = (orow0 + g) * D + d0;
-                if (p.out_dtype == 2) {
-                    float *dst = static_cast<float *>(p.out) + off;
-                    if constexpr (L::kDimsPerLane == 4)
-                        *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-                    else
-                        *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
-                } else {
-                    uint16_t h[L::kDimsPerLane];
-#pragma unroll
-                    for (int i = 0; i < L::kDimsPerLane; ++i)
-                        h[i] = p.out_dtype == 1 ? float_to_bf16_bits(o[i]) : float_to_f16_bits(o[i]);
-                    uint16_t *dst = static_cast<uint16_t *>(p.out) + off;
-                    if constexpr (L::kDimsPerLane == 4)
-                        *reinterpret_cast<uint2 *>(dst) =
-                            make_uint2(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16));
-                    else
-                        *reinterpret_cast<uint32_t *>(dst) = h[0] | (uint32_t(h[1]) << 16);
-                }
-            };
-            if (m.nparts == 1) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float inv = l_tot[g] > 0.f ? 1.f / l_tot[g] : 0.f;
-                    float o[L::kDimsPerLane];
-#pragma unroll
-                    for (int i = 0; i < L::kDimsPerLane; ++i) o[i] = acc[g][i] * inv;
-                    store_out(g, o);
-                }
-            } else {
-                const int64_t pair = static_cast<int64_t>(m.s) * Hkv + m.kvh;
-                const int64_t base = pair * p.max_partitions;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float *a = p.ws_acc + ((base + m.part) * G + g) * D + d0;
-                    if constexpr (L::kDimsPerLane == 4)
-                        *reinterpret_cast<float4 *>(a) =
-                            make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-                    else
-                        *reinterpret_cast<float2 *>(a) = make_float2(acc[g][0], acc[g][1]);
-                    if (lane == 0)
-                        *reinterpret_cast<float2 *>(p.ws_ml + ((base + m.part) * G + g) * 2) =
-                            make_float2(m_run[g], l_tot[g]);
-                }
-                __threadfence();
-                __syncwarp();
-                uint32_t ticket = 0;
-                if (lane == 0) ticket = atomicAdd(p.counters + pair, 1u);
-                ticket = __shfl_sync(kFull, ticket, 0);
-                if (ticket == static_cast<uint32_t>(m.nparts - 1)) {
-                    // Last partition to finish: merge all of them in order.
-                    if (lane == 0) p.counters[pair] = 0u;
-                    __threadfence();
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        float M = -INFINITY;
-                        for (int j = 0; j < m.nparts; ++j) {
-                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-                                p.ws_ml + ((base + j) * G + g) * 2));
-                            M = fmaxf(M, ml.x);
-                        }
-                        float Lsum = 0.f, o[L::kDimsPerLane];
-#pragma unroll
-                        for (int i = 0; i < L::kDimsPerLane; ++i) o[i] = 0.f;
-                        for (int j = 0; j < m.nparts; ++j) {
-                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-                                p.ws_ml + ((base + j) * G + g) * 2));
-                            const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-                            Lsum = fmaf(ml.y, w, Lsum);
-                            const float *a = p.ws_acc + ((base + j) * G + g) * D + d0;
-                            if constexpr (L::kDimsPerLane == 4) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(a));
-                                o[0] = fmaf(v.x, w, o[0]); o[1] = fmaf(v.y, w, o[1]);
-                                o[2] = fmaf(v.z, w, o[2]); o[3] = fmaf(v.w, w, o[3]);
-                            } else {
-                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(a));
-                                o[0] = fmaf(v.x, w, o[0]); o[1] = fmaf(v.y, w, o[1]);
-                            }
-                        }
-                        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-#pragma unroll
-                        for (int i = 0; i < L::kDimsPerLane; ++i) o[i] *= inv;
-                        store_out(g, o);
-                    }
-                }
-            }
-        }
-
-        ++consumed;
+        --inflight;
         if (more) {
             fence_proxy_async_smem();
             __syncwarp();
             issue();
+            ++inflight;
         } else {
             __syncwarp();
         }
     }
 }
 
+// Merge of split sequences: one warp per (sequence, KV head) with more than
+// one partition combines the partial states (m_j, l_j, acc_j) in partition
+// order:  M = max_j m_j,  out = sum_j acc_j 2^(m_j - M) / sum_j l_j 2^(m_j - M).
+// Launched after the decode kernel with programmatic dependent launch.
 template <int D, int G>
-size_t smem_for(int warps, int num_seqs) {
+__global__ void __launch_bounds__(256)
+    paged_decode_merge_kernel(const __grid_constant__ DecodeParams p) {
+    pdl_wait();
+    constexpr int DPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t pair = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int Hkv = p.num_kv_heads;
+    if (pair >= static_cast<int64_t>(p.num_seqs) * Hkv) return;
+    const int s = static_cast<int>(pair / Hkv), kvh = static_cast<int>(pair % Hkv);
+    int ctx = p.context_lens[s];
+    if (ctx < 0 || ctx > p.max_context_len) ctx = 0;
+    const int np = ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1;
+    if (np <= 1) return;
+    const int64_t base = pair * p.max_partitions;
+    const int d0 = lane * DPL;
+    for (int h = 0; h < G; ++h) {
+        const float *mlh = p.ws_ml + (base * G + h) * 2;
+        float mx = -INFINITY;
+        for (int j = lane; j < np; j += 32) mx = fmaxf(mx, __ldcg(mlh + static_cast<int64_t>(j) * G * 2));
+        const float M = warp_max(mx);
+        float Lp = 0.f, o[DPL];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+        for (int j0 = 0; j0 < np; j0 += 32) {
+            const int j = j0 + lane;
+            float w = 0.f;
+            if (j < np) {
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(mlh + static_cast<int64_t>(j) * G * 2));
+                w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+                Lp = fmaf(ml.y, w, Lp);
+            }
+            const int cnt = min(32, np - j0);
+#pragma unroll 4
+            for (int jj = 0; jj < cnt; ++jj) {
+                const float wj = __shfl_sync(kFull, w, jj);
+                const float *ap = p.ws_acc + ((base + j0 + jj) * G + h) * D + d0;
+                if constexpr (DPL == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(ap));
+                    o[0] = fmaf(v.x, wj, o[0]); o[1] = fmaf(v.y, wj, o[1]);
+                    o[2] = fmaf(v.z, wj, o[2]); o[3] = fmaf(v.w, wj, o[3]);
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(ap));
+                    o[0] = fmaf(v.x, wj, o[0]); o[1] = fmaf(v.y, wj, o[1]);
+                }
+            }
+        }
+        const float Lsum = warp_sum(Lp);
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[i] *= inv;
+        store_row<D>(p.out, p.out_dtype, (static_cast<int64_t>(s) * p.num_heads + kvh * G + h) * D + d0, o);
+    }
+}
+
+template <int D, int G>
+size_t smem_for(int warps, int stages, int num_seqs) {
     using L = Layout<D, G>;
-    size_t per_warp = static_cast<size_t>(kStages) * L::kSlotBytes + L::kQ32Bytes +
-                      kStages * kMetaBytes + kStages * 8;
+    size_t per_warp = static_cast<size_t>(stages) * (L::kSlotBytes + kMetaBytes + 8) + L::kOBytes;
     return 1024 + per_warp * warps + 32 * 4 + 4 * static_cast<size_t>(num_seqs) +
            4 * (static_cast<size_t>(num_seqs) + 1);
 }
@@ -552,7 +660,21 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtenso
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, warps * 32, smem, stream>>>(p, tk, tv);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.max_partitions <= 1) return e;
+    // Merge of split sequences, chained with programmatic dependent launch.
+    const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((pairs + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel<D, G>, p);
 }
 
 template <int D, int G>
@@ -577,21 +699,21 @@ cudaError_t launch_g(const DecodeParams &p, int group, bool bf16, const CUtensor
 }
 
 template <int D>
-size_t smem_g(int group, int warps, int num_seqs) {
+size_t smem_g(int group, int warps, int stages, int num_seqs) {
     switch (group) {
-        case 1: return smem_for<D, 1>(warps, num_seqs);
-        case 2: return smem_for<D, 2>(warps, num_seqs);
-        case 4: return smem_for<D, 4>(warps, num_seqs);
-        case 8: return smem_for<D, 8>(warps, num_seqs);
+        case 1: return smem_for<D, 1>(warps, stages, num_seqs);
+        case 2: return smem_for<D, 2>(warps, stages, num_seqs);
+        case 4: return smem_for<D, 4>(warps, stages, num_seqs);
+        case 8: return smem_for<D, 8>(warps, stages, num_seqs);
         default: return 0;
     }
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int head_dim, int group, int warps, int num_seqs) {
-    return head_dim == 64 ? smem_g<64>(group, warps, num_seqs)
-                          : smem_g<128>(group, warps, num_seqs);
+size_t decode_smem_bytes(int head_dim, int group, int warps, int stages, int num_seqs) {
+    return head_dim == 64 ? smem_g<64>(group, warps, stages, num_seqs)
+                          : smem_g<128>(group, warps, stages, num_seqs);
 }
 
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, bool bf16,

@@ -69,12 +69,9 @@ PA_EXPORT pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype, const void 
     if (num_seqs == 0) return PA_OK;
     void *scratch = scratch_on_current_device();
     if (scratch == nullptr) return PA_ERR_CUDA;
-    // The array keeps the previous call's contents.  The completion tickets -
-    // one uint32 per (sequence, KV head) at the start of the workspace - must
-    // start at zero; partial results need no initial value.
-    const size_t tickets = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(uint32_t);
-    if (cudaMemsetAsync(scratch, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return PA_ERR_CUDA;
+    // The array keeps the previous call's contents; nothing in the decode
+    // workspace needs an initial value (every partial state is written before
+    // the merge kernel reads it), so no clearing is needed.
     return pa_decode(out, out_dtype, query, k_cache, v_cache, kv_dtype, block_tables,
                      max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size, scratch,

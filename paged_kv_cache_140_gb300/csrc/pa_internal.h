@@ -10,8 +10,11 @@ namespace pa {
 // Tokens per pipeline stage of the decode kernel: one stage brings 16 K rows
 // and 16 V rows of one KV head into shared memory.
 constexpr int kStageTokens = 16;
-// Stages in flight per warp (ring depth).
-constexpr int kStages = 3;
+// Default ring depth (shared-memory slots) per warp and warps per CTA for
+// 128-dim heads: 2 x 8 measured best on GB300 for every workload tried (13B,
+// 7B, GQA, prefix sharing); deeper rings or more warps only add L2/HBM queueing.
+constexpr int kDefaultStages = 2;
+constexpr int kDefaultWarps128 = 8;
 
 struct DecodeParams {
     void *out;
@@ -29,15 +32,15 @@ struct DecodeParams {
     float scale_log2;            // softmax scale * log2(e)
     int partition_size;          // tokens per partition, multiple of 16
     int max_partitions;          // partition slots per (seq, KV head) in the workspace
-    uint32_t *counters;          // [B * Hkv] completion tickets (zero between calls)
     float *ws_ml;                // [B * Hkv * max_partitions, G, 2]  (max, sum)
     float *ws_acc;               // [B * Hkv * max_partitions, G, D]
     int *err_flag;
+    int stages;                  // shared-memory slots per warp (ring depth)
 };
 
-// Shared memory the decode kernel needs for `warps` warps and `num_seqs`
-// sequences (including alignment slack).
-size_t decode_smem_bytes(int head_dim, int group, int warps, int num_seqs);
+// Shared memory the decode kernel needs for `warps` warps with `stages`
+// slots each and `num_seqs` sequences (including alignment slack).
+size_t decode_smem_bytes(int head_dim, int group, int warps, int stages, int num_seqs);
 
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, bool bf16,
                           const CUtensorMap &tmap_k, const CUtensorMap &tmap_v, int grid,
