@@ -202,14 +202,6 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     uint32_t *prefix = reinterpret_cast<uint32_t *>(misc + 4 * B);
 
     // ---- CTA prologue: validated context lengths and the work prefix ----
-    for (int i = threadIdx.x; i < B; i += blockDim.x) {
-        int c = p.context_lens[i];
-        if (c < 0 || c > p.max_context_len) {
-            if (blockIdx.x == 0) report(p.err_flag, 0x4 /* PA_FLAG_BAD_CONTEXT_LEN */);
-            c = 0;
-        }
-        ctx_s[i] = c;
-    }
     if (lane == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
@@ -217,6 +209,18 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
+    }
+    // Launched with programmatic dependent launch: wait for the previous
+    // kernel in the stream (e.g. reshape_and_cache writing this step's rows)
+    // before reading any input.
+    pdl_wait();
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+        int c = p.context_lens[i];
+        if (c < 0 || c > p.max_context_len) {
+            if (blockIdx.x == 0) report(p.err_flag, 0x4 /* PA_FLAG_BAD_CONTEXT_LEN */);
+            c = 0;
+        }
+        ctx_s[i] = c;
     }
     // The merge kernel (if launched) may start launching now; it waits for
     // this grid's completion before reading any partial state.
@@ -585,19 +589,24 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     }
 }
 
-// Merge of split sequences: one warp per (sequence, KV head) with more than
-// one partition combines the partial states (m_j, l_j, acc_j) in partition
-// order:  M = max_j m_j,  out = sum_j acc_j 2^(m_j - M) / sum_j l_j 2^(m_j - M).
-// Launched after the decode kernel with programmatic dependent launch.
+// Merge of split sequences: one warp per (sequence, KV head, query head) with
+// more than one partition combines the partial states (m_j, l_j, acc_j) in
+// partition order:  M = max_j m_j,
+//   out = sum_j acc_j 2^(m_j - M) / sum_j l_j 2^(m_j - M).
+// Lanes split the partitions for (m, l) and the head dims for acc; the acc
+// loads of eight partitions are in flight at once.  Launched after the
+// decode kernel with programmatic dependent launch.
 template <int D, int G>
 __global__ void __launch_bounds__(256)
     paged_decode_merge_kernel(const __grid_constant__ DecodeParams p) {
     pdl_wait();
     constexpr int DPL = D / 32;
     const int lane = threadIdx.x & 31;
-    const int64_t pair = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t task = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int Hkv = p.num_kv_heads;
-    if (pair >= static_cast<int64_t>(p.num_seqs) * Hkv) return;
+    if (task >= static_cast<int64_t>(p.num_seqs) * Hkv * G) return;
+    const int h = static_cast<int>(task % G);
+    const int64_t pair = task / G;
     const int s = static_cast<int>(pair / Hkv), kvh = static_cast<int>(pair % Hkv);
     int ctx = p.context_lens[s];
     if (ctx < 0 || ctx > p.max_context_len) ctx = 0;
@@ -605,43 +614,54 @@ __global__ void __launch_bounds__(256)
     if (np <= 1) return;
     const int64_t base = pair * p.max_partitions;
     const int d0 = lane * DPL;
-    for (int h = 0; h < G; ++h) {
-        const float *mlh = p.ws_ml + (base * G + h) * 2;
-        float mx = -INFINITY;
-        for (int j = lane; j < np; j += 32) mx = fmaxf(mx, __ldcg(mlh + static_cast<int64_t>(j) * G * 2));
-        const float M = warp_max(mx);
-        float Lp = 0.f, o[DPL];
+    const float *mlh = p.ws_ml + (base * G + h) * 2;
+    float mx = -INFINITY;
+    for (int j = lane; j < np; j += 32) mx = fmaxf(mx, __ldcg(mlh + static_cast<int64_t>(j) * G * 2));
+    const float M = warp_max(mx);
+    float Lp = 0.f, o[DPL];
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) o[i] = 0.f;
-        for (int j0 = 0; j0 < np; j0 += 32) {
-            const int j = j0 + lane;
-            float w = 0.f;
-            if (j < np) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(mlh + static_cast<int64_t>(j) * G * 2));
-                w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-                Lp = fmaf(ml.y, w, Lp);
-            }
-            const int cnt = min(32, np - j0);
-#pragma unroll 4
-            for (int jj = 0; jj < cnt; ++jj) {
-                const float wj = __shfl_sync(kFull, w, jj);
-                const float *ap = p.ws_acc + ((base + j0 + jj) * G + h) * D + d0;
-                if constexpr (DPL == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(ap));
-                    o[0] = fmaf(v.x, wj, o[0]); o[1] = fmaf(v.y, wj, o[1]);
-                    o[2] = fmaf(v.z, wj, o[2]); o[3] = fmaf(v.w, wj, o[3]);
+    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+    for (int j0 = 0; j0 < np; j0 += 32) {
+        const int j = j0 + lane;
+        float w = 0.f;
+        if (j < np) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(mlh + static_cast<int64_t>(j) * G * 2));
+            w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+            Lp = fmaf(ml.y, w, Lp);
+        }
+        const int cnt = min(32, np - j0);
+        const float *ap0 = p.ws_acc + ((base + j0) * G + h) * D + d0;
+        for (int jb = 0; jb < cnt; jb += 8) {
+            float v[8][DPL];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (jb + u < cnt) {
+                    const float *ap = ap0 + static_cast<int64_t>(jb + u) * G * D;
+                    if constexpr (DPL == 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(ap));
+                        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                    } else {
+                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(ap));
+                        v[u][0] = x.x; v[u][1] = x.y;
+                    }
                 } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(ap));
-                    o[0] = fmaf(v.x, wj, o[0]); o[1] = fmaf(v.y, wj, o[1]);
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) v[u][i] = 0.f;
                 }
             }
-        }
-        const float Lsum = warp_sum(Lp);
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) o[i] *= inv;
-        store_row<D>(p.out, p.out_dtype, (static_cast<int64_t>(s) * p.num_heads + kvh * G + h) * D + d0, o);
+            for (int u = 0; u < 8; ++u) {
+                const float wj = __shfl_sync(kFull, w, (jb + u) & 31);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) o[i] = fmaf(v[u][i], wj, o[i]);
+            }
+        }
     }
+    const float Lsum = warp_sum(Lp);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] *= inv;
+    store_row<D>(p.out, p.out_dtype, (static_cast<int64_t>(s) * p.num_heads + kvh * G + h) * D + d0, o);
 }
 
 template <int D, int G>
@@ -652,6 +672,25 @@ size_t smem_for(int warps, int stages, int num_seqs) {
            4 * (static_cast<size_t>(num_seqs) + 1);
 }
 
+// Launch `kern` with programmatic stream serialization: it may start while
+// the previous kernel in the stream finishes, and waits (griddepcontrol.wait)
+// before reading anything that kernel wrote.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int D, int G, bool BF16>
 cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                      int grid, int warps, size_t smem, cudaStream_t stream) {
@@ -659,22 +698,12 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtenso
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, warps * 32, smem, stream>>>(p, tk, tv);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid), dim3(warps * 32), smem, stream, p, tk, tv);
     if (e != cudaSuccess || p.max_partitions <= 1) return e;
-    // Merge of split sequences, chained with programmatic dependent launch.
-    const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((pairs + 7) / 8));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel<D, G>, p);
+    // Merge of split sequences: one warp per (sequence, KV head, query head).
+    const int64_t tasks = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * G;
+    return launch_pdl(paged_decode_merge_kernel<D, G>, dim3(static_cast<unsigned>((tasks + 7) / 8)),
+                      dim3(256), 0, stream, p);
 }
 
 template <int D, int G>
