@@ -64,6 +64,7 @@ bool device_info(DeviceInfo &info) {
 struct Tuning {
     int stages = 0;  // 0: default
     int warps = 0;
+    int interleave = 1;
 };
 
 int env_int(const char *name, int lo, int hi) {
@@ -78,6 +79,8 @@ const Tuning &tuning() {
         Tuning r;
         r.stages = env_int("PA_DECODE_STAGES", 2, 8);
         r.warps = env_int("PA_DECODE_WARPS", 1, 16);
+        const char *il = getenv("PA_DECODE_INTERLEAVE");
+        r.interleave = (il != nullptr && il[0] == '0') ? 0 : 1;
         return r;
     }();
     return t;
@@ -308,6 +311,7 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
     p.ws_acc = w.bytes ? reinterpret_cast<float *>(ws + w.acc_off) : nullptr;
     p.err_flag = err_flag;
     p.stages = stages;
+    p.interleave = tune.interleave;
 
     cudaError_t e = pa::launch_decode(p, head_dim, G, kv_dtype == PA_BF16, tk, tv, dev.sms, warps,
                                       smem_used, static_cast<cudaStream_t>(stream));

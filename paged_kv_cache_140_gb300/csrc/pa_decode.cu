@@ -256,12 +256,18 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         __syncthreads();
     }
 
-    // ---- this warp's range of work [lo, hi) in stage units ----
+    // ---- the range of work [lo, hi) in stage units ----
+    // Interleaved (default): the CTA owns a contiguous range and its warps take
+    // every nw-th item of it, so at any moment they read neighbouring KV heads
+    // of the same token rows (DRAM locality).  Otherwise each warp owns a
+    // contiguous range of its own.
     const uint32_t total = prefix[B];
-    const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw;
-    const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw + warp;
-    const uint32_t lo = static_cast<uint32_t>(static_cast<uint64_t>(total) * gw / nwarps);
-    const uint32_t hi = static_cast<uint32_t>(static_cast<uint64_t>(total) * (gw + 1) / nwarps);
+    const bool inter = p.interleave != 0;
+    const uint64_t nranges = inter ? gridDim.x : static_cast<uint64_t>(gridDim.x) * nw;
+    const uint64_t rid = inter ? blockIdx.x : static_cast<uint64_t>(blockIdx.x) * nw + warp;
+    const int step = inter ? nw : 1;
+    const uint32_t lo = static_cast<uint32_t>(static_cast<uint64_t>(total) * rid / nranges);
+    const uint32_t hi = static_cast<uint32_t>(static_cast<uint64_t>(total) * (rid + 1) / nranges);
     if (lo >= hi) return;
 
     // First item whose first stage is >= lo.
@@ -289,9 +295,12 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
             ic.advance(ctx_s, prefix, Hkv, P, B);
         }
     }
+    if (inter)
+        for (int k = 0; k < warp; ++k) ic.advance(ctx_s, prefix, Hkv, P, B);
     if (ic.start >= hi) return;
 
     const uint64_t policy = l2_policy_evict_first();
+    const uint64_t keep = l2_policy_evict_last();
     const int bs = p.block_size;
     const int Hq = p.num_heads;
     const int rows = min(bs, kStageTokens);          // rows per TMA box
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
             fb = (ic.part * P) / bs;
             // Prefetch the next item's block ids; they are used one item later.
             Cursor nx = ic;
-            nx.advance(ctx_s, prefix, Hkv, P, B);
+            for (int k = 0; k < step; ++k) nx.advance(ctx_s, prefix, Hkv, P, B);
             if (nx.start < hi) {
                 bid_next = load_item_blocks(p, nx, P, lane);
                 next_ready = true;
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         }
         if (++ij == ic.nst) {
             ij = 0;
-            ic.advance(ctx_s, prefix, Hkv, P, B);
+            for (int k = 0; k < step; ++k) ic.advance(ctx_s, prefix, Hkv, P, B);
             more = ic.start < hi;
         }
     };
@@ -564,14 +573,21 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
                 for (int h = 0; h < G; ++h) store_row<D>(p.out, p.out_dtype, (orow0 + h) * D + d0, obuf + h * L::kOStride + d0);
             } else {
                 const int64_t slot_id = (static_cast<int64_t>(m.s) * Hkv + m.kvh) * p.max_partitions + m.part;
+                // Partials stay in L2 (evict-last) for the merge kernel.
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-                    store_row<D>(p.ws_acc, 2, (slot_id * G + h) * D + d0, obuf + h * L::kOStride + d0);
+                for (int h = 0; h < G; ++h) {
+                    float *dst = p.ws_acc + (slot_id * G + h) * D + d0;
+                    const float *src = obuf + h * L::kOStride + d0;
+                    if constexpr (DPL == 4)
+                        st_global_hint(dst, make_float4(src[0], src[1], src[2], src[3]), keep);
+                    else
+                        st_global_hint(dst, make_float2(src[0], src[1]), keep);
+                }
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int h = 2 * t + e;
                     if (g == 0 && h < G)
-                        *reinterpret_cast<float2 *>(p.ws_ml + (slot_id * G + h) * 2) = make_float2(m_run[e], lt[e]);
+                        st_global_hint(p.ws_ml + (slot_id * G + h) * 2, make_float2(m_run[e], lt[e]), keep);
                 }
             }
             __syncwarp();
@@ -589,76 +605,103 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     }
 }
 
-// Merge of split sequences: one warp per (sequence, KV head, query head) with
-// more than one partition combines the partial states (m_j, l_j, acc_j) in
+// Merge of split sequences: for each (sequence, KV head, query head) with more
+// than one partition, combine the partial states (m_j, l_j, acc_j) in
 // partition order:  M = max_j m_j,
 //   out = sum_j acc_j 2^(m_j - M) / sum_j l_j 2^(m_j - M).
-// Lanes split the partitions for (m, l) and the head dims for acc; the acc
-// loads of eight partitions are in flight at once.  Launched after the
-// decode kernel with programmatic dependent launch.
+// `wt` warps share one task (1, 2, 4 or 8; more for long partition lists):
+// each takes a contiguous run of partitions with eight acc loads in flight,
+// and the first folds the runs together in shared memory in run order.
+// Launched after the decode kernel with programmatic dependent launch.
 template <int D, int G>
 __global__ void __launch_bounds__(256)
-    paged_decode_merge_kernel(const __grid_constant__ DecodeParams p) {
+    paged_decode_merge_kernel(const __grid_constant__ DecodeParams p, int wt) {
     pdl_wait();
     constexpr int DPL = D / 32;
-    const int lane = threadIdx.x & 31;
-    const int64_t task = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    __shared__ float red_o[8][D];
+    __shared__ float red_l[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t task = static_cast<int64_t>(blockIdx.x) * (8 / wt) + warp / wt;
+    const int sub = warp % wt;
     const int Hkv = p.num_kv_heads;
-    if (task >= static_cast<int64_t>(p.num_seqs) * Hkv * G) return;
-    const int h = static_cast<int>(task % G);
-    const int64_t pair = task / G;
-    const int s = static_cast<int>(pair / Hkv), kvh = static_cast<int>(pair % Hkv);
-    int ctx = p.context_lens[s];
-    if (ctx < 0 || ctx > p.max_context_len) ctx = 0;
-    const int np = ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1;
-    if (np <= 1) return;
-    const int64_t base = pair * p.max_partitions;
+    bool active = task < static_cast<int64_t>(p.num_seqs) * Hkv * G;
+    int np = 1, s = 0, kvh = 0, h = 0;
+    int64_t pair = 0;
+    if (active) {
+        h = static_cast<int>(task % G);
+        pair = task / G;
+        s = static_cast<int>(pair / Hkv);
+        kvh = static_cast<int>(pair % Hkv);
+        int ctx = p.context_lens[s];
+        if (ctx < 0 || ctx > p.max_context_len) ctx = 0;
+        np = ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1;
+        active = np > 1;
+    }
     const int d0 = lane * DPL;
-    const float *mlh = p.ws_ml + (base * G + h) * 2;
-    float mx = -INFINITY;
-    for (int j = lane; j < np; j += 32) mx = fmaxf(mx, __ldcg(mlh + static_cast<int64_t>(j) * G * 2));
-    const float M = warp_max(mx);
     float Lp = 0.f, o[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) o[i] = 0.f;
-    for (int j0 = 0; j0 < np; j0 += 32) {
-        const int j = j0 + lane;
-        float w = 0.f;
-        if (j < np) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(mlh + static_cast<int64_t>(j) * G * 2));
-            w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-            Lp = fmaf(ml.y, w, Lp);
-        }
-        const int cnt = min(32, np - j0);
-        const float *ap0 = p.ws_acc + ((base + j0) * G + h) * D + d0;
-        for (int jb = 0; jb < cnt; jb += 8) {
-            float v[8][DPL];
+    if (active) {
+        const int64_t base = pair * p.max_partitions;
+        const float *mlh = p.ws_ml + (base * G + h) * 2;
+        float mx = -INFINITY;
+        for (int j = lane; j < np; j += 32) mx = fmaxf(mx, __ldcg(mlh + static_cast<int64_t>(j) * G * 2));
+        const float M = warp_max(mx);
+        const int per = (np + wt - 1) / wt;
+        const int jb = min(np, sub * per), je = min(np, jb + per);
+        for (int j0 = jb; j0 < je; j0 += 32) {
+            const int j = j0 + lane;
+            float w = 0.f;
+            if (j < je) {
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(mlh + static_cast<int64_t>(j) * G * 2));
+                w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+                Lp = fmaf(ml.y, w, Lp);
+            }
+            const int cnt = min(32, je - j0);
+            const float *ap0 = p.ws_acc + ((base + j0) * G + h) * D + d0;
+            for (int u0 = 0; u0 < cnt; u0 += 8) {
+                float v[8][DPL];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (jb + u < cnt) {
-                    const float *ap = ap0 + static_cast<int64_t>(jb + u) * G * D;
-                    if constexpr (DPL == 4) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(ap));
-                        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                for (int u = 0; u < 8; ++u) {
+                    if (u0 + u < cnt) {
+                        const float *ap = ap0 + static_cast<int64_t>(u0 + u) * G * D;
+                        if constexpr (DPL == 4) {
+                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(ap));
+                            v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                        } else {
+                            const float2 x = __ldcg(reinterpret_cast<const float2 *>(ap));
+                            v[u][0] = x.x; v[u][1] = x.y;
+                        }
                     } else {
-                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(ap));
-                        v[u][0] = x.x; v[u][1] = x.y;
-                    }
-                } else {
 #pragma unroll
-                    for (int i = 0; i < DPL; ++i) v[u][i] = 0.f;
+                        for (int i = 0; i < DPL; ++i) v[u][i] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float wj = __shfl_sync(kFull, w, (u0 + u) & 31);
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) o[i] = fmaf(v[u][i], wj, o[i]);
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float wj = __shfl_sync(kFull, w, (jb + u) & 31);
-#pragma unroll
-                for (int i = 0; i < DPL; ++i) o[i] = fmaf(v[u][i], wj, o[i]);
-            }
         }
+        Lp = warp_sum(Lp);
     }
-    const float Lsum = warp_sum(Lp);
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    if (wt > 1) {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) red_o[warp][d0 + i] = o[i];
+        if (lane == 0) red_l[warp] = Lp;
+        __syncthreads();
+        if (!active || sub != 0) return;
+        for (int k = 1; k < wt; ++k) {
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) o[i] += red_o[warp + k][d0 + i];
+            Lp += red_l[warp + k];
+        }
+    } else if (!active) {
+        return;
+    }
+    const float inv = Lp > 0.f ? 1.f / Lp : 0.f;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) o[i] *= inv;
     store_row<D>(p.out, p.out_dtype, (static_cast<int64_t>(s) * p.num_heads + kvh * G + h) * D + d0, o);
@@ -700,10 +743,15 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtenso
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(grid), dim3(warps * 32), smem, stream, p, tk, tv);
     if (e != cudaSuccess || p.max_partitions <= 1) return e;
-    // Merge of split sequences: one warp per (sequence, KV head, query head).
+    // Merge of split sequences: 1-8 warps per (sequence, KV head, query head),
+    // about 16 partitions per warp.
+    int wt = 1;
+    while (wt < 8 && wt * 16 < p.max_partitions) wt *= 2;
     const int64_t tasks = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * G;
-    return launch_pdl(paged_decode_merge_kernel<D, G>, dim3(static_cast<unsigned>((tasks + 7) / 8)),
-                      dim3(256), 0, stream, p);
+    const int64_t per_cta = 8 / wt;
+    return launch_pdl(paged_decode_merge_kernel<D, G>,
+                      dim3(static_cast<unsigned>((tasks + per_cta - 1) / per_cta)), dim3(256), 0,
+                      stream, p, wt);
 }
 
 template <int D, int G>

@@ -36,6 +36,7 @@ struct DecodeParams {
     float *ws_acc;               // [B * Hkv * max_partitions, G, D]
     int *err_flag;
     int stages;                  // shared-memory slots per warp (ring depth)
+    int interleave;              // 1: a CTA's warps take every nw-th item of the CTA's range
 };
 
 // Shared memory the decode kernel needs for `warps` warps with `stages`
