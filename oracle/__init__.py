@@ -7,7 +7,8 @@ imports the product.
 
 Contents:
   * ``pa_oracle.c`` -- fp64 C implementation of reshape_and_cache,
-    copy_blocks, paged attention and the partition-then-merge variant, loaded
+    copy_blocks, paged attention and the partition-then-merge variant, plus
+    the FP8 (e4m3) cache codec, reshape and attention, loaded
     through ctypes (built with gcc on first use, or by ``build()``).
   * ``brute.py`` -- an independent NumPy brute force for tiny inputs.
   * ``accounting.py`` -- the pages' block-count and KV-size formulas.
@@ -56,6 +57,16 @@ def _load():
         lib.oracle_paged_attention_partitioned.argtypes = [P, P, P, P, P, P, P, i32, P, i32, P,
                                                            i32, i32, i32, i32, i32, dbl, i32, i32]
         lib.oracle_paged_attention_partitioned.restype = None
+        lib.oracle_e4m3_encode_array.argtypes = [P, P, i64]
+        lib.oracle_e4m3_encode_array.restype = None
+        lib.oracle_e4m3_decode_array.argtypes = [P, P, i64]
+        lib.oracle_e4m3_decode_array.restype = None
+        f32 = ctypes.c_float
+        lib.oracle_reshape_and_cache_fp8.argtypes = [P, P, i32, P, P, P, i64, i64, i32, i32, i32, f32, f32]
+        lib.oracle_reshape_and_cache_fp8.restype = i64
+        lib.oracle_paged_attention_fp8.argtypes = [P, P, i32, P, P, dbl, dbl, P, i32, P, i32, i32, i32,
+                                                   i32, i32, dbl]
+        lib.oracle_paged_attention_fp8.restype = None
         _lib = lib
     return _lib
 
@@ -149,12 +160,80 @@ def paged_attention_partitioned(q, k_cache, v_cache, dtype: str, block_tables, c
 def decode_step(batch):
     """The whole step on the CPU: copy_blocks, reshape_and_cache, attention.
 
-    ``batch`` is a workloads.Batch.  Returns (out fp64 [B,Hq,D], k_cache_after,
-    v_cache_after)."""
+    ``batch`` is a workloads.Batch (16-bit or e4m3 cache).  Returns
+    (out fp64 [B,Hq,D], k_cache_after, v_cache_after)."""
     kc, vc = batch.k_cache, batch.v_cache
+    fp8 = getattr(batch, "cache_dtype", batch.dtype) == "fp8"
     if len(batch.block_mapping):
-        kc, vc, _ = copy_blocks(kc, vc, batch.block_mapping)
+        kc, vc, _ = (copy_blocks_bytes if fp8 else copy_blocks)(kc, vc, batch.block_mapping)
+    if fp8:
+        kc, vc, _ = reshape_and_cache_fp8(batch.key, batch.value, batch.dtype, kc, vc, batch.slot_mapping,
+                                          batch.k_scale, batch.v_scale)
+        out = paged_attention_fp8(batch.q, batch.dtype, kc, vc, batch.k_scale, batch.v_scale,
+                                  batch.block_tables, batch.context_lens, batch.scale)
+        return out, kc, vc
     kc, vc, _ = reshape_and_cache(batch.key, batch.value, kc, vc, batch.slot_mapping)
     out = paged_attention(batch.q, kc, vc, batch.dtype, batch.block_tables, batch.context_lens,
                           batch.scale)
     return out, kc, vc
+
+
+# ------------------------------------------------------------ FP8 (e4m3) cache
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest e4m3 codes (ties to even, finite values saturate at +-448)."""
+    lib = _load()
+    a = _c(x, np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    lib.oracle_e4m3_encode_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.oracle_e4m3_decode_array(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def reshape_and_cache_fp8(key, value, dtype: str, k_cache, v_cache, slot_mapping, k_scale, v_scale):
+    """Quantise the step's rows (x / scale in fp32, e4m3) into copies of the caches."""
+    lib = _load()
+    kc = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint8, copy=True, order="C")
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    nb, bs, hkv, d = kc.shape
+    bad = lib.oracle_reshape_and_cache_fp8(_ptr(key), _ptr(value), DTYPE_CODE[dtype], _ptr(kc), _ptr(vc),
+                                           _ptr(sm), len(sm), nb, bs, hkv, d, float(k_scale), float(v_scale))
+    return kc, vc, int(bad)
+
+
+def paged_attention_fp8(q, q_dtype: str, k_cache, v_cache, k_scale, v_scale, block_tables,
+                        context_lens, scale) -> np.ndarray:
+    """Paged attention over e4m3 caches (K = code value * k_scale, V alike), fp64."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint8)
+    vc = _c(v_cache, np.uint8)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, bs, hkv, _ = kc.shape
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    lib.oracle_paged_attention_fp8(_ptr(out), _ptr(q), DTYPE_CODE[q_dtype], _ptr(kc), _ptr(vc),
+                                   float(k_scale), float(v_scale), _ptr(bt), bt.shape[1], _ptr(cl), B, Hq,
+                                   hkv, D, bs, float(scale))
+    return out
+
+
+def copy_blocks_bytes(k_cache, v_cache, block_mapping):
+    """copy_blocks for caches of any element size (viewed as 16-bit words)."""
+    kc = np.ascontiguousarray(k_cache)
+    shape = kc.shape
+    k16 = kc.view(np.uint16).reshape(shape[0], shape[1], shape[2], -1)
+    v16 = np.ascontiguousarray(v_cache).view(np.uint16).reshape(k16.shape)
+    a, b, bad = copy_blocks(k16, v16, block_mapping)
+    return a.view(kc.dtype).reshape(shape), b.view(kc.dtype).reshape(shape), bad

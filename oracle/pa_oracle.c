@@ -273,3 +273,140 @@ void oracle_paged_attention_partitioned(double *out, double *part_max, double *p
         }
     }
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 (e4m3, "fn": no infinities, max 448) KV cache.
+ *
+ * The pages list FP8 among vLLM's quantisation options ("LLM推理优化：vLLM
+ * PagedAttention深度解析与工程实践", §八 comparison table).  Readings used here
+ * (the pages give no detail): one scale per tensor for K and one for V; the
+ * cache stores code = e4m3(x / scale) with x widened to fp32, the division in
+ * fp32, rounding to nearest-even and saturation of finite values to +-448
+ * (NaN stays NaN); attention reads K = e4m3_value(code) * k_scale (V alike).
+ * ------------------------------------------------------------------------ */
+
+/* Exact value of an e4m3 code: s eeee mmm, bias 7; e=15,m=7 is NaN. */
+double oracle_e4m3_decode(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xf;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);              /* subnormal: m * 2^-9 */
+    else v = ldexp((double)(8 + m), e - 10);           /* 1.m * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Round a float to the nearest e4m3 code (ties to even), saturating finite
+ * values (and infinities) to +-448; NaN -> 0x7f. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (x != x) return 0x7f;
+    uint8_t sign = (x < 0.0f || (x == 0.0f && signbit(x))) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+    int code;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal grid, step 2^-9; a result of 8 is the smallest normal */
+        code = (int)rint(a / ldexp(1.0, -9));
+    } else {
+        int e;
+        frexp(a, &e);                    /* a = f * 2^e, f in [0.5, 1) */
+        int ue = e - 1;                  /* a in [2^ue, 2^(ue+1)) */
+        double q = rint(a / ldexp(1.0, ue - 3));   /* in [8, 16] */
+        code = ((ue + 7) << 3) + ((int)q - 8);     /* q = 16 carries into the exponent */
+    }
+    if (code > 0x7e) code = 0x7e;
+    return (uint8_t)(sign | code);
+}
+
+static double half_or_bf16(uint16_t bits, int dtype) { return oracle_half_to_double(bits, dtype); }
+
+/* reshape_and_cache into an e4m3 cache: key/value hold 16-bit values of
+ * `dtype`; caches hold one byte per element.  Returns the number of skipped
+ * out-of-range slots (negative slots are padding and skipped silently). */
+int64_t oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value, int dtype,
+                                     uint8_t *k_cache, uint8_t *v_cache,
+                                     const int64_t *slot_mapping, int64_t num_tokens,
+                                     int64_t num_blocks, int block_size,
+                                     int num_kv_heads, int head_dim, float k_scale, float v_scale) {
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    int64_t bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) { ++bad; continue; }
+        for (int64_t i = 0; i < row; ++i) {
+            float kx = (float)half_or_bf16(key[t * row + i], dtype);
+            float vx = (float)half_or_bf16(value[t * row + i], dtype);
+            volatile float kq = kx / k_scale;    /* fp32 division */
+            volatile float vq = vx / v_scale;
+            k_cache[slot * row + i] = oracle_e4m3_encode(kq);
+            v_cache[slot * row + i] = oracle_e4m3_encode(vq);
+        }
+    }
+    return bad;
+}
+
+/* Paged attention over an e4m3 cache: q holds 16-bit values of `q_dtype`;
+ * K_p = e4m3(k_cache) * k_scale, V_p = e4m3(v_cache) * v_scale; otherwise as
+ * oracle_paged_attention (fp64 throughout). */
+void oracle_paged_attention_fp8(double *out, const uint16_t *q, int q_dtype,
+                                const uint8_t *k_cache, const uint8_t *v_cache,
+                                double k_scale, double v_scale,
+                                const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *context_lens, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_dim, int block_size, double scale) {
+    int group = num_heads / num_kv_heads;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int s = 0; s < num_seqs; ++s) {
+        for (int hq = 0; hq < num_heads; ++hq) {
+            double *o = out + ((int64_t)s * num_heads + hq) * head_dim;
+            int n = context_lens[s];
+            for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+            if (n <= 0) continue;
+            int kvh = hq / group;
+            const int32_t *table_row = block_tables + (int64_t)s * max_blocks_per_seq;
+            double *Kg = (double *)malloc(sizeof(double) * (size_t)n * head_dim);
+            double *Vg = (double *)malloc(sizeof(double) * (size_t)n * head_dim);
+            double *x = (double *)malloc(sizeof(double) * (size_t)n);
+            double *qd = (double *)malloc(sizeof(double) * (size_t)head_dim);
+            for (int p = 0; p < n; ++p) {
+                int64_t block = table_row[p / block_size];
+                int64_t offset = p % block_size;
+                int64_t base = ((block * block_size + offset) * num_kv_heads + kvh) * (int64_t)head_dim;
+                for (int d = 0; d < head_dim; ++d) {
+                    Kg[(int64_t)p * head_dim + d] = oracle_e4m3_decode(k_cache[base + d]) * k_scale;
+                    Vg[(int64_t)p * head_dim + d] = oracle_e4m3_decode(v_cache[base + d]) * v_scale;
+                }
+            }
+            for (int d = 0; d < head_dim; ++d)
+                qd[d] = oracle_half_to_double(q[((int64_t)s * num_heads + hq) * head_dim + d], q_dtype);
+            double m = -INFINITY;
+            for (int p = 0; p < n; ++p) {
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d) dot += qd[d] * Kg[(int64_t)p * head_dim + d];
+                x[p] = scale * dot;
+                if (x[p] > m) m = x[p];
+            }
+            double den = 0.0;
+            for (int p = 0; p < n; ++p) {
+                x[p] = exp(x[p] - m);
+                den += x[p];
+            }
+            for (int d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int p = 0; p < n; ++p) acc += x[p] * Vg[(int64_t)p * head_dim + d];
+                o[d] = acc / den;
+            }
+            free(Kg); free(Vg); free(x); free(qd);
+        }
+    }
+}
+
+/* Elementwise helpers for the Python wrapper. */
+void oracle_e4m3_encode_array(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+void oracle_e4m3_decode_array(const uint8_t *c, double *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+}

@@ -34,8 +34,11 @@ import numpy as np
 
 __all__ = ["CONFIGS", "Batch", "make_batch", "make_context_lens", "subset_batch", "NAN_BITS", "BlockPool"]
 
-# Quiet-NaN bit patterns used to poison unused cache slots.
-NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+# Quiet-NaN bit patterns used to poison unused cache slots (e4m3: 0x7F).
+NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "fp8": 0x7F}
+# Scale of the e4m3 caches: a code c stands for c * FP8_SCALE, so N(0, 1)
+# data uses codes of magnitude up to ~64 (well inside e4m3's +-448).
+FP8_SCALE = 1.0 / 16.0
 
 # The five decode workloads.  ``ctx`` describes the context-length law;
 # ``ctx_max`` is the longest context the workload can produce and sizes the
@@ -54,6 +57,10 @@ CONFIGS = {
     "13b": dict(number=3, num_seqs=256, num_heads=40, num_kv_heads=40, head_dim=128,
                 block_size=16, dtype="bf16", ctx=("lognormal", 300.0, 1.0, 1, 2048),
                 ctx_max=2048, pool=("demand", 1.2), partition_size=0),
+    # The 13B-shaped step with an FP8 (e4m3) KV cache (per-tensor scales).
+    "13b_fp8": dict(number=3, num_seqs=256, num_heads=40, num_kv_heads=40, head_dim=128,
+                    block_size=16, dtype="bf16", cache_dtype="fp8", ctx=("lognormal", 300.0, 1.0, 1, 2048),
+                    ctx_max=2048, pool=("demand", 1.2), partition_size=0),
     # GQA long context: 16 sequences, 32 query / 8 KV heads, 16k-32k tokens,
     # split into 512-token partitions; block_size 16 and 32 variants.
     "gqa": dict(number=4, num_seqs=16, num_heads=32, num_kv_heads=8, head_dim=128,
@@ -105,6 +112,13 @@ class Batch:
     context_lens: np.ndarray  # int32 [B]
     block_mapping: np.ndarray  # int64 [P, 2] (src, dst) copy pairs, maybe empty
     seed: int = 0
+    cache_dtype: str = ""     # "f16" / "bf16" (= dtype) or "fp8" (e4m3 codes, uint8 caches)
+    k_scale: float = 1.0      # e4m3 caches: a code c stands for c * scale
+    v_scale: float = 1.0
+
+    def __post_init__(self):
+        if not self.cache_dtype:
+            self.cache_dtype = self.dtype
 
     @property
     def kv_token_count(self) -> int:
@@ -112,7 +126,7 @@ class Batch:
 
     @property
     def elem_bytes(self) -> int:
-        return 2
+        return 1 if self.cache_dtype == "fp8" else 2
 
 
 class BlockPool:
@@ -161,12 +175,19 @@ def _round_half(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def _normal_bits(rng: np.random.Generator, shape, dtype: str, chunk: int = 1 << 24) -> np.ndarray:
-    """Draw N(0,1) float32 values in a fixed order and return half bits."""
+    """Draw N(0,1) float32 values in a fixed order and return half bits
+    (or, for "fp8", the e4m3 codes nearest to value / FP8_SCALE, via torch)."""
     n = int(np.prod(shape))
-    out = np.empty(n, dtype=np.uint16)
+    out = np.empty(n, dtype=np.uint8 if dtype == "fp8" else np.uint16)
     for lo in range(0, n, chunk):
         hi = min(n, lo + chunk)
-        out[lo:hi] = _round_half(rng.standard_normal(hi - lo, dtype=np.float32), dtype)
+        z = rng.standard_normal(hi - lo, dtype=np.float32)
+        if dtype == "fp8":
+            import torch
+            out[lo:hi] = torch.from_numpy(z * np.float32(1.0 / FP8_SCALE)).to(torch.float8_e4m3fn) \
+                .view(torch.uint8).numpy()
+        else:
+            out[lo:hi] = _round_half(z, dtype)
     return out.reshape(shape)
 
 
@@ -209,7 +230,8 @@ def make_context_lens(name: str, num_seqs: int | None = None, seed: int | None =
 
 def make_batch(name: str, *, num_seqs: int | None = None, groups: int | None = None,
                seed: int | None = None, ctx_cap: int | None = None,
-               block_size: int | None = None, context_lens=None, **overrides) -> Batch:
+               block_size: int | None = None, context_lens=None, cache_dtype: str | None = None,
+               **overrides) -> Batch:
     """Build the inputs of workload ``name`` (a key of :data:`CONFIGS`).
 
     ``num_seqs`` (or ``groups`` for "prefix") shrinks the batch while keeping
@@ -224,6 +246,8 @@ def make_batch(name: str, *, num_seqs: int | None = None, groups: int | None = N
         if k not in ("num_heads", "num_kv_heads", "head_dim", "dtype", "partition_size"):
             raise TypeError(f"unknown override {k}")
         cfg[k] = v
+    if cache_dtype is not None:
+        cfg["cache_dtype"] = cache_dtype
     if seed is None:
         seed = 140000 + cfg["number"]
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -258,10 +282,12 @@ def make_batch(name: str, *, num_seqs: int | None = None, groups: int | None = N
         blocks = pool.allocate(int(nblk[s]))
         tables[s, : len(blocks)] = blocks
 
+    cdt = cfg.get("cache_dtype", dt)
     q = _normal_bits(rng, (B, Hq, D), dt)
-    nan = NAN_BITS[dt]
-    k_cache = np.full((NB, bs, Hkv, D), nan, dtype=np.uint16)
-    v_cache = np.full((NB, bs, Hkv, D), nan, dtype=np.uint16)
+    nan = NAN_BITS[cdt]
+    cnp = np.uint8 if cdt == "fp8" else np.uint16
+    k_cache = np.full((NB, bs, Hkv, D), nan, dtype=cnp)
+    v_cache = np.full((NB, bs, Hkv, D), nan, dtype=cnp)
 
     # History rows: positions 0 .. ctx-2 of every sequence (the last position
     # is this step's new token, written by reshape_and_cache).
@@ -270,7 +296,7 @@ def make_batch(name: str, *, num_seqs: int | None = None, groups: int | None = N
         p = np.arange(max(int(ctx[s]) - 1, 0), dtype=np.int64)
         pos_slots.append(tables[s, p // bs].astype(np.int64) * bs + p % bs)
     hist = np.concatenate(pos_slots) if pos_slots else np.zeros(0, np.int64)
-    _fill_history(rng, k_cache, v_cache, hist, dt)
+    _fill_history(rng, k_cache, v_cache, hist, cdt)
 
     T = int((ctx > 0).sum())
     seqs_with_token = np.nonzero(ctx > 0)[0]
@@ -284,11 +310,13 @@ def make_batch(name: str, *, num_seqs: int | None = None, groups: int | None = N
                  partition_size=int(cfg["partition_size"]), scale=np.float32(1.0 / math.sqrt(D)),
                  q=q, k_cache=k_cache, v_cache=v_cache, key=key, value=value,
                  slot_mapping=slot_mapping, block_tables=tables, context_lens=ctx,
-                 block_mapping=np.zeros((0, 2), dtype=np.int64), seed=int(seed))
+                 block_mapping=np.zeros((0, 2), dtype=np.int64), seed=int(seed), cache_dtype=cdt,
+                 k_scale=FP8_SCALE if cdt == "fp8" else 1.0, v_scale=FP8_SCALE if cdt == "fp8" else 1.0)
 
 
 def _fill_history(rng, k_cache, v_cache, slots, dt, rows_per_chunk=1 << 14):
-    """Fill K rows for ``slots`` then V rows, drawing values in slot order."""
+    """Fill K rows for ``slots`` then V rows, drawing values in slot order
+    (``dt`` is the cache's element type)."""
     nb, bs, hkv, d = k_cache.shape
     for cache in (k_cache, v_cache):
         for lo in range(0, len(slots), rows_per_chunk):
@@ -353,11 +381,13 @@ def _make_prefix(cfg, rng, groups, seed, ctx_cap):
             row += pool.allocate(int(priv_blocks[s]))
             tables[s, : len(row)] = row
 
+    cdt = cfg.get("cache_dtype", dt)
     q = _normal_bits(rng, (B, Hq, D), dt)
-    nan = NAN_BITS[dt]
-    k_cache = np.full((NB, bs, Hkv, D), nan, dtype=np.uint16)
-    v_cache = np.full((NB, bs, Hkv, D), nan, dtype=np.uint16)
-    _fill_history(rng, k_cache, v_cache, np.concatenate(shared_slots), dt)
+    nan = NAN_BITS[cdt]
+    cnp = np.uint8 if cdt == "fp8" else np.uint16
+    k_cache = np.full((NB, bs, Hkv, D), nan, dtype=cnp)
+    v_cache = np.full((NB, bs, Hkv, D), nan, dtype=cnp)
+    _fill_history(rng, k_cache, v_cache, np.concatenate(shared_slots), cdt)
 
     # The step writes every private position P .. ctx-1 of every sample.
     slots = []
@@ -374,7 +404,8 @@ def _make_prefix(cfg, rng, groups, seed, ctx_cap):
                  partition_size=int(cfg["partition_size"]), scale=np.float32(1.0 / math.sqrt(D)),
                  q=q, k_cache=k_cache, v_cache=v_cache, key=key, value=value,
                  slot_mapping=slot_mapping, block_tables=tables, context_lens=ctx,
-                 block_mapping=bm, seed=int(seed))
+                 block_mapping=bm, seed=int(seed), cache_dtype=cdt,
+                 k_scale=FP8_SCALE if cdt == "fp8" else 1.0, v_scale=FP8_SCALE if cdt == "fp8" else 1.0)
 
 
 def subset_batch(b: Batch, seqs) -> Batch:
