@@ -37,6 +37,9 @@ WORKLOAD_TEXT = {
     "13b": "LLaMA-13B-shaped decode step, one layer: 256 seqs, 40 heads (MHA), head_dim 128, block_size 16, "
            "context lognormal(median 300, sigma 1) clipped to [1,2048], bf16, reshape_and_cache of each "
            "sequence's new token via a random slot_mapping",
+    "13b_fp8": "LLaMA-13B-shaped decode step, one layer, FP8 (e4m3) KV cache with per-tensor scales: 256 seqs, "
+               "40 heads, head_dim 128, block_size 16, context lognormal(median 300, sigma 1) clipped to [1,2048], "
+               "bf16 queries, quantising reshape_and_cache of each sequence's new token",
     "7b": "LLaMA-7B-shaped decode step, one layer: 64 seqs, 32 heads (MHA), head_dim 128, block_size 16, "
           "context uniform [32,2048], f16",
     "gqa": "GQA long-context decode: 16 seqs, 32 q / 8 kv heads, head_dim 128, block_size 16, context "
@@ -56,8 +59,8 @@ NOMINAL_HBM_GBS = 8000.0
 # --------------------------------------------------------------- accounting
 
 def kv_bytes(b) -> int:
-    """Bytes of K and V a decode step reads: sum_s ctx_s * Hkv * D * 2 (K,V) * 2 B."""
-    return int(b.context_lens.astype("int64").sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+    """Bytes of K and V a decode step reads: sum_s ctx_s * Hkv * D * 2 (K,V) * element bytes."""
+    return int(b.context_lens.astype("int64").sum()) * b.num_kv_heads * b.head_dim * 2 * b.elem_bytes
 
 
 def decode_bytes(b, partition: int) -> int:
@@ -76,8 +79,8 @@ def decode_bytes(b, partition: int) -> int:
 
 
 def step_bytes(b, partition: int) -> int:
-    rows = len(b.slot_mapping) * b.num_kv_heads * b.head_dim * 2 * 2 * 2  # K,V read + write
-    copies = len(b.block_mapping) * b.block_size * b.num_kv_heads * b.head_dim * 2 * 2 * 2
+    rows = len(b.slot_mapping) * b.num_kv_heads * b.head_dim * 2 * (2 + b.elem_bytes)  # K,V read + write
+    copies = len(b.block_mapping) * b.block_size * b.num_kv_heads * b.head_dim * 2 * 2 * b.elem_bytes
     return decode_bytes(b, partition) + rows + copies
 
 
@@ -195,8 +198,12 @@ def device_tensors(b, device):
                 context_lens=torch.from_numpy(b.context_lens),
                 block_mapping=torch.from_numpy(np.ascontiguousarray(b.block_mapping)))
     dev = {k: v.to(device) for k, v in host.items()}
-    dev["k_cache"] = h(b.k_cache).to(device)
-    dev["v_cache"] = h(b.v_cache).to(device)
+    if b.cache_dtype == "fp8":
+        dev["k_cache"] = torch.from_numpy(b.k_cache).to(device)
+        dev["v_cache"] = torch.from_numpy(b.v_cache).to(device)
+    else:
+        dev["k_cache"] = h(b.k_cache).to(device)
+        dev["v_cache"] = h(b.v_cache).to(device)
     return host, dev
 
 
@@ -232,19 +239,20 @@ def run_ours(args, world, rank, local):
     def step(ev=None):
         if has_pairs:
             pa.copy_blocks(T["k_cache"], T["v_cache"], T["block_mapping"])
-        pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"])
+        pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"],
+                             k_scale=b.k_scale, v_scale=b.v_scale)
         if ev is not None:
             ev[0].record(stream)
         pa.decode(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"],
                   float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
-                  workspace=ws)
+                  workspace=ws, k_scale=b.k_scale, v_scale=b.v_scale)
         if ev is not None:
             ev[1].record(stream)
 
     err = pa.new_err_flag(device)
     pa.decode(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"],
               float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
-              workspace=ws, err_flag=err)
+              workspace=ws, err_flag=err, k_scale=b.k_scale, v_scale=b.v_scale)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -297,10 +305,11 @@ def run_ours(args, world, rank, local):
             e2e_in[k].copy_(v, non_blocking=True)
         if has_pairs:
             pa.copy_blocks(T["k_cache"], T["v_cache"], e2e_in["block_mapping"])
-        pa.reshape_and_cache(e2e_in["key"], e2e_in["value"], T["k_cache"], T["v_cache"], e2e_in["slot_mapping"])
+        pa.reshape_and_cache(e2e_in["key"], e2e_in["value"], T["k_cache"], T["v_cache"], e2e_in["slot_mapping"],
+                             k_scale=b.k_scale, v_scale=b.v_scale)
         pa.decode(out, e2e_in["q"], T["k_cache"], T["v_cache"], e2e_in["block_tables"], e2e_in["context_lens"],
                   float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
-                  workspace=ws)
+                  workspace=ws, k_scale=b.k_scale, v_scale=b.v_scale)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -338,7 +347,7 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": b.dtype,
+        "dtype": b.dtype if b.cache_dtype == b.dtype else f"{b.dtype} q, {b.cache_dtype} kv",
         "data": "synthetic (seeded N(0,1) K/V/Q, seeded block permutation, NaN in unused slots)",
         "impl": "ours",
         "config": {
@@ -414,10 +423,23 @@ def _oracle_threads() -> int:
 def _post_step_caches(b):
     import oracle
     kc, vc = b.k_cache, b.v_cache
+    fp8 = b.cache_dtype == "fp8"
     if len(b.block_mapping):
-        kc, vc, _ = oracle.copy_blocks(kc, vc, b.block_mapping)
-    kc, vc, _ = oracle.reshape_and_cache(b.key, b.value, kc, vc, b.slot_mapping)
+        kc, vc, _ = (oracle.copy_blocks_bytes if fp8 else oracle.copy_blocks)(kc, vc, b.block_mapping)
+    if fp8:
+        kc, vc, _ = oracle.reshape_and_cache_fp8(b.key, b.value, b.dtype, kc, vc, b.slot_mapping, b.k_scale,
+                                                 b.v_scale)
+    else:
+        kc, vc, _ = oracle.reshape_and_cache(b.key, b.value, kc, vc, b.slot_mapping)
     return kc, vc
+
+
+def _oracle_attention(b, sub, kc, vc):
+    import oracle
+    if b.cache_dtype == "fp8":
+        return oracle.paged_attention_fp8(sub.q, b.dtype, kc, vc, b.k_scale, b.v_scale, sub.block_tables,
+                                          sub.context_lens, b.scale)
+    return oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
 
 
 def _pick_sample(b, target_s, kc, vc):
@@ -429,7 +451,7 @@ def _pick_sample(b, target_s, kc, vc):
     probe = list(range(0, b.num_seqs, max(1, b.num_seqs // 8)))[:8]
     sub = W.subset_batch(b, probe)
     t = time.perf_counter()
-    oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
+    _oracle_attention(b, sub, kc, vc)
     dt = max(time.perf_counter() - t, 1e-4)
     per_tok = dt / max(1, int(sub.context_lens.sum()))
     want_tok = target_s / per_tok
@@ -451,7 +473,7 @@ def cpu_baseline(b, target_s):
     runs = 0
     t = time.perf_counter()
     while True:  # repeat a sample that is the whole batch until ~target_s of CPU work
-        oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
+        _oracle_attention(b, sub, kc, vc)
         runs += 1
         if time.perf_counter() - t >= target_s or len(pick) < b.num_seqs:
             break
@@ -479,7 +501,7 @@ def run_reference(args, world, rank):
     sub = W.subset_batch(b, pick)
 
     def one():
-        oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
+        _oracle_attention(b, sub, kc, vc)
 
     for _ in range(args.warmup):
         one()

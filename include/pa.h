@@ -26,6 +26,13 @@
  *  - Element types: PA_F16 (IEEE binary16) or PA_BF16 for q/K/V; the decode
  *    output may also be PA_F32.  Arithmetic is fp32 (Page C §6: accumulating
  *    QK^T in half precision overflowed on long sequences).
+ *  - FP8 KV cache (Page A §八 lists FP8 among vLLM's quantisation options):
+ *    caches of PA_FP8_E4M3 hold one e4m3 code per element (bias 7, no
+ *    infinities, largest value 448) with one scale per tensor: a K code c
+ *    stands for value(c) * k_scale, V alike.  Writing quantises
+ *    code = e4m3(fp32(x) / scale): the division in fp32 (IEEE), rounding to
+ *    nearest-even, finite values saturating at +-448, NaN staying NaN.  The
+ *    FP8 cache is supported for head_dim 128.
  *  - Supported shapes: head_dim 64 or 128; block_size 8 or a multiple of 16
  *    up to 256; num_heads a multiple of num_kv_heads with
  *    num_heads / num_kv_heads in {1, 2, 4, 8}.
@@ -59,7 +66,7 @@ typedef enum {
     PA_ERR_DEVICE_BOUNDS = 5   /* returned by pa_check_err_flag for a non-zero flag */
 } pa_status;
 
-typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 /* Bits OR-ed into *err_flag by the kernels. */
 #define PA_FLAG_BAD_SLOT        0x1   /* slot_mapping entry >= num_blocks * block_size */
@@ -76,21 +83,24 @@ typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
  * §2.3 step 3 (write back and update the block's token count); Page A §二
  * (each step appends the new token's K and V to the cache).
  *
- *   key, value   : [num_tokens, num_kv_heads, head_dim], dtype
- *   k_cache/v_cache : [num_blocks, block_size, num_kv_heads, head_dim], dtype
+ *   key, value   : [num_tokens, num_kv_heads, head_dim], dtype (F16 or BF16)
+ *   k_cache/v_cache : [num_blocks, block_size, num_kv_heads, head_dim],
+ *                  cache_dtype (= dtype, or PA_FP8_E4M3)
  *   slot_mapping : [num_tokens] int64.  For token t with slot >= 0:
  *                    k_cache[slot / bs][slot % bs][h][:] = key[t][h][:]
  *                    v_cache[slot / bs][slot % bs][h][:] = value[t][h][:]
  *                  slot < 0 means "no write" (padding token).
- * The copy is bit-exact.  Slots must be distinct (else the surviving row is
- * unspecified).  slot >= num_blocks * block_size: skipped, PA_FLAG_BAD_SLOT.
- * num_tokens == 0 is a no-op.
+ *   k_scale, v_scale : FP8 caches only (> 0): code = e4m3(x / scale).
+ * A 16-bit copy is bit-exact.  Slots must be distinct (else the surviving row
+ * is unspecified).  slot >= num_blocks * block_size: skipped,
+ * PA_FLAG_BAD_SLOT.  num_tokens == 0 is a no-op.
  */
 pa_status pa_reshape_and_cache(const void *key, const void *value,
                                void *k_cache, void *v_cache,
                                const int64_t *slot_mapping, int64_t num_tokens,
                                int64_t num_blocks, int block_size,
                                int num_kv_heads, int head_dim, pa_dtype dtype,
+                               pa_dtype cache_dtype, float k_scale, float v_scale,
                                int *err_flag, void *stream);
 
 /*
@@ -138,8 +148,13 @@ int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads,
  * and is bitwise reproducible run to run for a given partition size.
  *
  *   out          : [num_seqs, num_heads, head_dim], out_dtype (F16/BF16/F32)
- *   query        : [num_seqs, num_heads, head_dim], kv_dtype
- *   k_cache/v_cache : [num_blocks, block_size, num_kv_heads, head_dim], kv_dtype
+ *   query        : [num_seqs, num_heads, head_dim], q_dtype (F16 or BF16)
+ *   k_cache/v_cache : [num_blocks, block_size, num_kv_heads, head_dim], kv_dtype:
+ *                  q_dtype, or PA_FP8_E4M3 with k_scale / v_scale (> 0;
+ *                  ignored for 16-bit caches).  With an FP8 cache the
+ *                  products run in binary16: e4m3 values are exact there and
+ *                  a bfloat16 query is rounded to binary16 (exact for
+ *                  |q| in [2^-14, 65504]).
  *   block_tables : [num_seqs, max_blocks_per_seq] int32; only the first
  *                  ceil(context_lens[s] / bs) entries of row s are read
  *   context_lens : [num_seqs] int32, each in [0, max_context_len]; 0 gives a
@@ -157,8 +172,9 @@ int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads,
  * PA_FLAG_BAD_CONTEXT_LEN.
  */
 pa_status pa_decode(void *out, pa_dtype out_dtype,
-                    const void *query,
+                    const void *query, pa_dtype q_dtype,
                     const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                    float k_scale, float v_scale,
                     const int32_t *block_tables, int max_blocks_per_seq,
                     const int32_t *context_lens, int max_context_len,
                     int num_seqs, int num_heads, int num_kv_heads, int head_dim,
@@ -198,8 +214,9 @@ pa_status pa_decode(void *out, pa_dtype out_dtype,
  */
 #define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype,
-                            const void *query,
+                            const void *query, pa_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                            float k_scale, float v_scale,
                             const int32_t *block_tables, int max_blocks_per_seq,
                             const int32_t *context_lens, int max_context_len,
                             int num_seqs, int num_heads, int num_kv_heads, int head_dim,
@@ -214,7 +231,8 @@ pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype,
  * section: parallel sampling of one prompt; Page A §3.1; Page B §3 prefix
  * sharing).  For every pair p:
  *     k_cache[dst_p] = k_cache[src_p],  v_cache[dst_p] = v_cache[src_p]
- * (whole blocks: block_size * num_kv_heads * head_dim elements each), bit-exact.
+ * (whole blocks: block_size * num_kv_heads * head_dim elements each, of
+ * `dtype`: F16, BF16 or FP8_E4M3), bit-exact.
  *
  *   block_mapping : [num_pairs, 2] int64 (src, dst), device memory
  * Destinations must be distinct and no destination may also be a source

@@ -11,6 +11,8 @@ PyTorch fallback - a missing library raises.
 
 Cache layout: ``[num_blocks, block_size, num_kv_heads, head_dim]`` per layer
 for K and for V ("LLM推理优化：vLLM PagedAttention深度解析与工程实践", §4.1).
+Caches are float16 / bfloat16, or FP8 e4m3 codes (``torch.float8_e4m3fn`` or
+``torch.uint8``) with per-tensor ``k_scale`` / ``v_scale``.
 """
 from __future__ import annotations
 
@@ -18,7 +20,7 @@ import ctypes
 
 from . import _lib
 from ._lib import (FLAG_BAD_BLOCK_ID, FLAG_BAD_CONTEXT_LEN, FLAG_BAD_COPY_PAIR, FLAG_BAD_SLOT,
-                   FLAG_TIMEOUT, PA_BF16, PA_F16, PA_F32, PagedAttentionError)
+                   FLAG_TIMEOUT, PA_BF16, PA_F16, PA_F32, PA_FP8_E4M3, PagedAttentionError)
 
 __all__ = ["reshape_and_cache", "decode", "copy_blocks", "decode_workspace_size",
            "decode_partition_size", "DecodeWorkspace", "new_err_flag", "read_err_flag",
@@ -44,6 +46,13 @@ def _dtype_code(t, allow_f32=False) -> int:
     if allow_f32 and t.dtype == torch.float32:
         return PA_F32
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _cache_code(t) -> int:
+    torch = _torch()
+    if t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        return PA_FP8_E4M3
+    return _dtype_code(t)
 
 
 def _need(cond: bool, msg: str) -> None:
@@ -81,8 +90,10 @@ def read_err_flag(err_flag, clear: bool = True) -> int:
     return int(out.value)
 
 
-def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, err_flag=None) -> None:
-    """Write key/value rows [T, Hkv, D] into cache slots (slot < 0: skip)."""
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, err_flag=None,
+                      k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+    """Write key/value rows [T, Hkv, D] into cache slots (slot < 0: skip);
+    an FP8 cache receives e4m3(x / scale)."""
     for n, t in (("key", key), ("value", value), ("k_cache", k_cache), ("v_cache", v_cache),
                  ("slot_mapping", slot_mapping)):
         _cuda_contig(n, t)
@@ -90,13 +101,14 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, err_flag=None)
     _need(key.dim() == 3 and value.shape == key.shape, "key/value must be [T, Hkv, D]")
     _need(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [NB, bs, Hkv, D]")
     _need(k_cache.shape[2:] == key.shape[1:], "cache and key head shapes differ")
-    _need(key.dtype == value.dtype == k_cache.dtype == v_cache.dtype, "dtype mismatch")
+    _need(key.dtype == value.dtype and k_cache.dtype == v_cache.dtype, "dtype mismatch")
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == key.shape[0],
           "slot_mapping must be int64 [T]")
     nb, bs, hkv, d = k_cache.shape
     st = _lib.load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
                                           _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d,
-                                          _dtype_code(key), _ptr(err_flag), _stream(key.device))
+                                          _dtype_code(key), _cache_code(k_cache), float(k_scale),
+                                          float(v_scale), _ptr(err_flag), _stream(key.device))
     _lib.check(st, "pa_reshape_and_cache")
 
 
@@ -110,7 +122,7 @@ def copy_blocks(k_cache, v_cache, block_mapping, err_flag=None) -> None:
     _need(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype, "cache mismatch")
     nb, bs, hkv, d = k_cache.shape
     st = _lib.load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_mapping),
-                                    block_mapping.shape[0], nb, bs, hkv, d, _dtype_code(k_cache),
+                                    block_mapping.shape[0], nb, bs, hkv, d, _cache_code(k_cache),
                                     _ptr(err_flag), _stream(k_cache.device))
     _lib.check(st, "pa_copy_blocks")
 
@@ -157,7 +169,7 @@ _default_ws: dict = {}
 
 def decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: float,
            max_context_len: int | None = None, partition_size: int = 0, workspace=None,
-           err_flag=None) -> None:
+           err_flag=None, k_scale: float = 1.0, v_scale: float = 1.0) -> None:
     """Paged decode attention into ``out`` [B, Hq, D] (f16, bf16 or f32).
 
     ``max_context_len`` is a host-side bound on ``context_lens`` (defaults to
@@ -168,7 +180,7 @@ def decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: floa
         _cuda_contig(n, t)
     _need(query.dim() == 3 and out.shape == query.shape, "query/out must be [B, Hq, D]")
     _need(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [NB, bs, Hkv, D]")
-    _need(query.dtype == k_cache.dtype == v_cache.dtype, "query and caches must share a dtype")
+    _need(k_cache.dtype == v_cache.dtype, "K and V caches must share a dtype")
     _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
           block_tables.shape[0] == query.shape[0], "block_tables must be int32 [B, maxNB]")
     _need(context_lens.dtype == torch.int32 and context_lens.numel() == query.shape[0],
@@ -186,8 +198,9 @@ def decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: floa
     layout = (B, Hq, hkv, D, bs, int(max_context_len), int(partition_size))
     buf = workspace.get(ws_bytes, layout) if isinstance(workspace, DecodeWorkspace) else workspace
     nbytes = 0 if buf is None else buf.numel() * buf.element_size()
-    st = _lib.load().pa_decode(_ptr(out), _dtype_code(out, allow_f32=True), _ptr(query),
-                               _ptr(k_cache), _ptr(v_cache), _dtype_code(query), _ptr(block_tables),
+    st = _lib.load().pa_decode(_ptr(out), _dtype_code(out, allow_f32=True), _ptr(query), _dtype_code(query),
+                               _ptr(k_cache), _ptr(v_cache), _cache_code(k_cache), float(k_scale),
+                               float(v_scale), _ptr(block_tables),
                                maxnb, _ptr(context_lens), int(max_context_len), B, Hq, hkv, D, bs, nb,
                                float(scale), int(partition_size), _ptr(buf), nbytes, _ptr(err_flag),
                                _stream(query.device))

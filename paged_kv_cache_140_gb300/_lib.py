@@ -11,7 +11,7 @@ import os
 from . import _build
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE, PA_ERR_DEVICE_BOUNDS = range(6)
-PA_F16, PA_BF16, PA_F32 = 0, 1, 2
+PA_F16, PA_BF16, PA_F32, PA_FP8_E4M3 = 0, 1, 2, 3
 
 FLAG_BAD_SLOT = 0x1
 FLAG_BAD_BLOCK_ID = 0x2
@@ -22,14 +22,14 @@ FLAG_TIMEOUT = 0x10
 # Every symbol include/pa.h declares, with (restype, argtypes).
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 SIGNATURES = {
-    "pa_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _P, _P]),
+    "pa_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _F, _F, _P, _P]),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "pa_decode_workspace_init": (_I, [_P, _SZ, _P]),
     "pa_decode_partition_size": (_I, [_I, _I, _I, _I, _I, _I, _I]),
-    "pa_decode": (_I, [_P, _I, _P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64, _F, _I,
-                       _P, _SZ, _P, _P]),
-    "pa_decode_noalloc": (_I, [_P, _I, _P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64, _F,
-                               _I, _P, _P]),
+    "pa_decode": (_I, [_P, _I, _P, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64, _F,
+                       _I, _P, _SZ, _P, _P]),
+    "pa_decode_noalloc": (_I, [_P, _I, _P, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64,
+                               _F, _I, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _I, _I, _I, _P, _P]),
     "pa_check_err_flag": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int), _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),

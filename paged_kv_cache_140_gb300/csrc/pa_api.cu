@@ -39,6 +39,9 @@ EncodeTiledFn encode_tiled() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool half_dtype(pa_dtype d) { return d == PA_F16 || d == PA_BF16; }
+bool cache_dtype_ok(pa_dtype d) { return half_dtype(d) || d == PA_FP8_E4M3; }
+int elem_bytes(pa_dtype d) { return d == PA_FP8_E4M3 ? 1 : 2; }
+bool scale_ok(float s) { return s > 0.f && s < 3.0e38f; }
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
 bool supported_block_size(int bs) { return bs == 8 || (bs >= 16 && bs <= 256 && bs % 16 == 0); }
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
@@ -131,18 +134,22 @@ bool plan_workspace(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
     return true;
 }
 
+// Tensor map over a cache [NB * bs, Hkv, D] with 128-byte boxes of one KV
+// head's row and min(bs, 16) rows, 128-byte swizzle.
 bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int block_size,
-                      int num_kv_heads, int head_dim) {
+                      int num_kv_heads, int head_dim, int es) {
     EncodeTiledFn fn = encode_tiled();
     if (fn == nullptr) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
                                 static_cast<cuuint64_t>(num_kv_heads),
                                 static_cast<cuuint64_t>(num_blocks) * block_size};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                   static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
-    const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(std::min(block_size, 16))};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * es,
+                                   static_cast<cuuint64_t>(num_kv_heads) * head_dim * es};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1u,
+                               static_cast<cuuint32_t>(std::min(block_size, 16))};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(cache), dims, strides,
+    return fn(map, es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+              const_cast<void *>(cache), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -168,19 +175,30 @@ PA_EXPORT pa_status pa_reshape_and_cache(const void *key, const void *value, voi
                                          void *v_cache, const int64_t *slot_mapping,
                                          int64_t num_tokens, int64_t num_blocks, int block_size,
                                          int num_kv_heads, int head_dim, pa_dtype dtype,
+                                         pa_dtype cache_dtype, float k_scale, float v_scale,
                                          int *err_flag, void *stream) {
     if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
-        head_dim <= 0 || !half_dtype(dtype))
+        head_dim <= 0 || !half_dtype(dtype) || !cache_dtype_ok(cache_dtype))
         return PA_ERR_INVALID_ARG;
-    if ((static_cast<int64_t>(num_kv_heads) * head_dim * 2) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    const bool fp8 = cache_dtype == PA_FP8_E4M3;
+    if (!fp8 && cache_dtype != dtype) return PA_ERR_UNSUPPORTED;
+    if (fp8 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return PA_ERR_INVALID_ARG;
+    const int64_t row_elems = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if ((row_elems * 2) % 16 != 0 || row_elems % 8 != 0) return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
     if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
     if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
-    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
-    cudaError_t e = pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping,
-                                                 num_tokens, num_blocks * block_size, row_bytes,
-                                                 err_flag, static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (fp8)
+        e = pa::launch_reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                             num_blocks * block_size, row_elems, dtype == PA_BF16,
+                                             k_scale, v_scale, err_flag,
+                                             static_cast<cudaStream_t>(stream));
+    else
+        e = pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                         num_blocks * block_size, row_elems * 2, err_flag,
+                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -189,9 +207,10 @@ PA_EXPORT pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *
                                    int num_kv_heads, int head_dim, pa_dtype dtype, int *err_flag,
                                    void *stream) {
     if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
-        head_dim <= 0 || !half_dtype(dtype))
+        head_dim <= 0 || !cache_dtype_ok(dtype))
         return PA_ERR_INVALID_ARG;
-    const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+    const int64_t block_bytes =
+        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * elem_bytes(dtype);
     if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
     if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
@@ -232,8 +251,9 @@ PA_EXPORT pa_status pa_decode_workspace_init(void *workspace, size_t workspace_b
                : PA_ERR_CUDA;
 }
 
-PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
+PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
                               const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                              float k_scale, float v_scale,
                               const int32_t *block_tables, int max_blocks_per_seq,
                               const int32_t *context_lens, int max_context_len, int num_seqs,
                               int num_heads, int num_kv_heads, int head_dim, int block_size,
@@ -243,8 +263,13 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
         return PA_ERR_INVALID_ARG;
-    if (!half_dtype(kv_dtype) || (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32))
+    if (!half_dtype(q_dtype) || !cache_dtype_ok(kv_dtype) ||
+        (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32))
         return PA_ERR_INVALID_ARG;
+    const bool fp8 = kv_dtype == PA_FP8_E4M3;
+    if (fp8 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return PA_ERR_INVALID_ARG;
+    if (!fp8 && kv_dtype != q_dtype) return PA_ERR_UNSUPPORTED;     // 16-bit caches: same type as q
+    if (fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (!supported_group(num_heads / num_kv_heads) || !supported_head_dim(head_dim) ||
         !supported_block_size(block_size))
@@ -277,17 +302,18 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
     const Tuning &tune = tuning();
     const int stages = tune.stages > 0 ? tune.stages : pa::kDefaultStages;
     const int max_warps = head_dim == 128 ? 12 : 16;
-    const int def_warps = head_dim == 128 ? pa::kDefaultWarps128 : 16;
+    const int def_warps = head_dim == 128 ? (fp8 ? pa::kDefaultWarpsFp8 : pa::kDefaultWarps128) : 16;
     int warps = tune.warps > 0 ? std::min(tune.warps, max_warps) : def_warps;
-    while (warps > 1 && pa::decode_smem_bytes(head_dim, G, warps, stages, num_seqs) >
+    const int es = elem_bytes(kv_dtype);
+    while (warps > 1 && pa::decode_smem_bytes(head_dim, G, es, warps, stages, num_seqs) >
                             static_cast<size_t>(dev.smem_optin))
         --warps;
-    const size_t smem_used = pa::decode_smem_bytes(head_dim, G, warps, stages, num_seqs);
+    const size_t smem_used = pa::decode_smem_bytes(head_dim, G, es, warps, stages, num_seqs);
     if (smem_used > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
     CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim) ||
-        !encode_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim))
+    if (!encode_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, es) ||
+        !encode_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, es))
         return PA_ERR_CUDA;
 
     pa::DecodeParams p{};
@@ -303,7 +329,8 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
     p.num_kv_heads = num_kv_heads;
     p.block_size = block_size;
     p.num_blocks = num_blocks;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.0f);
+    p.v_scale = fp8 ? v_scale : 1.0f;
     p.partition_size = w.partition;
     p.max_partitions = w.max_partitions;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -313,7 +340,8 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query,
     p.stages = stages;
     p.interleave = tune.interleave;
 
-    cudaError_t e = pa::launch_decode(p, head_dim, G, kv_dtype == PA_BF16, tk, tv, dev.sms, warps,
+    const int kv = fp8 ? (q_dtype == PA_F16 ? 2 : 3) : (kv_dtype == PA_BF16 ? 1 : 0);
+    cudaError_t e = pa::launch_decode(p, head_dim, G, kv, tk, tv, dev.sms, warps,
                                       smem_used, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

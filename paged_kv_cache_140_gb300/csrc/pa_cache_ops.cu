@@ -43,6 +43,45 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// Quantising variant for an e4m3 cache: each thread turns 8 elements of a
+// 16-bit row into 8 codes, code = e4m3(x / scale) with the division in fp32
+// (IEEE, round to nearest) and nearest-even rounding that saturates finite
+// values at +-448.
+template <bool BF16>
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                                 uint2 *__restrict__ k_cache, uint2 *__restrict__ v_cache,
+                                 const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                                 int64_t num_slots, int64_t row8, float k_scale, float v_scale,
+                                 int *err_flag) {
+    pdl_launch_dependents();
+    const int64_t i = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
+    auto quant8 = [](uint4 w, float sc) {
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        uint32_t code[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = Half2x<BF16>::to_float2(in[k]);
+            code[k] = f32x2_to_e4m3x2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc));
+        }
+        return make_uint2(code[0] | (code[1] << 16), code[2] | (code[3] << 16));
+    };
+    for (int64_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (threadIdx.x == 0 && blockIdx.y == 0) report(err_flag, 0x1 /* PA_FLAG_BAD_SLOT */);
+            continue;
+        }
+        for (int64_t c = i; c < row8; c += static_cast<int64_t>(gridDim.y) * blockDim.x) {
+            const uint4 a = __ldg(key + t * row8 + c);
+            const uint4 b = __ldg(value + t * row8 + c);
+            k_cache[slot * row8 + c] = quant8(a, k_scale);
+            v_cache[slot * row8 + c] = quant8(b, v_scale);
+        }
+    }
+}
+
 // grid.x: copy pairs (grid-stride), grid.y: slices of the block; each thread
 // moves 4 chunks of 16 bytes of K and of V per iteration.
 __global__ void __launch_bounds__(256)
@@ -103,6 +142,25 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
         num_slots, row16, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, void *k_cache,
+                                         void *v_cache, const int64_t *slot_mapping,
+                                         int64_t num_tokens, int64_t num_slots, int64_t row_elems,
+                                         bool bf16, float k_scale, float v_scale, int *err_flag,
+                                         cudaStream_t stream) {
+    const int64_t row8 = row_elems / 8;
+    const int threads = 128;
+    const int64_t slices = (row8 + threads - 1) / threads;
+    const int64_t cap = (static_cast<int64_t>(sm_count()) * 32 + slices - 1) / slices;
+    const int64_t gx = num_tokens < cap ? num_tokens : cap;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(slices < 65535 ? slices : 65535));
+    auto kern = bf16 ? reshape_and_cache_fp8_kernel<true> : reshape_and_cache_fp8_kernel<false>;
+    kern<<<grid, threads, 0, stream>>>(static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                                       static_cast<uint2 *>(k_cache), static_cast<uint2 *>(v_cache),
+                                       slot_mapping, num_tokens, num_slots, row8, k_scale, v_scale,
+                                       err_flag);
     return cudaGetLastError();
 }
 

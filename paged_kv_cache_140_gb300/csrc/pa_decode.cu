@@ -49,13 +49,15 @@ constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kRowBytes = 128;                          // one swizzled 64-element half row
 constexpr int kRegionBytes = kStageTokens * kRowBytes;  // 16 rows x 128 B = 2 KB
 
-template <int D, int G>
+// ES = bytes per cache element (2: f16/bf16, 1: e4m3).
+template <int D, int G, int ES>
 struct Layout {
-    static constexpr int kHalves = D / 64;                 // swizzled regions per K (or V) tile
-    static constexpr int kTileBytes = kHalves * kRegionBytes;
+    static constexpr int kBoxes = D * ES / 128;            // 128-byte TMA boxes per K (or V) row
+    static constexpr int kBoxElems = 128 / ES;             // elements per box row
+    static constexpr int kTileBytes = kBoxes * kRegionBytes;
     static constexpr int kVOffset = kTileBytes;
     static constexpr int kQOffset = 2 * kTileBytes;
-    static constexpr int kQBytes = G * D * 2;
+    static constexpr int kQBytes = G * D * 2;              // the query stays 16-bit
     static constexpr int kSlotBytes = ((2 * kTileBytes + kQBytes + 1023) / 1024) * 1024;
     static constexpr int kOStride = D + 4;                 // floats per staged output row
     static constexpr int kOBytes = G * kOStride * 4;       // per-warp output staging
@@ -166,12 +168,19 @@ __device__ __forceinline__ void store_row(void *base, int dtype, int64_t off, co
 template <int D>
 constexpr int kMaxThreads = D == 128 ? 384 : 512;
 
-template <int D, int G, bool BF16>
+// KV: 0 = f16 cache and query, 1 = bf16 cache and query, 2 / 3 = e4m3 cache
+// with an f16 / bf16 query (run as f16 MMAs; e4m3 values are exact in f16,
+// bf16 queries are rounded to f16).
+template <int D, int G, int KV>
 __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     paged_decode_kernel(const __grid_constant__ DecodeParams p,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v) {
-    using L = Layout<D, G>;
+    constexpr bool kFp8 = KV >= 2;
+    constexpr bool kQBf16 = KV == 1 || KV == 3;
+    constexpr bool BF16 = KV == 1;     // MMA operand type
+    static_assert(!kFp8 || D == 128, "the e4m3 cache path is built for head_dim 128");
+    using L = Layout<D, G, kFp8 ? 1 : 2>;
     using Cvt = Half2x<BF16>;
     constexpr int KS = L::kSteps;   // QK steps over the head dim
     constexpr int MT = L::kSteps;   // PV tiles over the head dim
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
                         if (lane == 0) report(p.err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
                     } else {
                         ids[b] = id;
-                        bytes += 2u * L::kHalves * rows * kRowBytes;
+                        bytes += 2u * L::kBoxes * rows * kRowBytes;
                     }
                 }
             }
@@ -366,11 +375,11 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
                 if (ids[b] >= 0) {
                     const int z = ids[b] * bs + ((tok0 + b * bs) % bs);
 #pragma unroll
-                    for (int h = 0; h < L::kHalves; ++h) {
+                    for (int h = 0; h < L::kBoxes; ++h) {
                         tma_load_3d(sp + h * kRegionBytes + b * rows * kRowBytes, &tmap_k,
-                                    &bars[slot], h * 64, ic.kvh, z, policy);
+                                    &bars[slot], h * L::kBoxElems, ic.kvh, z, policy);
                         tma_load_3d(sp + L::kVOffset + h * kRegionBytes + b * rows * kRowBytes,
-                                    &tmap_v, &bars[slot], h * 64, ic.kvh, z, policy);
+                                    &tmap_v, &bars[slot], h * L::kBoxElems, ic.kvh, z, policy);
                     }
                 }
             }
@@ -425,10 +434,28 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         if (m.j == 0) {
             // New item: the query's B fragments straight from the slot (16-bit).
             const uint32_t *qw = reinterpret_cast<const uint32_t *>(sp + L::kQOffset);
+            if constexpr (!kFp8) {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                qf[ks][0] = g < G ? qw[(g * D + ks * 16 + 2 * t) >> 1] : 0u;
-                qf[ks][1] = g < G ? qw[(g * D + ks * 16 + 2 * t + 8) >> 1] : 0u;
+                for (int ks = 0; ks < KS; ++ks) {
+                    qf[ks][0] = g < G ? qw[(g * D + ks * 16 + 2 * t) >> 1] : 0u;
+                    qf[ks][1] = g < G ? qw[(g * D + ks * 16 + 2 * t + 8) >> 1] : 0u;
+                }
+            } else {
+                // Dims in the order the e4m3 K fragments arrive (see QK):
+                // step 2kc+hl takes dims 32kc + 4t + 2hl (+1) and the same + 16.
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int d = 32 * (ks >> 1) + 4 * t + 2 * (ks & 1);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        uint32_t w = g < G ? qw[(g * D + d + 16 * k) >> 1] : 0u;
+                        if constexpr (kQBf16) {
+                            const float2 f = Half2x<true>::to_float2(w);
+                            w = pack2<false>(f.x, f.y);
+                        }
+                        qf[ks][k] = w;
+                    }
+                }
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -444,12 +471,28 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         {
             const int j = lane >> 3, r = lane & 7;
             const int tok = r + 8 * (j & 1);
+            if constexpr (!kFp8) {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int ch = 2 * ks + (j >> 1);
-                uint32_t a[4];
-                ldsm_x4(a, sa + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
-                mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int ch = 2 * ks + (j >> 1);
+                    uint32_t a[4];
+                    ldsm_x4(a, sa + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
+                    mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
+                }
+            } else {
+                // ldmatrix on the byte tile viewed as 16-bit: each register holds
+                // four consecutive dims of one token; split into two f16 pairs,
+                // each 32-dim chunk feeds two MMAs (dims permuted alike in q).
+#pragma unroll
+                for (int kc = 0; kc < D / 32; ++kc) {
+                    const int ch = 2 * kc + (j >> 1);
+                    uint32_t a[4], lo[4], hi[4];
+                    ldsm_x4(a, sa + tok * kRowBytes + ((ch ^ r) << 4));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(a[i], lo[i], hi[i]);
+                    mma_16816<false>(c[0], lo, qf[2 * kc][0], qf[2 * kc][1]);
+                    mma_16816<false>(c[1], hi, qf[2 * kc + 1][0], qf[2 * kc + 1][1]);
+                }
             }
         }
         // x[i]: i = 0 (token g, head 2t), 1 (g, 2t+1), 2 (g+8, 2t), 3 (g+8, 2t+1)
@@ -523,7 +566,7 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
             // NaN; 0 * NaN would poison the tensor-core sums, so clear them.
             uint8_t *vt = sp + L::kVOffset;
 #pragma unroll
-            for (int k = 0; k < kStageTokens * L::kHalves * 8 / 32; ++k) {
+            for (int k = 0; k < kStageTokens * L::kBoxes * 8 / 32; ++k) {
                 const int q16 = lane + 32 * k;                // 16-byte chunk index
                 const int row = (q16 >> 3) % kStageTokens;    // 8 chunks per 128-byte row
                 if (!((m.mask >> row) & 1))
@@ -534,13 +577,32 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         {
             const int j = lane >> 3, r = lane & 7;
             const int tok = r + 8 * (j >> 1);
+            if constexpr (!kFp8) {
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const int ch = 2 * mt + (j & 1);
-                uint32_t a[4];
-                ldsm_x4_trans(a, va + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
-                mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
-                mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int ch = 2 * mt + (j & 1);
+                    uint32_t a[4];
+                    ldsm_x4_trans(a, va + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
+                    mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
+                    mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                }
+            } else {
+                // Transposed ldmatrix of the byte tile viewed as 16-bit gives
+                // (tokens 2t, 2t+1) x (dims 2g, 2g+1); regroup the bytes so
+                // each f16 pair is one dim over two tokens: even dims feed
+                // acc[2vc], odd dims acc[2vc+1].
+#pragma unroll
+                for (int vc = 0; vc < D / 32; ++vc) {
+                    const int ch = 2 * vc + (j & 1);
+                    uint32_t a[4], ev[4], od[4];
+                    ldsm_x4_trans(a, va + tok * kRowBytes + ((ch ^ r) << 4));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(prmt(a[i], 0x3120u), ev[i], od[i]);
+                    mma_16816<false>(acc[2 * vc], ev, bhi[0], bhi[1]);
+                    mma_16816<false>(acc[2 * vc], ev, blo[0], blo[1]);
+                    mma_16816<false>(acc[2 * vc + 1], od, bhi[0], bhi[1]);
+                    mma_16816<false>(acc[2 * vc + 1], od, blo[0], blo[1]);
+                }
             }
         }
 
@@ -557,11 +619,22 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
             for (int e = 0; e < 2; ++e) {
                 const int h = 2 * t + e;
                 if (h < G) {
-                    const float s = final_out ? (lt[e] > 0.f ? 1.f / lt[e] : 0.f) : 1.f;
+                    const float s = (final_out ? (lt[e] > 0.f ? 1.f / lt[e] : 0.f) : 1.f) * p.v_scale;
+                    float *orow = obuf + h * L::kOStride;
+                    if constexpr (!kFp8) {
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        obuf[h * L::kOStride + mt * 16 + g] = acc[mt][e] * s;
-                        obuf[h * L::kOStride + mt * 16 + g + 8] = acc[mt][2 + e] * s;
+                        for (int mt = 0; mt < MT; ++mt) {
+                            orow[mt * 16 + g] = acc[mt][e] * s;
+                            orow[mt * 16 + g + 8] = acc[mt][2 + e] * s;
+                        }
+                    } else {
+#pragma unroll
+                        for (int vc = 0; vc < D / 32; ++vc) {
+                            orow[32 * vc + 2 * g] = acc[2 * vc][e] * s;
+                            orow[32 * vc + 16 + 2 * g] = acc[2 * vc][2 + e] * s;
+                            orow[32 * vc + 2 * g + 1] = acc[2 * vc + 1][e] * s;
+                            orow[32 * vc + 16 + 2 * g + 1] = acc[2 * vc + 1][2 + e] * s;
+                        }
                     }
                 }
             }
@@ -707,9 +780,9 @@ __global__ void __launch_bounds__(256)
     store_row<D>(p.out, p.out_dtype, (static_cast<int64_t>(s) * p.num_heads + kvh * G + h) * D + d0, o);
 }
 
-template <int D, int G>
+template <int D, int G, int ES>
 size_t smem_for(int warps, int stages, int num_seqs) {
-    using L = Layout<D, G>;
+    using L = Layout<D, G, ES>;
     size_t per_warp = static_cast<size_t>(stages) * (L::kSlotBytes + kMetaBytes + 8) + L::kOBytes;
     return 1024 + per_warp * warps + 32 * 4 + 4 * static_cast<size_t>(num_seqs) +
            4 * (static_cast<size_t>(num_seqs) + 1);
@@ -734,10 +807,10 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int D, int G, bool BF16>
+template <int D, int G, int KV>
 cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                      int grid, int warps, size_t smem, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<D, G, BF16>;
+    auto kern = paged_decode_kernel<D, G, KV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -755,49 +828,58 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtenso
 }
 
 template <int D, int G>
-cudaError_t launch_dt(const DecodeParams &p, bool bf16, const CUtensorMap &tk,
-                      const CUtensorMap &tv, int grid, int warps, size_t smem,
-                      cudaStream_t stream) {
-    return bf16 ? launch_t<D, G, true>(p, tk, tv, grid, warps, smem, stream)
-                : launch_t<D, G, false>(p, tk, tv, grid, warps, smem, stream);
-}
-
-template <int D>
-cudaError_t launch_g(const DecodeParams &p, int group, bool bf16, const CUtensorMap &tk,
-                     const CUtensorMap &tv, int grid, int warps, size_t smem,
-                     cudaStream_t stream) {
-    switch (group) {
-        case 1: return launch_dt<D, 1>(p, bf16, tk, tv, grid, warps, smem, stream);
-        case 2: return launch_dt<D, 2>(p, bf16, tk, tv, grid, warps, smem, stream);
-        case 4: return launch_dt<D, 4>(p, bf16, tk, tv, grid, warps, smem, stream);
-        case 8: return launch_dt<D, 8>(p, bf16, tk, tv, grid, warps, smem, stream);
+cudaError_t launch_kv(const DecodeParams &p, int kv, const CUtensorMap &tk, const CUtensorMap &tv,
+                      int grid, int warps, size_t smem, cudaStream_t stream) {
+    switch (kv) {
+        case 0: return launch_t<D, G, 0>(p, tk, tv, grid, warps, smem, stream);
+        case 1: return launch_t<D, G, 1>(p, tk, tv, grid, warps, smem, stream);
+        case 2:
+            if constexpr (D == 128) return launch_t<D, G, 2>(p, tk, tv, grid, warps, smem, stream);
+            return cudaErrorInvalidValue;
+        case 3:
+            if constexpr (D == 128) return launch_t<D, G, 3>(p, tk, tv, grid, warps, smem, stream);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <int D>
+cudaError_t launch_g(const DecodeParams &p, int group, int kv, const CUtensorMap &tk,
+                     const CUtensorMap &tv, int grid, int warps, size_t smem,
+                     cudaStream_t stream) {
+    switch (group) {
+        case 1: return launch_kv<D, 1>(p, kv, tk, tv, grid, warps, smem, stream);
+        case 2: return launch_kv<D, 2>(p, kv, tk, tv, grid, warps, smem, stream);
+        case 4: return launch_kv<D, 4>(p, kv, tk, tv, grid, warps, smem, stream);
+        case 8: return launch_kv<D, 8>(p, kv, tk, tv, grid, warps, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D, int ES>
 size_t smem_g(int group, int warps, int stages, int num_seqs) {
     switch (group) {
-        case 1: return smem_for<D, 1>(warps, stages, num_seqs);
-        case 2: return smem_for<D, 2>(warps, stages, num_seqs);
-        case 4: return smem_for<D, 4>(warps, stages, num_seqs);
-        case 8: return smem_for<D, 8>(warps, stages, num_seqs);
+        case 1: return smem_for<D, 1, ES>(warps, stages, num_seqs);
+        case 2: return smem_for<D, 2, ES>(warps, stages, num_seqs);
+        case 4: return smem_for<D, 4, ES>(warps, stages, num_seqs);
+        case 8: return smem_for<D, 8, ES>(warps, stages, num_seqs);
         default: return 0;
     }
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int head_dim, int group, int warps, int stages, int num_seqs) {
-    return head_dim == 64 ? smem_g<64>(group, warps, stages, num_seqs)
-                          : smem_g<128>(group, warps, stages, num_seqs);
+size_t decode_smem_bytes(int head_dim, int group, int elem_bytes, int warps, int stages, int num_seqs) {
+    if (head_dim == 64) return smem_g<64, 2>(group, warps, stages, num_seqs);
+    return elem_bytes == 1 ? smem_g<128, 1>(group, warps, stages, num_seqs)
+                           : smem_g<128, 2>(group, warps, stages, num_seqs);
 }
 
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, bool bf16,
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, int kv,
                           const CUtensorMap &tk, const CUtensorMap &tv, int grid, int warps,
                           size_t smem, cudaStream_t stream) {
-    if (head_dim == 64) return launch_g<64>(p, group, bf16, tk, tv, grid, warps, smem, stream);
-    if (head_dim == 128) return launch_g<128>(p, group, bf16, tk, tv, grid, warps, smem, stream);
+    if (head_dim == 64) return launch_g<64>(p, group, kv, tk, tv, grid, warps, smem, stream);
+    if (head_dim == 128) return launch_g<128>(p, group, kv, tk, tv, grid, warps, smem, stream);
     return cudaErrorInvalidValue;
 }
 

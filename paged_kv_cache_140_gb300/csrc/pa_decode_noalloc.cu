@@ -49,7 +49,8 @@ void *scratch_on_current_device() {
 }  // namespace
 
 PA_EXPORT pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype, const void *query,
-                                      const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                                      pa_dtype q_dtype, const void *k_cache, const void *v_cache,
+                                      pa_dtype kv_dtype, float k_scale, float v_scale,
                                       const int32_t *block_tables, int max_blocks_per_seq,
                                       const int32_t *context_lens, int max_context_len,
                                       int num_seqs, int num_heads, int num_kv_heads, int head_dim,
@@ -60,7 +61,7 @@ PA_EXPORT pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype, const void 
     if (need == static_cast<size_t>(-1) || need == 0) {
         // Rejected arguments, or nothing to split: pa_decode needs no
         // workspace (and reports the exact argument error).
-        return pa_decode(out, out_dtype, query, k_cache, v_cache, kv_dtype, block_tables,
+        return pa_decode(out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
                          max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_heads,
                          num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
                          nullptr, 0, err_flag, stream);
@@ -72,7 +73,7 @@ PA_EXPORT pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype, const void 
     // The array keeps the previous call's contents; nothing in the decode
     // workspace needs an initial value (every partial state is written before
     // the merge kernel reads it), so no clearing is needed.
-    return pa_decode(out, out_dtype, query, k_cache, v_cache, kv_dtype, block_tables,
+    return pa_decode(out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
                      max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size, scratch,
                      static_cast<size_t>(PA_NOALLOC_SCRATCH_BYTES), err_flag, stream);

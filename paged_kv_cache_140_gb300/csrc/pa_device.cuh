@@ -169,6 +169,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
+// Four e4m3 codes (bytes 0..3 of `w`) -> two f16x2 registers: `lo` holds
+// bytes 0, 1 and `hi` bytes 2, 3 (lower byte in the lower half).  Exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// Byte permute: output byte i = input byte sel[i] (nibble i of `sel`).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+    return d;
+}
+
+// Two floats -> two e4m3 codes (nearest-even, finite values saturate at
+// +-448, NaN stays NaN): `lo` in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start
 // launching / wait until the previous kernel's memory is visible.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -15,6 +15,9 @@ constexpr int kStageTokens = 16;
 // 7B, GQA, prefix sharing); deeper rings or more warps only add L2/HBM queueing.
 constexpr int kDefaultStages = 2;
 constexpr int kDefaultWarps128 = 8;
+// e4m3 caches: a stage carries half the bytes and more per-byte work, so
+// more warps per SM keep HBM busy (12 x 2 measured best).
+constexpr int kDefaultWarpsFp8 = 12;
 
 struct DecodeParams {
     void *out;
@@ -29,7 +32,8 @@ struct DecodeParams {
     int num_kv_heads;
     int block_size;
     int64_t num_blocks;
-    float scale_log2;            // softmax scale * log2(e)
+    float scale_log2;            // softmax scale * log2(e) * k_scale (k_scale = 1 for 16-bit caches)
+    float v_scale;               // e4m3 caches: V code scale (1 for 16-bit caches)
     int partition_size;          // tokens per partition, multiple of 16
     int max_partitions;          // partition slots per (seq, KV head) in the workspace
     float *ws_ml;                // [B * Hkv * max_partitions, G, 2]  (max, sum)
@@ -41,9 +45,11 @@ struct DecodeParams {
 
 // Shared memory the decode kernel needs for `warps` warps with `stages`
 // slots each and `num_seqs` sequences (including alignment slack).
-size_t decode_smem_bytes(int head_dim, int group, int warps, int stages, int num_seqs);
+size_t decode_smem_bytes(int head_dim, int group, int elem_bytes, int warps, int stages,
+                         int num_seqs);
 
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, bool bf16,
+// kv: 0 = f16 cache/query, 1 = bf16, 2 = e4m3 cache + f16 query, 3 = e4m3 + bf16.
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, int kv,
                           const CUtensorMap &tmap_k, const CUtensorMap &tmap_v, int grid,
                           int warps, size_t smem, cudaStream_t stream);
 
@@ -51,6 +57,14 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
                                      void *v_cache, const int64_t *slot_mapping,
                                      int64_t num_tokens, int64_t num_slots, int64_t row_bytes,
                                      int *err_flag, cudaStream_t stream);
+
+// Quantising variant: 16-bit rows (bf16 if `bf16`) -> e4m3 codes of
+// x / scale; `row_elems` elements per token row (a multiple of 8).
+cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, void *k_cache,
+                                         void *v_cache, const int64_t *slot_mapping,
+                                         int64_t num_tokens, int64_t num_slots, int64_t row_elems,
+                                         bool bf16, float k_scale, float v_scale, int *err_flag,
+                                         cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                                int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,

@@ -20,12 +20,20 @@ def half_tensor(bits: np.ndarray, dtype: str, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch_dtype(dtype)).to(device)
 
 
+def cache_tensor(b, bits, device="cuda"):
+    """The cache as a device tensor: 16-bit values, or e4m3 codes as uint8."""
+    import torch
+    if b.cache_dtype == "fp8":
+        return torch.from_numpy(np.ascontiguousarray(bits)).to(device)
+    return half_tensor(bits, b.cache_dtype, device)
+
+
 def to_device(b, device="cuda"):
     import torch
     return dict(
         q=half_tensor(b.q, b.dtype, device),
-        k_cache=half_tensor(b.k_cache, b.dtype, device),
-        v_cache=half_tensor(b.v_cache, b.dtype, device),
+        k_cache=cache_tensor(b, b.k_cache, device),
+        v_cache=cache_tensor(b, b.v_cache, device),
         key=half_tensor(b.key, b.dtype, device),
         value=half_tensor(b.value, b.dtype, device),
         slot_mapping=torch.from_numpy(b.slot_mapping).to(device),
@@ -44,12 +52,14 @@ def run_step(b, out_dtype=OUT_F32, partition_size=None, dev=None, device="cuda")
     err = pa.new_err_flag(device)
     if len(b.block_mapping):
         pa.copy_blocks(T["k_cache"], T["v_cache"], T["block_mapping"], err_flag=err)
-    pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"], err_flag=err)
+    pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"], err_flag=err,
+                         k_scale=b.k_scale, v_scale=b.v_scale)
     out = torch.empty(T["q"].shape, dtype=torch_dtype(out_dtype if out_dtype != "native" else b.dtype),
                       device=device)
     P = b.partition_size if partition_size is None else partition_size
     pa.decode(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"],
-              float(b.scale), max_context_len=b.max_context_len, partition_size=P, err_flag=err)
+              float(b.scale), max_context_len=b.max_context_len, partition_size=P, err_flag=err,
+              k_scale=b.k_scale, v_scale=b.v_scale)
     torch.cuda.synchronize()
     return out, T, pa.read_err_flag(err)
 
@@ -79,4 +89,6 @@ def assert_attention_close(out, ref: np.ndarray, out_dtype: str, what: str = "")
 
 def cache_bits(t) -> np.ndarray:
     import torch
+    if t.element_size() == 1:
+        return t.cpu().view(torch.uint8).numpy()
     return t.cpu().view(torch.int16).numpy().view(np.uint16)

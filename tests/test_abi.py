@@ -91,28 +91,32 @@ def test_argument_checks_return_before_touching_a_gpu(lib):
     from paged_kv_cache_140_gb300 import _lib as L
     nul = ctypes.c_void_p(0)
     # pa_decode: negative sizes, bad dtype, bad grouping, context bound beyond the table.
-    assert lib.pa_decode(nul, 2, nul, nul, nul, 1, nul, 8, nul, 100, -1, 4, 4, 64, 16, 64, 0.1, 0,
-                         nul, 0, nul, nul) == L.PA_ERR_INVALID_ARG
-    assert lib.pa_decode(nul, 2, nul, nul, nul, 2, nul, 8, nul, 100, 4, 4, 4, 64, 16, 64, 0.1, 0,
-                         nul, 0, nul, nul) == L.PA_ERR_INVALID_ARG
-    assert lib.pa_decode(nul, 2, nul, nul, nul, 1, nul, 8, nul, 100, 4, 12, 4, 64, 16, 64, 0.1, 0,
-                         nul, 0, nul, nul) == L.PA_ERR_UNSUPPORTED
-    assert lib.pa_decode(nul, 2, nul, nul, nul, 1, nul, 4, nul, 100, 4, 4, 4, 64, 16, 64, 0.1, 0,
-                         nul, 0, nul, nul) == L.PA_ERR_INVALID_ARG
-    assert lib.pa_decode(nul, 2, nul, nul, nul, 1, nul, 8, nul, 100, 4, 4, 4, 64, 16, 64,
-                         float("nan"), 0, nul, 0, nul, nul) == L.PA_ERR_INVALID_ARG
+    def dec(out_dt, q_dt, kv_dt, maxnb, maxctx, B, hq, hkv, d, scale=0.1, ks=1.0, vs=1.0, bs=16):
+        return lib.pa_decode(nul, out_dt, nul, q_dt, nul, nul, kv_dt, ks, vs, nul, maxnb, nul, maxctx, B, hq,
+                             hkv, d, bs, 64, scale, 0, nul, 0, nul, nul)
+    # pa_decode: negative sizes, bad dtype, bad grouping, context bound beyond the table.
+    assert dec(2, 1, 1, 8, 100, -1, 4, 4, 64) == L.PA_ERR_INVALID_ARG
+    assert dec(2, 2, 2, 8, 100, 4, 4, 4, 64) == L.PA_ERR_INVALID_ARG          # f32 query / cache
+    assert dec(2, 1, 1, 8, 100, 4, 12, 4, 64) == L.PA_ERR_UNSUPPORTED         # group of 3
+    assert dec(2, 1, 1, 4, 100, 4, 4, 4, 64) == L.PA_ERR_INVALID_ARG          # 100 > 4 * 16
+    assert dec(2, 1, 1, 8, 100, 4, 4, 4, 64, scale=float("nan")) == L.PA_ERR_INVALID_ARG
+    assert dec(2, 0, 1, 8, 100, 4, 4, 4, 64) == L.PA_ERR_UNSUPPORTED          # f16 query, bf16 cache
+    assert dec(2, 1, 3, 8, 100, 4, 4, 4, 64) == L.PA_ERR_UNSUPPORTED          # fp8 cache needs D 128
+    assert dec(2, 1, 3, 8, 100, 4, 4, 4, 128, ks=0.0) == L.PA_ERR_INVALID_ARG  # fp8 scale must be > 0
     # Null tensors with real work.
-    assert lib.pa_decode(nul, 2, nul, nul, nul, 1, nul, 8, nul, 100, 4, 4, 4, 64, 16, 64, 0.1, 0,
-                         nul, 0, nul, nul) == L.PA_ERR_INVALID_ARG
+    assert dec(2, 1, 1, 8, 100, 4, 4, 4, 64) == L.PA_ERR_INVALID_ARG
+    assert dec(2, 1, 3, 8, 100, 4, 4, 4, 128, ks=0.5, vs=0.5) == L.PA_ERR_INVALID_ARG
     # Empty batch is a no-op.
-    assert lib.pa_decode(nul, 2, nul, nul, nul, 1, nul, 8, nul, 100, 0, 4, 4, 64, 16, 64, 0.1, 0,
-                         nul, 0, nul, nul) == L.PA_OK
+    assert dec(2, 1, 1, 8, 100, 0, 4, 4, 64) == L.PA_OK
     # reshape_and_cache / copy_blocks.
-    assert lib.pa_reshape_and_cache(nul, nul, nul, nul, nul, 0, 64, 16, 4, 64, 0, nul, nul) == L.PA_OK
-    assert lib.pa_reshape_and_cache(nul, nul, nul, nul, nul, 3, 64, 16, 4, 64, 0, nul, nul) == \
-        L.PA_ERR_INVALID_ARG
-    assert lib.pa_reshape_and_cache(nul, nul, nul, nul, nul, 3, 64, 16, 4, 64, 2, nul, nul) == \
-        L.PA_ERR_INVALID_ARG
+    def rc(T, dt, cdt, ks=1.0, vs=1.0):
+        return lib.pa_reshape_and_cache(nul, nul, nul, nul, nul, T, 64, 16, 4, 64, dt, cdt, ks, vs, nul, nul)
+    assert rc(0, 0, 0) == L.PA_OK
+    assert rc(3, 0, 0) == L.PA_ERR_INVALID_ARG                # null tensors
+    assert rc(3, 2, 2) == L.PA_ERR_INVALID_ARG                # f32 rows
+    assert rc(3, 0, 1) == L.PA_ERR_UNSUPPORTED                # f16 rows into a bf16 cache
+    assert rc(3, 1, 3, ks=-1.0) == L.PA_ERR_INVALID_ARG       # fp8 scale must be > 0
+    assert rc(3, 1, 3, ks=0.25, vs=0.25) == L.PA_ERR_INVALID_ARG  # null tensors
     assert lib.pa_copy_blocks(nul, nul, nul, 0, 64, 16, 4, 64, 1, nul, nul) == L.PA_OK
     assert lib.pa_copy_blocks(nul, nul, nul, 2, 64, 16, 4, 64, 1, nul, nul) == L.PA_ERR_INVALID_ARG
     misaligned = ctypes.c_void_p(0x1008)

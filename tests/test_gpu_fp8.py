@@ -1,0 +1,95 @@
+"""GPU parity of the FP8 (e4m3) KV-cache path against the CPU oracle.
+
+The quantising reshape_and_cache must produce the oracle's codes bit for bit
+(code = e4m3(fp32(x) / scale), nearest-even, saturating); attention over the
+e4m3 cache must stay within 2e-3 of the oracle's fp64 result on the same codes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_140_gb300 import workloads as W
+
+from pa_harness import assert_attention_close, cache_bits, run_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_140_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+def check(b, out_dtype="f32", partition_size=None, caches=True):
+    assert b.cache_dtype == "fp8"
+    ref, kc, vc = oracle.decode_step(b)
+    out, T, flag = run_step(b, out_dtype=out_dtype, partition_size=partition_size)
+    assert flag == 0, f"err_flag {flag:#x}"
+    assert_attention_close(out, ref, b.dtype if out_dtype == "native" else out_dtype, b.name + "/fp8")
+    if caches:
+        assert np.array_equal(cache_bits(T["k_cache"]), kc), "k_cache codes differ from oracle"
+        assert np.array_equal(cache_bits(T["v_cache"]), vc), "v_cache codes differ from oracle"
+    return out
+
+
+CASES = [
+    ("13b", dict(num_seqs=24)),
+    ("7b", dict(num_seqs=6)),
+    ("gqa", dict(num_seqs=2, ctx_cap=12000)),
+    ("gqa32", dict(num_seqs=2, ctx_cap=12000)),
+    ("prefix", dict(groups=2)),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("out_dtype", ["f32", "native"])
+def test_fp8_workloads(name, kw, out_dtype):
+    check(W.make_batch(name, cache_dtype="fp8", **kw), out_dtype)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 4), (16, 2)])
+@pytest.mark.parametrize("qdt", ["f16", "bf16"])
+def test_fp8_groups_and_query_types(hq, hkv, qdt):
+    b = W.make_batch("7b", num_seqs=4, ctx_cap=700, num_heads=hq, num_kv_heads=hkv, dtype=qdt,
+                     cache_dtype="fp8")
+    check(b, "f32", partition_size=128)
+
+
+@pytest.mark.parametrize("P", [0, 16, 48, 512])
+def test_fp8_partition_sizes(P):
+    check(W.make_batch("13b", num_seqs=6, cache_dtype="fp8"), "f32", partition_size=P, caches=False)
+
+
+@pytest.mark.parametrize("bs", [8, 32])
+def test_fp8_block_sizes(bs):
+    check(W.make_batch("13b", num_seqs=8, block_size=bs, cache_dtype="fp8"), "f32",
+          partition_size=128 if bs == 8 else 0)
+
+
+def test_fp8_edge_lengths():
+    b = W.make_batch("7b", context_lens=[0, 1, 16, 17, 0, 2048, 255, 257], cache_dtype="fp8")
+    out = check(b, "f32")
+    o = out.cpu().numpy()
+    assert np.all(o[0] == 0) and np.all(o[4] == 0)
+
+
+def test_fp8_full_size_sampled():
+    b = W.make_batch("13b_fp8")
+    out, T, flag = run_step(b, out_dtype="native")
+    assert flag == 0
+    order = np.argsort(b.context_lens)
+    pick = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2]), 3, 77, 200})
+    sub = W.subset_batch(b, pick)
+    kc, vc, _ = oracle.reshape_and_cache_fp8(b.key, b.value, b.dtype, b.k_cache, b.v_cache, b.slot_mapping,
+                                             b.k_scale, b.v_scale)
+    ref = oracle.paged_attention_fp8(sub.q, b.dtype, kc, vc, b.k_scale, b.v_scale, sub.block_tables,
+                                     sub.context_lens, b.scale)
+    assert_attention_close(out[pick], ref, b.dtype, "13b_fp8 sampled")
+    rows = b.slot_mapping
+    gk = cache_bits(T["k_cache"]).reshape(-1, 40 * 128)
+    assert np.array_equal(gk[rows], kc.reshape(-1, 40 * 128)[rows])

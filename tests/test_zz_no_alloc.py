@@ -6,8 +6,8 @@ memory, or a deployment with a device-memory budget fixed at load time - so
 they cannot hand pa_decode a workspace.  pa_decode_noalloc keeps that
 workspace in a fixed scratch array inside the library instead.  These tests
 call it through the C ABI and check it against pa_decode on consecutive calls
-(the array keeps the previous call's contents, so each call must clear what
-has to start at zero), including calls whose workspace layouts differ.
+(the array keeps the previous call's contents, so nothing in it may be assumed
+to start clean), including calls whose workspace layouts differ.
 
 This file is named to be collected last.
 """
@@ -55,9 +55,10 @@ def _noalloc(torch, lib, b, T):
     out = torch.full(T["q"].shape, float("nan"), dtype=torch.float32, device="cuda")
     err = pa.new_err_flag()
     P = ctypes.c_void_p
+    dt = 1 if b.dtype == "bf16" else 0
     st = lib.pa_decode_noalloc(
-        P(out.data_ptr()), 2, P(T["q"].data_ptr()), P(T["k_cache"].data_ptr()), P(T["v_cache"].data_ptr()),
-        1 if b.dtype == "bf16" else 0, P(T["block_tables"].data_ptr()), T["block_tables"].shape[1],
+        P(out.data_ptr()), 2, P(T["q"].data_ptr()), dt, P(T["k_cache"].data_ptr()), P(T["v_cache"].data_ptr()),
+        dt, 1.0, 1.0, P(T["block_tables"].data_ptr()), T["block_tables"].shape[1],
         P(T["context_lens"].data_ptr()), b.max_context_len, b.num_seqs, b.num_heads, b.num_kv_heads,
         b.head_dim, b.block_size, b.num_blocks, float(b.scale), b.partition_size, P(err.data_ptr()),
         P(torch.cuda.current_stream().cuda_stream))
@@ -100,6 +101,6 @@ def test_noalloc_rejects_requests_beyond_the_scratch_limit(env):
     need = lib.pa_decode_workspace_size(256, 40, 40, 128, 16, 2048, 16)
     assert need > 32 * 1024 * 1024
     nul = ctypes.c_void_p(0)
-    st = lib.pa_decode_noalloc(nul, 2, nul, nul, nul, 1, nul, 128, nul, 2048, 256, 40, 40, 128, 16,
+    st = lib.pa_decode_noalloc(nul, 2, nul, 1, nul, nul, 1, 1.0, 1.0, nul, 128, nul, 2048, 256, 40, 40, 128, 16,
                                10000, 0.088, 16, nul, nul)
     assert st == L.PA_ERR_WORKSPACE
