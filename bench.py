@@ -526,6 +526,43 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args):
+    """swap_blocks bandwidth between the GPU cache and pinned host memory
+    (13B-shaped blocks: 16 tokens x 40 heads x 128 dims, bf16, K and V)."""
+    import torch
+
+    import paged_kv_cache_140_gb300 as pa
+    if not torch.cuda.is_available():
+        raise SystemExit("--swap needs a CUDA device")
+    n_gpu, n_swap = 8192, 2048
+    shape = (16, 40, 128)
+    gk = torch.randn((n_gpu,) + shape, device="cuda").to(torch.bfloat16)
+    gv = torch.randn((n_gpu,) + shape, device="cuda").to(torch.bfloat16)
+    hk = torch.empty((n_swap,) + shape, dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty((n_swap,) + shape, dtype=torch.bfloat16).pin_memory()
+    g = torch.Generator().manual_seed(140)
+    src = torch.randperm(n_gpu, generator=g)[:n_swap]
+    out_map = torch.stack([src, torch.arange(n_swap)], 1).to("cuda")
+    in_map = torch.stack([torch.arange(n_swap), torch.randperm(n_gpu, generator=g)[:n_swap]], 1).to("cuda")
+    nbytes = 2 * n_swap * 16 * 40 * 128 * 2
+    res = {}
+    for name, fn in (("swap_out", lambda: pa.swap_blocks(gk, gv, hk, hv, out_map)),
+                     ("swap_in", lambda: pa.swap_blocks(hk, hv, gk, gv, in_map))):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        res[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    print(json.dumps({"metric": "swap_blocks GPU<->pinned host GB/s", "blocks": n_swap,
+                      "bytes_per_call": nbytes, "steps": args.steps, **res}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -535,12 +572,15 @@ def main(argv=None):
     ap.add_argument("--workload", default="13b", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--swap", action="store_true", help="measure swap_blocks bandwidth instead")
     ap.add_argument("--clock-probe-s", type=float, default=2.0,
                     help="seconds of steps run under the clock sampler before the timed region")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_env()
+    if args.swap:
+        return run_swap(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -245,6 +245,30 @@ pa_status pa_copy_blocks(void *k_cache, void *v_cache,
                          int64_t num_blocks, int block_size, int num_kv_heads,
                          int head_dim, pa_dtype dtype, int *err_flag, void *stream);
 
+/*
+ * pa_swap_blocks -- copy whole blocks between two caches.
+ *
+ * Swap-mode preemption moves a preempted request's KV blocks from GPU memory
+ * to CPU memory and back when it resumes (Page B §5, strategy 1: swapping);
+ * the block table then names the blocks' new physical ids.  For every pair p:
+ *     dst_k[dst_p] = src_k[src_p],  dst_v[dst_p] = src_v[src_p]
+ * (whole blocks of block_size * num_kv_heads * head_dim elements of `dtype`),
+ * bit-exact.  src and dst are [src_num_blocks, ...] and [dst_num_blocks, ...]
+ * caches; either may live in page-locked host memory (cudaHostAlloc /
+ * cudaHostRegister, which the GPU reads and writes directly over the
+ * host link) and the other in device memory.  block_mapping [num_pairs, 2]
+ * int64 (src, dst) may be device or page-locked host memory.  Every pointer is
+ * checked with cudaPointerGetAttributes first: any other memory (e.g.
+ * pageable host memory) gives PA_ERR_INVALID_ARG and nothing is launched.
+ * Destinations must be distinct.  A pair with an id outside its cache is
+ * skipped and sets PA_FLAG_BAD_COPY_PAIR.
+ */
+pa_status pa_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                         const int64_t *block_mapping, int64_t num_pairs,
+                         int64_t src_num_blocks, int64_t dst_num_blocks,
+                         int block_size, int num_kv_heads, int head_dim, pa_dtype dtype,
+                         int *err_flag, void *stream);
+
 /* Host helper: synchronously read *err_flag (device), optionally clear it,
  * and map it to PA_OK / PA_ERR_DEVICE_BOUNDS.  `flag_out` (nullable, host)
  * receives the raw bits. */

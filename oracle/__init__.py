@@ -67,6 +67,8 @@ def _load():
         lib.oracle_paged_attention_fp8.argtypes = [P, P, i32, P, P, dbl, dbl, P, i32, P, i32, i32, i32,
                                                    i32, i32, dbl]
         lib.oracle_paged_attention_fp8.restype = None
+        lib.oracle_swap_blocks.argtypes = [P, P, P, P, P, i64, i64, i64, i64]
+        lib.oracle_swap_blocks.restype = i64
         _lib = lib
     return _lib
 
@@ -237,3 +239,17 @@ def copy_blocks_bytes(k_cache, v_cache, block_mapping):
     v16 = np.ascontiguousarray(v_cache).view(np.uint16).reshape(k16.shape)
     a, b, bad = copy_blocks(k16, v16, block_mapping)
     return a.view(kc.dtype).reshape(shape), b.view(kc.dtype).reshape(shape), bad
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping):
+    """Copy whole blocks src -> dst between two caches (copies of the destination
+    are returned).  Returns (dst_k_after, dst_v_after, number_of_skipped_pairs)."""
+    lib = _load()
+    sk, sv = np.ascontiguousarray(src_k), np.ascontiguousarray(src_v)
+    dk, dv = np.array(dst_k, copy=True, order="C"), np.array(dst_v, copy=True, order="C")
+    assert sk.dtype == dk.dtype and sk.shape[1:] == dk.shape[1:]
+    bm = _c(np.asarray(block_mapping).reshape(-1, 2), np.int64)
+    block_bytes = int(np.prod(sk.shape[1:])) * sk.itemsize
+    bad = lib.oracle_swap_blocks(_ptr(sk), _ptr(sv), _ptr(dk), _ptr(dv), _ptr(bm), len(bm), sk.shape[0],
+                                 dk.shape[0], block_bytes)
+    return dk, dv, int(bad)

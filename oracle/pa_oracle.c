@@ -410,3 +410,25 @@ void oracle_e4m3_encode_array(const float *x, uint8_t *out, int64_t n) {
 void oracle_e4m3_decode_array(const uint8_t *c, double *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
 }
+
+/* ------------------------------------------------------------------------
+ * swap_blocks: copy whole blocks between two caches (swap-mode preemption:
+ * a preempted request's KV blocks go to CPU memory and come back later,
+ * "vLLM 核心：PagedAttention 与 Continuous Batching", §5 strategy 1).
+ * For each pair (src, dst), in pair order: dst_k[dst] = src_k[src],
+ * dst_v[dst] = src_v[src].  `block_bytes` bytes per block and tensor.
+ * Pairs with an id outside its cache are skipped and counted.
+ * ------------------------------------------------------------------------ */
+int64_t oracle_swap_blocks(const uint8_t *src_k, const uint8_t *src_v, uint8_t *dst_k, uint8_t *dst_v,
+                           const int64_t *block_mapping, int64_t num_pairs, int64_t src_num_blocks,
+                           int64_t dst_num_blocks, int64_t block_bytes) {
+    int64_t bad = 0;
+    for (int64_t p = 0; p < num_pairs; ++p) {
+        int64_t src = block_mapping[2 * p];
+        int64_t dst = block_mapping[2 * p + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) { ++bad; continue; }
+        memcpy(dst_k + dst * block_bytes, src_k + src * block_bytes, (size_t)block_bytes);
+        memcpy(dst_v + dst * block_bytes, src_v + src * block_bytes, (size_t)block_bytes);
+    }
+    return bad;
+}

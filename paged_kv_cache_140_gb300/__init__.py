@@ -22,7 +22,7 @@ from . import _lib
 from ._lib import (FLAG_BAD_BLOCK_ID, FLAG_BAD_CONTEXT_LEN, FLAG_BAD_COPY_PAIR, FLAG_BAD_SLOT,
                    FLAG_TIMEOUT, PA_BF16, PA_F16, PA_F32, PA_FP8_E4M3, PagedAttentionError)
 
-__all__ = ["reshape_and_cache", "decode", "copy_blocks", "decode_workspace_size",
+__all__ = ["reshape_and_cache", "decode", "copy_blocks", "swap_blocks", "decode_workspace_size",
            "decode_partition_size", "DecodeWorkspace", "new_err_flag", "read_err_flag",
            "PagedAttentionError", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK_ID", "FLAG_BAD_CONTEXT_LEN",
            "FLAG_BAD_COPY_PAIR", "FLAG_TIMEOUT", "library_path"]
@@ -125,6 +125,27 @@ def copy_blocks(k_cache, v_cache, block_mapping, err_flag=None) -> None:
                                     block_mapping.shape[0], nb, bs, hkv, d, _cache_code(k_cache),
                                     _ptr(err_flag), _stream(k_cache.device))
     _lib.check(st, "pa_copy_blocks")
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, err_flag=None) -> None:
+    """Copy whole blocks src -> dst between two caches (for swap-mode
+    preemption); either cache may be a pinned host tensor (``pin_memory()``),
+    the other a CUDA tensor.  ``block_mapping`` [P, 2] int64 on the GPU."""
+    torch = _torch()
+    for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v)):
+        _need(t.is_contiguous(), f"{n} must be contiguous")
+        _need(t.is_cuda or t.is_pinned(), f"{n} must be a CUDA tensor or pinned host memory")
+    _cuda_contig("block_mapping", block_mapping)
+    _need(block_mapping.dtype == torch.int64 and block_mapping.dim() == 2 and block_mapping.shape[1] == 2,
+          "block_mapping must be int64 [P, 2]")
+    _need(src_k.shape[1:] == dst_k.shape[1:] and src_k.dtype == dst_k.dtype, "cache shapes differ")
+    _need(src_v.shape == src_k.shape and dst_v.shape == dst_k.shape, "K and V caches differ")
+    nb_src, bs, hkv, d = src_k.shape
+    device = block_mapping.device
+    st = _lib.load().pa_swap_blocks(_ptr(src_k), _ptr(src_v), _ptr(dst_k), _ptr(dst_v), _ptr(block_mapping),
+                                    block_mapping.shape[0], nb_src, dst_k.shape[0], bs, hkv, d,
+                                    _cache_code(src_k), _ptr(err_flag), _stream(device))
+    _lib.check(st, "pa_swap_blocks")
 
 
 def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,

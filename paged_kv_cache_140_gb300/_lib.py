@@ -31,6 +31,7 @@ SIGNATURES = {
     "pa_decode_noalloc": (_I, [_P, _I, _P, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64,
                                _F, _I, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _I, _I, _I, _P, _P]),
+    "pa_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P, _P]),
     "pa_check_err_flag": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int), _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_version": (_I, []),

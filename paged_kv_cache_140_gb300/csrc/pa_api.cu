@@ -155,6 +155,27 @@ bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The address a kernel on the current device may use for `p`: device or
+// managed memory as is, page-locked host memory through its mapped device
+// pointer.  False for anything else (e.g. pageable host memory), which the
+// caller rejects before any launch.
+bool device_address(const void *p, const void **out) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *out = p;
+        return true;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+        *out = a.devicePointer;
+        return true;
+    }
+    return false;
+}
+
 }  // namespace
 
 PA_EXPORT const char *pa_status_string(pa_status s) {
@@ -215,8 +236,34 @@ PA_EXPORT pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *
     if (num_pairs == 0) return PA_OK;
     if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
-    cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, num_blocks,
-                                           block_bytes, err_flag,
+    cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, k_cache, v_cache, block_mapping, num_pairs,
+                                           num_blocks, num_blocks, block_bytes, err_flag,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT pa_status pa_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                                   const int64_t *block_mapping, int64_t num_pairs,
+                                   int64_t src_num_blocks, int64_t dst_num_blocks, int block_size,
+                                   int num_kv_heads, int head_dim, pa_dtype dtype, int *err_flag,
+                                   void *stream) {
+    if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_size <= 0 ||
+        num_kv_heads <= 0 || head_dim <= 0 || !cache_dtype_ok(dtype))
+        return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes =
+        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * elem_bytes(dtype);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+        return PA_ERR_INVALID_ARG;
+    const void *sk, *sv, *dk, *dv, *bm;
+    if (!device_address(src_k, &sk) || !device_address(src_v, &sv) || !device_address(dst_k, &dk) ||
+        !device_address(dst_v, &dv) || !device_address(block_mapping, &bm))
+        return PA_ERR_INVALID_ARG;
+    cudaError_t e = pa::launch_copy_blocks(sk, sv, const_cast<void *>(dk), const_cast<void *>(dv),
+                                           static_cast<const int64_t *>(bm), num_pairs, src_num_blocks,
+                                           dst_num_blocks, block_bytes, err_flag,
                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -83,25 +83,27 @@ __global__ void __launch_bounds__(128)
 }
 
 // grid.x: copy pairs (grid-stride), grid.y: slices of the block; each thread
-// moves 4 chunks of 16 bytes of K and of V per iteration.
+// moves 4 chunks of 16 bytes of K and of V per iteration.  Source and
+// destination are separate caches (swap_blocks: e.g. GPU and pinned host
+// memory) or the same one (copy_blocks; its pairs never overlap).
 __global__ void __launch_bounds__(256)
-    copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+    copy_blocks_kernel(const uint4 *src_k, const uint4 *src_v, uint4 *dst_k, uint4 *dst_v,
                        const int64_t *__restrict__ block_mapping, int64_t num_pairs,
-                       int64_t num_blocks, int64_t block16, int *err_flag) {
+                       int64_t src_blocks, int64_t dst_blocks, int64_t block16, int *err_flag) {
     const int64_t slice = (block16 + gridDim.y - 1) / gridDim.y;
     const int64_t beg = blockIdx.y * slice;
     const int64_t end = min(block16, beg + slice);
     for (int64_t pr = blockIdx.x; pr < num_pairs; pr += gridDim.x) {
         const int64_t src = block_mapping[2 * pr];
         const int64_t dst = block_mapping[2 * pr + 1];
-        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
             if (threadIdx.x == 0 && blockIdx.y == 0) report(err_flag, 0x8 /* PA_FLAG_BAD_COPY_PAIR */);
             continue;
         }
-        const uint4 *ks = k_cache + src * block16;
-        const uint4 *vs = v_cache + src * block16;
-        uint4 *kd = k_cache + dst * block16;
-        uint4 *vd = v_cache + dst * block16;
+        const uint4 *ks = src_k + src * block16;
+        const uint4 *vs = src_v + src * block16;
+        uint4 *kd = dst_k + dst * block16;
+        uint4 *vd = dst_v + dst * block16;
         int64_t i = beg + threadIdx.x;
         const int64_t step = blockDim.x;
         for (; i + 3 * step < end; i += 4 * step) {
@@ -164,9 +166,10 @@ cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, voi
     return cudaGetLastError();
 }
 
-cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
-                               int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
-                               int *err_flag, cudaStream_t stream) {
+cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                               const int64_t *block_mapping, int64_t num_pairs, int64_t src_blocks,
+                               int64_t dst_blocks, int64_t block_bytes, int *err_flag,
+                               cudaStream_t stream) {
     const int64_t block16 = block_bytes / 16;
     const int threads = 256;
     const int sms = sm_count();
@@ -182,9 +185,9 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *bloc
     if (slices > 65535) slices = 65535;
     const int64_t gx = num_pairs < 65535LL * 16 ? num_pairs : 65535LL * 16;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(slices));
-    copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4 *>(k_cache),
-                                                     static_cast<uint4 *>(v_cache), block_mapping,
-                                                     num_pairs, num_blocks, block16, err_flag);
+    copy_blocks_kernel<<<grid, threads, 0, stream>>>(
+        static_cast<const uint4 *>(src_k), static_cast<const uint4 *>(src_v), static_cast<uint4 *>(dst_k),
+        static_cast<uint4 *>(dst_v), block_mapping, num_pairs, src_blocks, dst_blocks, block16, err_flag);
     return cudaGetLastError();
 }
 

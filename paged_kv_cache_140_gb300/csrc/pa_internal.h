@@ -66,8 +66,10 @@ cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, voi
                                          bool bf16, float k_scale, float v_scale, int *err_flag,
                                          cudaStream_t stream);
 
-cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
-                               int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
-                               int *err_flag, cudaStream_t stream);
+// Whole-block copies src -> dst (the same cache for copy_blocks).
+cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                               const int64_t *block_mapping, int64_t num_pairs, int64_t src_blocks,
+                               int64_t dst_blocks, int64_t block_bytes, int *err_flag,
+                               cudaStream_t stream);
 
 }  // namespace pa

@@ -352,3 +352,24 @@ def test_pins_catch_planted_mistakes(mutant):
                                    args[4].ctypes.data, 3, 4, 2, 8, 4, 0.35)
         want = brute.paged_attention(q, k, v, "f16", t, ctx, 0.35)
         assert not np.allclose(out, want, rtol=1e-9, atol=1e-9, equal_nan=False)
+
+
+def test_swap_blocks_between_two_caches(oracle_lib):
+    rng = np.random.default_rng(17)
+    gpu = rng.integers(0, 1 << 16, size=(9, 4, 2, 8), dtype=np.uint16)
+    gpv = rng.integers(0, 1 << 16, size=(9, 4, 2, 8), dtype=np.uint16)
+    host_k = np.zeros((5, 4, 2, 8), dtype=np.uint16)
+    host_v = np.zeros_like(host_k)
+    out_map = np.array([[3, 0], [7, 4], [1, 2], [8, 9]], dtype=np.int64)   # last pair out of range
+    hk, hv, bad = oracle_lib.swap_blocks(gpu, gpv, host_k, host_v, out_map)
+    assert bad == 1
+    want_k, want_v = host_k.copy(), host_v.copy()
+    for s, d in out_map[:3]:
+        want_k[d], want_v[d] = gpu[s], gpv[s]
+    assert np.array_equal(hk, want_k) and np.array_equal(hv, want_v)
+    # ... and back in, to other physical blocks.
+    in_map = np.array([[0, 5], [4, 6], [2, 0]], dtype=np.int64)
+    gk2, gv2, bad = oracle_lib.swap_blocks(hk, hv, gpu, gpv, in_map)
+    assert bad == 0
+    assert np.array_equal(gk2[5], gpu[3]) and np.array_equal(gk2[6], gpu[7]) and np.array_equal(gk2[0], gpu[1])
+    assert np.array_equal(gv2[5], gpv[3]) and np.array_equal(np.delete(gk2, [0, 5, 6], 0), np.delete(gpu, [0, 5, 6], 0))
