@@ -236,9 +236,29 @@ def run_ours(args, world, rank, local):
                                      b.max_context_len, b.partition_size) > 0
     stream = torch.cuda.current_stream(device)
 
+    fused = args.fused and not has_pairs and len(b.slot_mapping) == int((b.context_lens > 0).sum())
+    if fused:
+        has = torch.from_numpy(np.nonzero(b.context_lens > 0)[0]).to(device)
+        T["key_rows"] = torch.zeros((b.num_seqs, b.num_kv_heads, b.head_dim), dtype=T["key"].dtype,
+                                    device=device)
+        T["value_rows"] = torch.zeros_like(T["key_rows"])
+        T["key_rows"][has] = T["key"]
+        T["value_rows"][has] = T["value"]
+
     def step(ev=None):
         if has_pairs:
             pa.copy_blocks(T["k_cache"], T["v_cache"], T["block_mapping"])
+        if fused:
+            # reshape_and_cache fused into the decode launch
+            if ev is not None:
+                ev[0].record(stream)
+            pa.decode_append(out, T["q"], T["key_rows"], T["value_rows"], T["k_cache"], T["v_cache"],
+                             T["block_tables"], T["context_lens"], float(b.scale),
+                             max_context_len=b.max_context_len, partition_size=b.partition_size,
+                             workspace=ws, k_scale=b.k_scale, v_scale=b.v_scale)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"],
                              k_scale=b.k_scale, v_scale=b.v_scale)
         if ev is not None:
@@ -377,7 +397,8 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": int(d2h),
                 "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens -> device, "
                         "the step, output -> pinned host, stream sync; the KV cache stays resident"},
-        "gpu_launches": K * (2 + (1 if has_pairs else 0) + (1 if split else 0)),
+        "gpu_launches": K * ((1 if fused else 2) + (1 if has_pairs else 0) + (1 if split else 0)),
+        "fused_append": bool(fused),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -573,6 +594,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--swap", action="store_true", help="measure swap_blocks bandwidth instead")
+    ap.add_argument("--fused", action="store_true",
+                    help="run the step's reshape_and_cache inside the decode launch (pa_decode_append)")
     ap.add_argument("--clock-probe-s", type=float, default=2.0,
                     help="seconds of steps run under the clock sampler before the timed region")
     args = ap.parse_args(argv)

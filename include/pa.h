@@ -184,6 +184,36 @@ pa_status pa_decode(void *out, pa_dtype out_dtype,
                     int *err_flag, void *stream);
 
 /*
+ * pa_decode_append -- reshape_and_cache of the step's new token fused with
+ * pa_decode, in one launch.
+ *
+ * Each decode step appends one token per sequence and then attends over the
+ * context including it (Page C §2.3 steps 1-3; Page A §二).  Here the new
+ * token of sequence s is position context_lens[s] - 1: its K/V rows
+ *   key, value : [num_seqs, num_kv_heads, head_dim], q_dtype
+ * are written to the slot the block table gives for that position,
+ *   block_tables[s][(ctx - 1) / bs] * bs + (ctx - 1) % bs,
+ * (quantised as by pa_reshape_and_cache for an FP8 cache) and the attention
+ * uses them; the result equals pa_reshape_and_cache with that slot mapping
+ * followed by pa_decode, and the caches are bit-identical afterwards.  All
+ * other arguments and rules are those of pa_decode; the caches are written.
+ * A sequence with context length 0 appends nothing.  The last block of every
+ * sequence must be private to it (copy shared blocks first, pa_copy_blocks).
+ */
+pa_status pa_decode_append(void *out, pa_dtype out_dtype,
+                           const void *query, pa_dtype q_dtype,
+                           const void *key, const void *value,
+                           void *k_cache, void *v_cache, pa_dtype kv_dtype,
+                           float k_scale, float v_scale,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *context_lens, int max_context_len,
+                           int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                           int block_size, int64_t num_blocks, float scale,
+                           int partition_size,
+                           void *workspace, size_t workspace_bytes,
+                           int *err_flag, void *stream);
+
+/*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this call; it exists for callers of this

@@ -22,7 +22,7 @@ from . import _lib
 from ._lib import (FLAG_BAD_BLOCK_ID, FLAG_BAD_CONTEXT_LEN, FLAG_BAD_COPY_PAIR, FLAG_BAD_SLOT,
                    FLAG_TIMEOUT, PA_BF16, PA_F16, PA_F32, PA_FP8_E4M3, PagedAttentionError)
 
-__all__ = ["reshape_and_cache", "decode", "copy_blocks", "swap_blocks", "decode_workspace_size",
+__all__ = ["reshape_and_cache", "decode", "decode_append", "copy_blocks", "swap_blocks", "decode_workspace_size",
            "decode_partition_size", "DecodeWorkspace", "new_err_flag", "read_err_flag",
            "PagedAttentionError", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK_ID", "FLAG_BAD_CONTEXT_LEN",
            "FLAG_BAD_COPY_PAIR", "FLAG_TIMEOUT", "library_path"]
@@ -226,3 +226,40 @@ def decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: floa
                                float(scale), int(partition_size), _ptr(buf), nbytes, _ptr(err_flag),
                                _stream(query.device))
     _lib.check(st, "pa_decode")
+
+
+def decode_append(out, query, key, value, k_cache, v_cache, block_tables, context_lens, scale: float,
+                  max_context_len: int | None = None, partition_size: int = 0, workspace=None,
+                  err_flag=None, k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+    """reshape_and_cache of each sequence's new token (position context_lens[s] - 1,
+    rows ``key``/``value`` [B, Hkv, D]) fused with :func:`decode`, one launch."""
+    torch = _torch()
+    for n, t in (("out", out), ("query", query), ("key", key), ("value", value), ("k_cache", k_cache),
+                 ("v_cache", v_cache), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(query.dim() == 3 and out.shape == query.shape, "query/out must be [B, Hq, D]")
+    _need(k_cache.dim() == 4 and v_cache.shape == k_cache.shape and k_cache.dtype == v_cache.dtype,
+          "caches must be [NB, bs, Hkv, D] of one dtype")
+    B, Hq, D = query.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    _need(d2 == D and key.shape == (B, hkv, D) and value.shape == key.shape, "key/value must be [B, Hkv, D]")
+    _need(key.dtype == value.dtype == query.dtype, "key/value must have the query's dtype")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B,
+          "block_tables must be int32 [B, maxNB]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == B, "context_lens must be int32 [B]")
+    maxnb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = maxnb * bs
+    ws_bytes = decode_workspace_size(B, Hq, hkv, D, bs, max_context_len, partition_size)
+    if workspace is None:
+        wkey = (query.device.index, torch.cuda.current_stream(query.device).cuda_stream)
+        workspace = _default_ws.setdefault(wkey, DecodeWorkspace(query.device))
+    buf = workspace.get(ws_bytes) if isinstance(workspace, DecodeWorkspace) else workspace
+    nbytes = 0 if buf is None else buf.numel() * buf.element_size()
+    st = _lib.load().pa_decode_append(_ptr(out), _dtype_code(out, allow_f32=True), _ptr(query),
+                                      _dtype_code(query), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                      _cache_code(k_cache), float(k_scale), float(v_scale), _ptr(block_tables),
+                                      maxnb, _ptr(context_lens), int(max_context_len), B, Hq, hkv, D, bs, nb,
+                                      float(scale), int(partition_size), _ptr(buf), nbytes, _ptr(err_flag),
+                                      _stream(query.device))
+    _lib.check(st, "pa_decode_append")

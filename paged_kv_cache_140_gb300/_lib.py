@@ -28,6 +28,8 @@ SIGNATURES = {
     "pa_decode_partition_size": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "pa_decode": (_I, [_P, _I, _P, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64, _F,
                        _I, _P, _SZ, _P, _P]),
+    "pa_decode_append": (_I, [_P, _I, _P, _I, _P, _P, _P, _P, _I, _F, _F, _P, _I, _P, _I, _I, _I, _I, _I, _I,
+                              _I64, _F, _I, _P, _SZ, _P, _P]),
     "pa_decode_noalloc": (_I, [_P, _I, _P, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64,
                                _F, _I, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _I, _I, _I, _P, _P]),

@@ -298,9 +298,13 @@ PA_EXPORT pa_status pa_decode_workspace_init(void *workspace, size_t workspace_b
                : PA_ERR_CUDA;
 }
 
-PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
-                              const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
-                              float k_scale, float v_scale,
+namespace {
+
+// pa_decode and pa_decode_append share everything but the new rows.
+pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                      const void *new_k, const void *new_v,
+                      const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                      float k_scale, float v_scale,
                               const int32_t *block_tables, int max_blocks_per_seq,
                               const int32_t *context_lens, int max_context_len, int num_seqs,
                               int num_heads, int num_kv_heads, int head_dim, int block_size,
@@ -336,6 +340,8 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, 
     if (num_seqs == 0) return PA_OK;
     if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
         return PA_ERR_INVALID_ARG;
+    if ((new_k == nullptr) != (new_v == nullptr)) return PA_ERR_INVALID_ARG;
+    if (new_k && (!aligned16(new_k) || !aligned16(new_v))) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
     if (w.bytes > 0 && (workspace == nullptr || workspace_bytes < w.bytes || !aligned16(workspace)))
@@ -385,12 +391,53 @@ PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, 
     p.ws_acc = w.bytes ? reinterpret_cast<float *>(ws + w.acc_off) : nullptr;
     p.err_flag = err_flag;
     p.stages = stages;
+    p.new_k = new_k;
+    p.new_v = new_v;
+    p.k_cache_w = const_cast<void *>(k_cache);
+    p.v_cache_w = const_cast<void *>(v_cache);
+    p.k_scale_w = k_scale;
+    p.v_scale_w = v_scale;
     p.interleave = tune.interleave;
 
     const int kv = fp8 ? (q_dtype == PA_F16 ? 2 : 3) : (kv_dtype == PA_BF16 ? 1 : 0);
     cudaError_t e = pa::launch_decode(p, head_dim, G, kv, tk, tv, dev.sms, warps,
                                       smem_used, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+PA_EXPORT pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                              const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                              float k_scale, float v_scale, const int32_t *block_tables,
+                              int max_blocks_per_seq, const int32_t *context_lens,
+                              int max_context_len, int num_seqs, int num_heads, int num_kv_heads,
+                              int head_dim, int block_size, int64_t num_blocks, float scale,
+                              int partition_size, void *workspace, size_t workspace_bytes,
+                              int *err_flag, void *stream) {
+    return decode_impl(out, out_dtype, query, q_dtype, nullptr, nullptr, k_cache, v_cache, kv_dtype,
+                       k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens,
+                       max_context_len, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, scale, partition_size, workspace, workspace_bytes, err_flag,
+                       stream);
+}
+
+PA_EXPORT pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *query,
+                                     pa_dtype q_dtype, const void *key, const void *value,
+                                     void *k_cache, void *v_cache, pa_dtype kv_dtype, float k_scale,
+                                     float v_scale, const int32_t *block_tables,
+                                     int max_blocks_per_seq, const int32_t *context_lens,
+                                     int max_context_len, int num_seqs, int num_heads,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     int64_t num_blocks, float scale, int partition_size,
+                                     void *workspace, size_t workspace_bytes, int *err_flag,
+                                     void *stream) {
+    if (num_seqs > 0 && (key == nullptr || value == nullptr)) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, out_dtype, query, q_dtype, key, value, k_cache, v_cache, kv_dtype,
+                       k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens,
+                       max_context_len, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, scale, partition_size, workspace, workspace_bytes, err_flag,
+                       stream);
 }
 
 PA_EXPORT pa_status pa_check_err_flag(int *err_flag, int clear, int *flag_out, void *stream) {

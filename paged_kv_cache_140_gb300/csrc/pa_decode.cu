@@ -408,6 +408,13 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
     uint32_t qf[KS][2];          // query B fragments for the item
     float acc[MT][4];            // O^T accumulators
     float m_run[2], l_run[2];    // running max (log2 domain) and sum, heads 2t, 2t+1
+    // Fused append (p.new_k != nullptr): the item that holds a sequence's last
+    // position (this step's token) patches that row into its shared-memory
+    // tile and writes it to the cache.  nj: the stage holding it (-1: none).
+    const bool append = p.new_k != nullptr;
+    int nj = -1, nrow = 0, npos = 0;
+    int32_t nid = -1;       // block id of the new token (loaded at item start, used later)
+    uint2 nk = make_uint2(0u, 0u), nv = make_uint2(0u, 0u);   // this lane's 4 elements
 
     int inflight = 0;
     for (int k = 0; k < S && more; ++k) {
@@ -432,6 +439,23 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
         const StageMeta m = meta[slot];
 
         if (m.j == 0) {
+            nj = -1;
+            if (append && m.part == m.nparts - 1 && ctx_s[m.s] > 0) {
+                const int pos = ctx_s[m.s] - 1;
+                const int rel = pos - m.part * P;
+                nj = rel / kStageTokens;
+                nrow = rel % kStageTokens;
+                npos = pos;
+                nid = __ldg(p.block_tables + static_cast<int64_t>(m.s) * p.max_blocks_per_seq + pos / bs);
+                const int64_t src = (static_cast<int64_t>(m.s) * Hkv + m.kvh) * D + 4 * lane;
+                if constexpr (D == 128) {
+                    nk = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.new_k) + src));
+                    nv = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.new_v) + src));
+                } else if (lane < 16) {
+                    nk = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.new_k) + src));
+                    nv = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.new_v) + src));
+                }
+            }
             // New item: the query's B fragments straight from the slot (16-bit).
             const uint32_t *qw = reinterpret_cast<const uint32_t *>(sp + L::kQOffset);
             if constexpr (!kFp8) {
@@ -464,6 +488,38 @@ __global__ void __launch_bounds__(kMaxThreads<D>, 1)
             }
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        }
+
+        if (m.j == nj && ((m.mask >> nrow) & 1) && nid >= 0 && nid < p.num_blocks) {
+            // This stage holds the step's new token: put its K/V row into the
+            // tile (in place of whatever the cache slot held) and into the cache.
+            const int64_t nslot = static_cast<int64_t>(nid) * bs + npos % bs;
+            const int64_t row_off = (nslot * Hkv + m.kvh) * D;
+            if constexpr (kFp8) {
+                const float2 a = Half2x<kQBf16>::to_float2(nk.x), b = Half2x<kQBf16>::to_float2(nk.y);
+                const float2 c2 = Half2x<kQBf16>::to_float2(nv.x), d2 = Half2x<kQBf16>::to_float2(nv.y);
+                const uint32_t ck = f32x2_to_e4m3x2(__fdiv_rn(a.x, p.k_scale_w), __fdiv_rn(a.y, p.k_scale_w)) |
+                                    (f32x2_to_e4m3x2(__fdiv_rn(b.x, p.k_scale_w), __fdiv_rn(b.y, p.k_scale_w)) << 16);
+                const uint32_t cv = f32x2_to_e4m3x2(__fdiv_rn(c2.x, p.v_scale_w), __fdiv_rn(c2.y, p.v_scale_w)) |
+                                    (f32x2_to_e4m3x2(__fdiv_rn(d2.x, p.v_scale_w), __fdiv_rn(d2.y, p.v_scale_w)) << 16);
+                const int off = nrow * kRowBytes + (((lane >> 2) ^ (nrow & 7)) << 4) + (lane & 3) * 4;
+                *reinterpret_cast<uint32_t *>(sp + off) = ck;
+                *reinterpret_cast<uint32_t *>(sp + L::kVOffset + off) = cv;
+                reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.k_cache_w) + row_off)[lane] = ck;
+                reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.v_cache_w) + row_off)[lane] = cv;
+            } else {
+                if (D == 128 || lane < 16) {
+                    const int hr = D == 128 ? (lane >> 4) : 0, cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
+                    const int off = hr * kRegionBytes + nrow * kRowBytes + ((cc ^ (nrow & 7)) << 4) + sub;
+                    *reinterpret_cast<uint2 *>(sp + off) = nk;
+                    *reinterpret_cast<uint2 *>(sp + L::kVOffset + off) = nv;
+                    uint2 *kd = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.k_cache_w) + row_off);
+                    uint2 *vd = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.v_cache_w) + row_off);
+                    kd[lane] = nk;
+                    vd[lane] = nv;
+                }
+            }
+            __syncwarp();
         }
 
         // ---- QK^T: 16 tokens x 8 heads, two accumulators over the dim steps ----

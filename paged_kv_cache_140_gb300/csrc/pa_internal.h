@@ -39,6 +39,15 @@ struct DecodeParams {
     float *ws_ml;                // [B * Hkv * max_partitions, G, 2]  (max, sum)
     float *ws_acc;               // [B * Hkv * max_partitions, G, D]
     int *err_flag;
+    // Fused append (pa_decode_append): the step's new K/V rows, one per
+    // sequence [B, Hkv, D] in the query's 16-bit type, written at position
+    // context_lens[s] - 1 into the caches below; nullptr for plain decode.
+    const void *new_k;
+    const void *new_v;
+    void *k_cache_w;
+    void *v_cache_w;
+    float k_scale_w;             // e4m3 caches: quantisation scales of the new rows
+    float v_scale_w;
     int stages;                  // shared-memory slots per warp (ring depth)
     int interleave;              // 1: a CTA's warps take every nw-th item of the CTA's range
 };
