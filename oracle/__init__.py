@@ -253,3 +253,27 @@ def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping):
     bad = lib.oracle_swap_blocks(_ptr(sk), _ptr(sv), _ptr(dk), _ptr(dv), _ptr(bm), len(bm), sk.shape[0],
                                  dk.shape[0], block_bytes)
     return dk, dv, int(bad)
+
+
+# ------------------------------------------------------ prefill over paged KV
+
+def prefill_attention(q, k_cache, v_cache, dtype: str, block_tables, context_lens, cu_seqlens_q, scale):
+    """Causal attention of each sequence's new tokens over its paged context.
+
+    Sequence s owns query rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 (its last
+    q_len_s tokens); query token i sits at position ctx_s - q_len_s + i and
+    attends positions 0 .. that position.  By that definition each query token
+    is a decode query over a context of (position + 1) tokens, which is how it
+    is evaluated here.  q: uint16 [Tq, Hq, D].  Returns float64 [Tq, Hq, D]."""
+    bt = np.asarray(block_tables)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    rows, lens = [], []
+    for s in range(len(ctx)):
+        ql = int(cu[s + 1] - cu[s])
+        for i in range(ql):
+            rows.append(s)
+            lens.append(int(ctx[s]) - ql + i + 1)
+    if not rows:
+        return np.zeros((0,) + tuple(np.shape(q)[1:]))
+    return paged_attention(q, k_cache, v_cache, dtype, bt[rows], np.asarray(lens, dtype=np.int32), scale)

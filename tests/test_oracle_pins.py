@@ -373,3 +373,45 @@ def test_swap_blocks_between_two_caches(oracle_lib):
     assert bad == 0
     assert np.array_equal(gk2[5], gpu[3]) and np.array_equal(gk2[6], gpu[7]) and np.array_equal(gk2[0], gpu[1])
     assert np.array_equal(gv2[5], gpv[3]) and np.array_equal(np.delete(gk2, [0, 5, 6], 0), np.delete(gpu, [0, 5, 6], 0))
+
+
+def test_prefill_is_causal_attention_over_the_paged_context(oracle_lib):
+    """Brute force: each query token attends exactly the positions up to its own,
+    gathered through the block table; contiguous K/V built before paging."""
+    rng = np.random.default_rng(19)
+    Hq, Hkv, D, bs = 4, 2, 8, 4
+    ctx = [9, 14, 5]
+    qlen = [3, 6, 5]            # the last q_len tokens of each sequence are new
+    nblk = [-(-c // bs) for c in ctx]
+    NB = sum(nblk) + 2
+    perm = rng.permutation(NB)
+    tables = np.full((3, max(nblk)), -1, dtype=np.int32)
+    Ks, Vs = [], []
+    kc = np.full((NB, bs, Hkv, D), 0x7E00, dtype=np.uint16)
+    vc = kc.copy()
+    i = 0
+    for s, c in enumerate(ctx):
+        tables[s, :nblk[s]] = perm[i:i + nblk[s]]
+        i += nblk[s]
+        K = to_bits(rng.standard_normal((c, Hkv, D)), "f16")
+        V = to_bits(rng.standard_normal((c, Hkv, D)), "f16")
+        Ks.append(K)
+        Vs.append(V)
+        for p in range(c):
+            kc[tables[s, p // bs], p % bs] = K[p]
+            vc[tables[s, p // bs], p % bs] = V[p]
+    cu = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    q = to_bits(rng.standard_normal((int(cu[-1]), Hq, D)), "f16")
+    got = oracle_lib.prefill_attention(q, kc, vc, "f16", tables, np.array(ctx, np.int32), cu, 0.4)
+    for s in range(3):
+        for j in range(qlen[s]):
+            pos = ctx[s] - qlen[s] + j
+            for hq in range(Hq):
+                K = brute.widen(Ks[s][: pos + 1, hq // 2], "f16")
+                V = brute.widen(Vs[s][: pos + 1, hq // 2], "f16")
+                want = brute.attention_contiguous(brute.widen(q[cu[s] + j, hq], "f16"), K, V, 0.4)
+                np.testing.assert_allclose(got[cu[s] + j, hq], want, rtol=1e-12, atol=1e-13)
+    # The last new token of each sequence is exactly that sequence's decode query.
+    last = cu[1:] - 1
+    dec = oracle_lib.paged_attention(q[last], kc, vc, "f16", tables, np.array(ctx, np.int32), 0.4)
+    assert np.array_equal(got[last], dec)
