@@ -49,7 +49,16 @@ WORKLOAD_TEXT = {
     "prefix": "prefix-sharing decode: 64 prompts x 4 samples sharing a 1000-token prompt, private 0-256 "
               "token suffix, copy-on-write of the shared partial block, 32 heads, head_dim 128, f16",
     "tiny": "tiny paged decode: 4 seqs, context {1,17,35,100}, 4 heads, head_dim 64, block_size 16, f16",
+    "prefill": "LLaMA-13B-shaped chunked prefill, one layer: 16 seqs, a 512-token chunk each over a cached "
+               "prefix of U{0..2048} tokens, causal, 40 heads (MHA), head_dim 128, block_size 16, bf16, "
+               "reshape_and_cache of the chunk's K/V",
+    "prefill_gqa": "GQA chunked prefill, one layer: 8 seqs, a 1024-token chunk each over a cached prefix of "
+                   "U{0..8192} tokens, causal, 32 q / 8 kv heads, head_dim 128, block_size 16, bf16",
+    "prefill_prefix": "prefill after a prefix-cache hit: 64 prompts x 4 samples share a cached 1000-token prompt; "
+                      "each sample's private 1-257-token tail is prefilled causally over it (copy-on-write of "
+                      "the shared partial block first), 32 heads, head_dim 128, f16",
 }
+PREFILL_WORKLOADS = {"prefill": "prefill", "prefill_gqa": "prefill_gqa", "prefill_prefix": "prefix"}
 
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -82,6 +91,34 @@ def step_bytes(b, partition: int) -> int:
     rows = len(b.slot_mapping) * b.num_kv_heads * b.head_dim * 2 * (2 + b.elem_bytes)  # K,V read + write
     copies = len(b.block_mapping) * b.block_size * b.num_kv_heads * b.head_dim * 2 * 2 * b.elem_bytes
     return decode_bytes(b, partition) + rows + copies
+
+
+def prefill_row_positions(b):
+    """Position of every query row of a prefill batch (row i of sequence s:
+    ctx_s - q_len_s + i)."""
+    import numpy as np
+    cu = b.cu_seqlens_q.astype(np.int64)
+    ql = np.diff(cu)
+    seq = np.repeat(np.arange(b.num_seqs), ql)
+    return b.context_lens[seq].astype(np.int64) - ql[seq] + (np.arange(int(cu[-1])) - cu[seq])
+
+
+def prefill_flops(b, rows=None) -> int:
+    """Algorithmic FLOPs of causal prefill attention: every (query row, head)
+    attends pos + 1 keys, 2 D FLOPs for QK^T and 2 D for PV each."""
+    pos = prefill_row_positions(b)
+    if rows is not None:
+        pos = pos[rows]
+    return int((pos + 1).sum()) * 4 * b.head_dim * b.num_heads
+
+
+def tensor_peak():
+    """Measured dense bf16 tensor throughput (burst), TFLOP/s."""
+    try:
+        with open(MEASURED_PEAKS) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def hbm_peak():
@@ -407,6 +444,233 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def _prefill_batch(args, rank=0):
+    from paged_kv_cache_140_gb300 import workloads as W
+    name = PREFILL_WORKLOADS[args.workload]
+    if name == "prefix":
+        seed = 140000 + W.CONFIGS["prefix"]["number"] + 1000 * rank
+    else:
+        seed = 140000 + W.PREFILL_CONFIGS[name]["number"] + 1000 * rank
+    return W.make_prefill_batch(name, seed=seed)
+
+
+def run_prefill(args, world, rank, local):
+    """One prefill step: copy_blocks (if any), reshape_and_cache of the new
+    tokens' K/V, causal prefill attention of their queries."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_140_gb300 as pa
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist_init("nccl")
+    pa._lib.load()
+    b = _prefill_batch(args, rank)
+    host, T = device_tensors(b, device)
+    host["cu_seqlens_q"] = torch.from_numpy(b.cu_seqlens_q)
+    T["cu_seqlens_q"] = host["cu_seqlens_q"].to(device)
+    out = torch.empty(T["q"].shape, dtype=T["q"].dtype, device=device)
+    has_pairs = len(b.block_mapping) > 0
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None, src=T):
+        if has_pairs:
+            pa.copy_blocks(T["k_cache"], T["v_cache"], src["block_mapping"])
+        pa.reshape_and_cache(src["key"], src["value"], T["k_cache"], T["v_cache"], src["slot_mapping"])
+        if ev is not None:
+            ev[0].record(stream)
+        pa.prefill(out, src["q"], T["k_cache"], T["v_cache"], src["block_tables"], src["context_lens"],
+                   src["cu_seqlens_q"], float(b.scale), max_q_len=b.max_q_len)
+        if ev is not None:
+            ev[1].record(stream)
+
+    err = pa.new_err_flag(device)
+    pa.prefill(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"], T["cu_seqlens_q"],
+               float(b.scale), max_q_len=b.max_q_len, err_flag=err)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    flag = pa.read_err_flag(err)
+    if flag:
+        raise SystemExit(f"device error flag {flag:#x} during warm-up")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    if args.clock_probe_s > 0:
+        t_end = time.time() + args.clock_probe_s
+        while time.time() < t_end:
+            for _ in range(10):
+                step()
+            torch.cuda.synchronize()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for k in range(K):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_step = t0.elapsed_time(t1) / K
+    attn_ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
+
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    used = [k for k in pinned if k != "block_mapping" or has_pairs]
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in used)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for k in used:
+            e2e_in[k].copy_(pinned[k], non_blocking=True)
+        step(src=e2e_in)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    barrier(world)
+    w0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - w0) * 1e3 / K
+    barrier(world)
+
+    flops = prefill_flops(b)
+    ms_max, fl_all = aggregate(ms_step, float(flops), world)
+    e2e_max, _ = aggregate(e2e_ms, float(flops), world)
+    peak, peak_kind = tensor_peak()
+    value = fl_all / (ms_max * 1e-3) / 1e12
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    kvb = kv_bytes(b)
+    line = {
+        "metric": "paged prefill attention: causal TFLOP/s (algorithmic), us/step",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5),
+        "us_per_step": round(ms_max * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": b.dtype,
+        "data": "synthetic (seeded N(0,1) K/V/Q, seeded block permutation, NaN in unused slots)",
+        "impl": "ours",
+        "config": {
+            "workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+            "num_seqs": b.num_seqs, "num_heads": b.num_heads, "num_kv_heads": b.num_kv_heads,
+            "head_dim": b.head_dim, "block_size": b.block_size, "num_blocks": b.num_blocks,
+            "query_tokens": b.num_tokens, "context_tokens": int(b.context_lens.sum()),
+            "flops_per_step": flops, "kv_bytes_read_once": kvb,
+            "l2": "no flush: K/V %.2f GB plus queries %.2f GB per step, above the 126 MB L2"
+                  % (kvb / 1e9, b.q.nbytes / 1e9),
+            "parallelism": f"replicas x{world} (independent batches per GPU)",
+        },
+        "roofline": {
+            "kernel": "paged_prefill_kernel",
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "launch_us": round(attn_ms * 1e3, 2),
+            "peak_kind": peak_kind,
+        },
+        "e2e": {"value": round(fl_all / (e2e_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens/cu_seqlens_q -> "
+                        "device, the step, output -> pinned host, stream sync; the KV cache stays resident"},
+        "gpu_launches": K * (2 + (1 if has_pairs else 0)),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(b, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _prefill_oracle_rows(b, kc, vc, rows):
+    import numpy as np
+
+    import oracle
+    cu = b.cu_seqlens_q.astype(np.int64)
+    seq = np.searchsorted(cu, rows, side="right") - 1
+    pos = prefill_row_positions(b)[rows]
+    return oracle.paged_attention(b.q[rows], kc, vc, b.dtype, b.block_tables[seq], (pos + 1).astype(np.int32),
+                                  b.scale)
+
+
+def _prefill_sample(b, kc, vc, target_s):
+    """Evenly spaced query rows whose oracle attention takes about target_s."""
+    import numpy as np
+    n = b.num_tokens
+    probe = np.linspace(0, n - 1, min(n, 32)).astype(np.int64)
+    t = time.perf_counter()
+    _prefill_oracle_rows(b, kc, vc, probe)
+    per_flop = max(time.perf_counter() - t, 1e-4) / max(1, prefill_flops(b, probe))
+    want = max(1, min(n, int(round(n * target_s / (per_flop * prefill_flops(b))))))
+    return np.linspace(0, n - 1, want).astype(np.int64)
+
+
+def prefill_cpu_baseline(b, target_s):
+    threads = _oracle_threads()
+    kc, vc = _post_step_caches(b)
+    rows = _prefill_sample(b, kc, vc, target_s)
+    t = time.perf_counter()
+    _prefill_oracle_rows(b, kc, vc, rows)
+    dt = time.perf_counter() - t
+    fl = prefill_flops(b, rows)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"{len(rows)} of {b.num_tokens} query rows (evenly spaced, all heads; {fl} FLOPs) over the "
+                      f"post-step caches; fp64 C oracle, OpenMP over (row, head)"}
+
+
+def run_prefill_reference(args, world, rank):
+    if rank != 0:
+        return
+    threads = _oracle_threads()
+    b = _prefill_batch(args)
+    kc, vc = _post_step_caches(b)
+    rows = _prefill_sample(b, kc, vc, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        _prefill_oracle_rows(b, kc, vc, rows)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _prefill_oracle_rows(b, kc, vc, rows)
+    dt = (time.perf_counter() - t) / args.steps
+    fl = prefill_flops(b, rows)
+    value = fl / dt / 1e12
+    print(json.dumps({
+        "metric": "paged prefill attention: causal TFLOP/s (algorithmic), us/step",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": b.dtype, "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "sample_rows": len(rows)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(rows)} of {b.num_tokens} query rows per step ({fl} FLOPs)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def decode_source_hash() -> str:
     """Hash of the decode kernel's sources; a traffic figure taken from an
     older kernel is not reported."""
@@ -604,7 +868,12 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.swap:
         return run_swap(args)
-    if args.impl == "reference":
+    if args.workload in PREFILL_WORKLOADS:
+        if args.impl == "reference":
+            run_prefill_reference(args, world, rank)
+        else:
+            run_prefill(args, world, rank, local)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)

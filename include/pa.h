@@ -254,6 +254,57 @@ pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype,
                             int partition_size, int *err_flag, void *stream);
 
 /*
+ * pa_prefill -- causal attention of each sequence's new tokens over its
+ * paged context (prefill after a prefix-cache hit, or one chunk of a
+ * chunked prefill).
+ *
+ * When a request's prefix is already cached, only its tail is computed: the
+ * tail's query tokens attend to the cached prefix blocks and, causally, to
+ * each other (Page C §3.4 with the block table and slot layout of §2.2;
+ * Page A §二).  Sequence s owns query rows cu_seqlens_q[s] ..
+ * cu_seqlens_q[s+1]-1, its q_len = cu_seqlens_q[s+1] - cu_seqlens_q[s] newest
+ * tokens; with ctx = context_lens[s], its query token i sits at position
+ * ctx - q_len + i, and for query head h (kvh = h / G):
+ *     out[row][h][:] = sum_{p <= ctx - q_len + i} softmax(x)_p * V_p,
+ *     x_p = scale * <query[row][h][:], K_p>,  row = cu_seqlens_q[s] + i,
+ * K_p / V_p gathered through the block table as in pa_decode.  Each query
+ * token's result is exactly pa_decode's for a context of (its position + 1)
+ * tokens.  The K/V rows of the new tokens must already be in the cache
+ * (pa_reshape_and_cache first).
+ *
+ *   out          : [num_tokens, num_heads, head_dim], out_dtype (F16/BF16/F32)
+ *   query        : [num_tokens, num_heads, head_dim], kv_dtype
+ *   k_cache/v_cache : [num_blocks, block_size, num_kv_heads, head_dim], F16 or
+ *                  BF16 (the query's type; FP8 caches are not supported here)
+ *   block_tables : [num_seqs, max_blocks_per_seq] int32
+ *   context_lens : [num_seqs] int32, total tokens of each sequence including
+ *                  its new ones; q_len <= ctx <= max_blocks_per_seq * bs
+ *   cu_seqlens_q : [num_seqs + 1] int32 (device), cu_seqlens_q[0] = 0,
+ *                  non-decreasing, cu_seqlens_q[num_seqs] <= num_tokens
+ *   max_q_len    : host-known upper bound of every q_len (sizes the grid)
+ *   scale        : softmax scale, > 0 (usually 1/sqrt(head_dim))
+ * Supported: head_dim 64 or 128; block_size 8, 16, 32, 64 or 128;
+ * num_heads / num_kv_heads a power of two up to 128.  Products run on the
+ * tensor cores with fp32 accumulation; the softmax weights are rounded to
+ * binary16, or for bfloat16 inputs split into two bfloat16 parts.
+ * Device-side problems: an invalid cu_seqlens_q entry, or a q_len above
+ * max_q_len, sets PA_FLAG_BAD_CONTEXT_LEN and leaves the affected rows
+ * unwritten; a context length outside [q_len, max_blocks_per_seq * bs] gives
+ * zero rows and PA_FLAG_BAD_CONTEXT_LEN; a block id outside [0, num_blocks)
+ * is not read, sets PA_FLAG_BAD_BLOCK_ID and gives zero rows for the query
+ * tiles that needed it.  No workspace; nothing is allocated.
+ */
+pa_status pa_prefill(void *out, pa_dtype out_dtype,
+                     const void *query,
+                     const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                     const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *context_lens, const int32_t *cu_seqlens_q,
+                     int num_seqs, int64_t num_tokens, int max_q_len,
+                     int num_heads, int num_kv_heads, int head_dim,
+                     int block_size, int64_t num_blocks, float scale,
+                     int *err_flag, void *stream);
+
+/*
  * pa_copy_blocks -- copy-on-write of shared blocks.
  *
  * A block referenced by several sequences is read-only; before one of them

@@ -277,3 +277,16 @@ def prefill_attention(q, k_cache, v_cache, dtype: str, block_tables, context_len
     if not rows:
         return np.zeros((0,) + tuple(np.shape(q)[1:]))
     return paged_attention(q, k_cache, v_cache, dtype, bt[rows], np.asarray(lens, dtype=np.int32), scale)
+
+
+def prefill_step(batch):
+    """The whole prefill step on the CPU: copy_blocks, reshape_and_cache of the
+    new tokens, causal attention of their queries.  ``batch`` is a
+    workloads.PrefillBatch.  Returns (out fp64 [T,Hq,D], k_cache, v_cache)."""
+    kc, vc = batch.k_cache, batch.v_cache
+    if len(batch.block_mapping):
+        kc, vc, _ = copy_blocks(kc, vc, batch.block_mapping)
+    kc, vc, _ = reshape_and_cache(batch.key, batch.value, kc, vc, batch.slot_mapping)
+    out = prefill_attention(batch.q, kc, vc, batch.dtype, batch.block_tables, batch.context_lens,
+                            batch.cu_seqlens_q, batch.scale)
+    return out, kc, vc

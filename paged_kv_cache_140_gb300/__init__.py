@@ -7,6 +7,7 @@ PyTorch fallback - a missing library raises.
 
     reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)
     decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, ...)
+    prefill(out, query, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q, scale, ...)
     copy_blocks(k_cache, v_cache, block_mapping)
 
 Cache layout: ``[num_blocks, block_size, num_kv_heads, head_dim]`` per layer
@@ -22,7 +23,7 @@ from . import _lib
 from ._lib import (FLAG_BAD_BLOCK_ID, FLAG_BAD_CONTEXT_LEN, FLAG_BAD_COPY_PAIR, FLAG_BAD_SLOT,
                    FLAG_TIMEOUT, PA_BF16, PA_F16, PA_F32, PA_FP8_E4M3, PagedAttentionError)
 
-__all__ = ["reshape_and_cache", "decode", "decode_append", "copy_blocks", "swap_blocks", "decode_workspace_size",
+__all__ = ["reshape_and_cache", "decode", "decode_append", "prefill", "copy_blocks", "swap_blocks", "decode_workspace_size",
            "decode_partition_size", "DecodeWorkspace", "new_err_flag", "read_err_flag",
            "PagedAttentionError", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK_ID", "FLAG_BAD_CONTEXT_LEN",
            "FLAG_BAD_COPY_PAIR", "FLAG_TIMEOUT", "library_path"]
@@ -263,3 +264,36 @@ def decode_append(out, query, key, value, k_cache, v_cache, block_tables, contex
                                       float(scale), int(partition_size), _ptr(buf), nbytes, _ptr(err_flag),
                                       _stream(query.device))
     _lib.check(st, "pa_decode_append")
+
+
+def prefill(out, query, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q, scale: float,
+            max_q_len: int, err_flag=None) -> None:
+    """Causal attention of each sequence's newest tokens over its paged context
+    into ``out`` [T, Hq, D] (f16, bf16 or f32).
+
+    Sequence s owns query rows ``cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1`` (int32
+    [B+1] on the GPU); ``context_lens[s]`` counts all its tokens, new ones
+    included (their K/V rows already written with :func:`reshape_and_cache`).
+    ``max_q_len`` is a host-side bound on every sequence's new-token count."""
+    torch = _torch()
+    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens),
+                 ("cu_seqlens_q", cu_seqlens_q)):
+        _cuda_contig(n, t)
+    _need(query.dim() == 3 and out.shape == query.shape, "query/out must be [T, Hq, D]")
+    _need(k_cache.dim() == 4 and v_cache.shape == k_cache.shape and k_cache.dtype == v_cache.dtype,
+          "caches must be [NB, bs, Hkv, D] of one dtype")
+    _need(k_cache.dtype == query.dtype, "caches must have the query's dtype")
+    B = context_lens.numel()
+    _need(context_lens.dtype == torch.int32, "context_lens must be int32 [B]")
+    _need(cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.numel() == B + 1, "cu_seqlens_q must be int32 [B+1]")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B,
+          "block_tables must be int32 [B, maxNB]")
+    T, Hq, D = query.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    _need(d2 == D, "head_dim mismatch")
+    st = _lib.load().pa_prefill(_ptr(out), _dtype_code(out, allow_f32=True), _ptr(query), _ptr(k_cache),
+                                _ptr(v_cache), _dtype_code(query), _ptr(block_tables), block_tables.shape[1],
+                                _ptr(context_lens), _ptr(cu_seqlens_q), B, T, int(max_q_len), Hq, hkv, D, bs,
+                                nb, float(scale), _ptr(err_flag), _stream(query.device))
+    _lib.check(st, "pa_prefill")

@@ -32,6 +32,8 @@ SIGNATURES = {
                               _I64, _F, _I, _P, _SZ, _P, _P]),
     "pa_decode_noalloc": (_I, [_P, _I, _P, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64,
                                _F, _I, _P, _P]),
+    "pa_prefill": (_I, [_P, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I64, _I, _I, _I, _I, _I, _I64, _F, _P,
+                        _P]),
     "pa_copy_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _I, _I, _I, _P, _P]),
     "pa_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P, _P]),
     "pa_check_err_flag": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int), _P]),

@@ -13,6 +13,7 @@
 
 #include "pa.h"
 #include "pa_internal.h"
+#include "pa_prefill.h"
 
 #define PA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -438,6 +439,98 @@ PA_EXPORT pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *
                        max_context_len, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, scale, partition_size, workspace, workspace_bytes, err_flag,
                        stream);
+}
+
+namespace {
+
+// Tensor map over a dense 3-D array [d2][d1][d0] of 16-bit elements with a
+// (64, box1, box2) box and 128-byte swizzle.
+bool encode_map_16(CUtensorMap *map, const void *ptr, int64_t d0, int64_t d1, int64_t d2, int box1,
+                   int box2) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1),
+                                static_cast<cuuint64_t>(d2)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d0) * 2, static_cast<cuuint64_t>(d0 * d1) * 2};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
+                               const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, const int32_t *cu_seqlens_q,
+                               int num_seqs, int64_t num_tokens, int max_q_len, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               float scale, int *err_flag, void *stream) {
+    if (num_seqs < 0 || num_tokens < 0 || max_q_len < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!half_dtype(kv_dtype) || (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int G = num_heads / num_kv_heads;
+    if (G > pa::kPrefillTile || (G & (G - 1)) != 0) return PA_ERR_UNSUPPORTED;
+    if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (block_size < 8 || block_size > pa::kPrefillTile || (block_size & (block_size - 1)) != 0)
+        return PA_ERR_UNSUPPORTED;
+    if (num_blocks * block_size > INT32_MAX || num_tokens > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (!(scale > 0.f) || scale > 3.0e38f) return PA_ERR_INVALID_ARG;
+    int lg = 0;
+    while ((1 << lg) < G) ++lg;
+    const int tokens_per_tile = pa::kPrefillTile / G;
+    const int64_t tiles = (static_cast<int64_t>(max_q_len) + tokens_per_tile - 1) / tokens_per_tile;
+    const int64_t grid = static_cast<int64_t>(num_seqs) * num_kv_heads * tiles;
+    if (grid >= (int64_t{1} << 31)) return PA_ERR_UNSUPPORTED;
+    if (grid == 0 || num_tokens == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || !cu_seqlens_q)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    if (!device_info(dev)) return PA_ERR_CUDA;
+    // K/V ring depth: as deep as shared memory allows, at most 4
+    // (PA_PREFILL_STAGES overrides for tuning).
+    int stages = env_int("PA_PREFILL_STAGES", 1, 4);
+    if (stages == 0) stages = 4;
+    while (stages > 1 && pa::prefill_smem_bytes(head_dim, stages) + 512 > static_cast<size_t>(dev.smem_optin))
+        --stages;
+    const size_t smem = pa::prefill_smem_bytes(head_dim, stages);
+    if (smem + 512 > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
+
+    CUtensorMap tq, tk, tv;
+    if (!encode_map_16(&tq, query, head_dim, num_heads, num_tokens, G, tokens_per_tile) ||
+        !encode_map_16(&tk, k_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
+        !encode_map_16(&tv, v_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size))
+        return PA_ERR_CUDA;
+
+    pa::PrefillParams p{};
+    p.out = out;
+    p.out_dtype = static_cast<int>(out_dtype);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_tokens = num_tokens;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.log2_group = lg;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.tiles_per_seq = static_cast<int>(tiles);
+    p.stages = stages;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err_flag = err_flag;
+    cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tq, tk, tv, smem,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_EXPORT pa_status pa_check_err_flag(int *err_flag, int clear, int *flag_out, void *stream) {

@@ -32,7 +32,8 @@ import math
 
 import numpy as np
 
-__all__ = ["CONFIGS", "Batch", "make_batch", "make_context_lens", "subset_batch", "NAN_BITS", "BlockPool"]
+__all__ = ["CONFIGS", "PREFILL_CONFIGS", "Batch", "PrefillBatch", "make_batch", "make_prefill_batch",
+           "make_context_lens", "subset_batch", "NAN_BITS", "BlockPool"]
 
 # Quiet-NaN bit patterns used to poison unused cache slots (e4m3: 0x7F).
 NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "fp8": 0x7F}
@@ -77,6 +78,23 @@ CONFIGS = {
                    num_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
                    dtype="f16", ctx_max=1000 + 256 + 1, pool=("demand", 1.2),
                    partition_size=0),
+}
+
+# Prefill workloads: each sequence has ``prefix`` tokens already cached and
+# ``q_len`` new tokens whose queries attend causally over prefix + new tokens
+# (prefill of the uncached tail after a prefix-cache hit, or one chunk of a
+# chunked prefill; nano-vllm walkthrough §3.4).  "prefix" reuses the prefix-
+# sharing workload above: every sample's private tail is prefilled over the
+# shared 1000-token prompt.
+PREFILL_CONFIGS = {
+    # LLaMA-13B-shaped layer, 16 sequences, a 512-token chunk over a cached
+    # prefix of U{0..2048} tokens.
+    "prefill": dict(number=6, num_seqs=16, num_heads=40, num_kv_heads=40, head_dim=128, block_size=16,
+                    dtype="bf16", prefix=("uniform", 0, 2048), q_len=("fixed", 512), pool=("demand", 1.2)),
+    # GQA (32 query / 8 KV heads), 8 sequences, 1024-token chunks over
+    # U{0..8192} cached tokens.
+    "prefill_gqa": dict(number=7, num_seqs=8, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                        dtype="bf16", prefix=("uniform", 0, 8192), q_len=("fixed", 1024), pool=("demand", 1.2)),
 }
 
 
@@ -417,3 +435,113 @@ def subset_batch(b: Batch, seqs) -> Batch:
     return dataclasses.replace(b, num_seqs=len(seqs), q=b.q[seqs].copy(),
                                block_tables=b.block_tables[seqs].copy(),
                                context_lens=b.context_lens[seqs].copy())
+
+
+@dataclasses.dataclass
+class PrefillBatch(Batch):
+    """One prefill step's inputs: ``q`` is [T, Hq, D] for the T new tokens of
+    all sequences, sequence s owning rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1
+    (its newest tokens, positions ctx - q_len .. ctx - 1).  ``key``/``value``/
+    ``slot_mapping`` are those tokens' K/V rows and slots; the caches hold the
+    cached prefix (everything else NaN).  The step is copy_blocks, then
+    reshape_and_cache, then the prefill attention."""
+    cu_seqlens_q: np.ndarray = None   # int32 [B + 1]
+    max_q_len: int = 0
+
+    @property
+    def q_lens(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_q).astype(np.int64)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+
+def _law(spec, rng, n):
+    if spec[0] == "fixed":
+        return np.full(n, int(spec[1]), dtype=np.int64)
+    if spec[0] == "uniform":
+        return rng.integers(spec[1], spec[2], size=n, endpoint=True).astype(np.int64)
+    raise ValueError(spec)
+
+
+def make_prefill_batch(name: str, *, num_seqs: int | None = None, groups: int | None = None,
+                       seed: int | None = None, prefix_cap: int | None = None, q_len_cap: int | None = None,
+                       prefix_lens=None, q_lens=None, block_size: int | None = None,
+                       **overrides) -> PrefillBatch:
+    """Build prefill workload ``name`` (a key of :data:`PREFILL_CONFIGS`, or
+    "prefix" for the tails of the prefix-sharing workload).
+
+    ``num_seqs`` (``groups`` for "prefix") shrinks the batch; ``prefix_cap`` /
+    ``q_len_cap`` clip the drawn lengths; ``prefix_lens`` / ``q_lens`` replace
+    them outright (edge-case tests); ``num_heads``, ``num_kv_heads``,
+    ``head_dim`` and ``dtype`` may be overridden.
+    """
+    if name == "prefix":
+        b = make_batch("prefix", groups=groups, seed=seed, ctx_cap=None if prefix_cap is None
+                       else CONFIGS["prefix"]["prompt_len"] + 1 + int(prefix_cap))
+        P = CONFIGS["prefix"]["prompt_len"]
+        ql = b.context_lens.astype(np.int64) - P
+        rng = np.random.Generator(np.random.PCG64(b.seed + 1))
+        q = _normal_bits(rng, (int(ql.sum()), b.num_heads, b.head_dim), b.dtype)
+        cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        fields = {f.name: getattr(b, f.name) for f in dataclasses.fields(Batch)}
+        fields.update(name="prefill_prefix", q=q)
+        return PrefillBatch(**fields, cu_seqlens_q=cu, max_q_len=int(ql.max(initial=0)))
+
+    cfg = dict(PREFILL_CONFIGS[name])
+    for k, v in overrides.items():
+        if k not in ("num_heads", "num_kv_heads", "head_dim", "dtype"):
+            raise TypeError(f"unknown override {k}")
+        cfg[k] = v
+    if block_size is not None:
+        cfg["block_size"] = int(block_size)
+    if seed is None:
+        seed = 140000 + cfg["number"]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    B = int(num_seqs or cfg["num_seqs"])
+    if prefix_lens is not None:
+        prefix = np.asarray(prefix_lens, dtype=np.int64).copy()
+        B = len(prefix)
+    else:
+        prefix = _law(cfg["prefix"], rng, B)
+    ql = np.asarray(q_lens, dtype=np.int64).copy() if q_lens is not None else _law(cfg["q_len"], rng, B)
+    if len(ql) != B:
+        raise ValueError("q_lens and prefix_lens differ in length")
+    if prefix_cap is not None:
+        prefix = np.minimum(prefix, prefix_cap)
+    if q_len_cap is not None:
+        ql = np.minimum(ql, q_len_cap)
+    Hq, Hkv, D, bs, dt = cfg["num_heads"], cfg["num_kv_heads"], cfg["head_dim"], cfg["block_size"], cfg["dtype"]
+    ctx = (prefix + ql).astype(np.int32)
+    nblk = np.array([_blocks_for(c, bs) for c in ctx], dtype=np.int64)
+    NB = max(1, int(math.ceil(cfg["pool"][1] * int(nblk.sum()))))
+    maxNB = max(1, int(nblk.max(initial=1)))
+    pool = BlockPool(NB, rng)
+    tables = np.full((B, maxNB), -1, dtype=np.int32)
+    for s in range(B):
+        blocks = pool.allocate(int(nblk[s]))
+        tables[s, : len(blocks)] = blocks
+
+    k_cache = np.full((NB, bs, Hkv, D), NAN_BITS[dt], dtype=np.uint16)
+    v_cache = np.full((NB, bs, Hkv, D), NAN_BITS[dt], dtype=np.uint16)
+    hist, new = [], []
+    for s in range(B):
+        p = np.arange(int(ctx[s]), dtype=np.int64)
+        slots = tables[s, p // bs].astype(np.int64) * bs + p % bs
+        hist.append(slots[: int(prefix[s])])
+        new.append(slots[int(prefix[s]):])
+    _fill_history(rng, k_cache, v_cache, np.concatenate(hist) if hist else np.zeros(0, np.int64), dt)
+    slot_mapping = np.concatenate(new).astype(np.int64) if new else np.zeros(0, np.int64)
+    T = len(slot_mapping)
+    key = _normal_bits(rng, (T, Hkv, D), dt)
+    value = _normal_bits(rng, (T, Hkv, D), dt)
+    q = _normal_bits(rng, (T, Hq, D), dt)
+    cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    return PrefillBatch(name=name, dtype=dt, num_seqs=B, num_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                        block_size=bs, num_blocks=NB, max_blocks_per_seq=maxNB,
+                        max_context_len=int(ctx.max(initial=0)), partition_size=0,
+                        scale=np.float32(1.0 / math.sqrt(D)), q=q, k_cache=k_cache, v_cache=v_cache,
+                        key=key, value=value, slot_mapping=slot_mapping, block_tables=tables,
+                        context_lens=ctx, block_mapping=np.zeros((0, 2), dtype=np.int64), seed=int(seed),
+                        cu_seqlens_q=cu, max_q_len=int(ql.max(initial=0)))

@@ -1,0 +1,207 @@
+"""GPU parity of pa_prefill (causal attention of each sequence's new tokens
+over its paged context) against the fp64 CPU oracle.
+
+Small cases are compared on every output element; the full-size workloads
+on sampled rows, each computed by the oracle on its own.  Edge cases: empty
+and one-token tails, tails with no cached prefix, lengths on and next to the
+128-token tile boundary, every supported group size, head_dim 64, block
+sizes 8/32/64, all output types, and a bad block id."""
+import numpy as np
+import pytest
+
+import oracle
+from pa_harness import assert_attention_close, cache_bits, half_tensor, to_device, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = pytest.importorskip("torch")
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_140_gb300._build as b
+    b.build()
+    return t
+
+
+def run_prefill(torch, b, out_dtype="f32", dev=None):
+    """copy_blocks -> reshape_and_cache -> prefill on the GPU."""
+    import paged_kv_cache_140_gb300 as pa
+    T = dev if dev is not None else to_device(b)
+    cu = torch.from_numpy(b.cu_seqlens_q).cuda()
+    err = pa.new_err_flag()
+    if len(b.block_mapping):
+        pa.copy_blocks(T["k_cache"], T["v_cache"], T["block_mapping"], err_flag=err)
+    if len(b.slot_mapping):
+        pa.reshape_and_cache(T["key"], T["value"], T["k_cache"], T["v_cache"], T["slot_mapping"], err_flag=err)
+    out = torch.full(T["q"].shape, float("nan"), dtype=torch_dtype(out_dtype), device="cuda")
+    pa.prefill(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"], cu,
+               float(b.scale), max_q_len=b.max_q_len, err_flag=err)
+    torch.cuda.synchronize()
+    return out, T, pa.read_err_flag(err)
+
+
+def oracle_rows(b, kc, vc, rows):
+    """Oracle output of selected query rows: row r of sequence s (token i of
+    its tail) is the decode query of a context of ctx - q_len + i + 1 tokens."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cu = b.cu_seqlens_q.astype(np.int64)
+    seq = np.searchsorted(cu, rows, side="right") - 1
+    pos = b.context_lens[seq].astype(np.int64) - (cu[seq + 1] - cu[seq]) + (rows - cu[seq])
+    return oracle.paged_attention(b.q[rows], kc, vc, b.dtype, b.block_tables[seq],
+                                  (pos + 1).astype(np.int32), b.scale)
+
+
+def make(name, **kw):
+    from paged_kv_cache_140_gb300 import workloads as W
+    return W.make_prefill_batch(name, **kw)
+
+
+SMALL = {
+    "13b_bf16": ("prefill", dict(num_seqs=3, prefix_cap=300, q_len_cap=200)),
+    "13b_f16": ("prefill", dict(num_seqs=3, prefix_cap=260, q_len_cap=150, dtype="f16")),
+    "gqa_g4": ("prefill_gqa", dict(num_seqs=2, prefix_cap=500, q_len_cap=100)),
+    "g2_bs32": ("prefill_gqa", dict(num_seqs=2, prefix_cap=400, q_len_cap=90, num_heads=16, block_size=32)),
+    "g8_bs8": ("prefill_gqa", dict(num_seqs=2, prefix_cap=333, q_len_cap=77, num_heads=64, block_size=8)),
+    "d64_f16_bs64": ("prefill", dict(num_seqs=3, prefix_cap=400, q_len_cap=140, head_dim=64, num_heads=8,
+                                     num_kv_heads=8, dtype="f16", block_size=64)),
+    "d64_g16_bs128": ("prefill_gqa", dict(num_seqs=2, prefix_cap=300, q_len_cap=40, head_dim=64, num_heads=32,
+                                          num_kv_heads=2, block_size=128)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_prefill_matches_oracle(torch, case):
+    name, kw = SMALL[case]
+    b = make(name, **kw)
+    ref, kc, vc = oracle.prefill_step(b)
+    out, T, err = run_prefill(torch, b)
+    assert err == 0
+    assert_attention_close(out, ref, "f32", case)
+    assert np.array_equal(cache_bits(T["k_cache"]), kc) and np.array_equal(cache_bits(T["v_cache"]), vc)
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "f16"])
+def test_prefill_half_outputs(torch, out_dtype):
+    b = make("prefill_gqa", num_seqs=2, prefix_cap=200, q_len_cap=70)
+    ref, _, _ = oracle.prefill_step(b)
+    out, _, err = run_prefill(torch, b, out_dtype)
+    assert err == 0
+    assert_attention_close(out, ref, out_dtype, out_dtype)
+
+
+def test_prefill_edge_lengths(torch):
+    """Empty tail, one-token tails, whole-prompt prefill (no cached prefix),
+    and contexts on / next to the 128-token tile boundary."""
+    prefix = [0, 127, 128, 5, 300, 0, 1, 255]
+    qlen = [1, 1, 129, 0, 128, 130, 127, 1]
+    b = make("prefill", prefix_lens=prefix, q_lens=qlen, num_heads=8, num_kv_heads=8)
+    ref, _, _ = oracle.prefill_step(b)
+    out, _, err = run_prefill(torch, b)
+    assert err == 0
+    assert_attention_close(out, ref, "f32", "edges")
+
+
+def test_prefill_gqa_edge_lengths(torch):
+    """G = 4: 32 tokens per query tile; tails of 31/32/33 tokens."""
+    b = make("prefill_gqa", prefix_lens=[0, 96, 17, 4000], q_lens=[33, 32, 31, 65], num_heads=16, num_kv_heads=4)
+    ref, _, _ = oracle.prefill_step(b)
+    out, _, err = run_prefill(torch, b)
+    assert err == 0
+    assert_attention_close(out, ref, "f32", "gqa edges")
+
+
+def test_prefill_of_prefix_hit_tails(torch):
+    """The prefix-sharing workload: every sample's private tail prefilled over
+    the shared 1000-token prompt (after copy-on-write of the partial block)."""
+    b = make("prefix", groups=2)
+    out, T, err = run_prefill(torch, b)
+    assert err == 0
+    kc, vc = cache_bits(T["k_cache"]), cache_bits(T["v_cache"])
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([b.cu_seqlens_q[:-1], b.cu_seqlens_q[1:] - 1,
+                                     rng.integers(0, b.num_tokens, 96)]))
+    ref = oracle_rows(b, kc, vc, rows)
+    assert_attention_close(out[torch.from_numpy(rows).cuda()], ref, "f32", "prefix tails")
+    # caches: the whole step is bit-exact against the oracle's copy + scatter
+    okc, ovc = _oracle_caches(b)
+    assert np.array_equal(kc, okc) and np.array_equal(vc, ovc)
+
+
+def _oracle_caches(b):
+    kc, vc = b.k_cache, b.v_cache
+    if len(b.block_mapping):
+        kc, vc, _ = oracle.copy_blocks(kc, vc, b.block_mapping)
+    kc, vc, _ = oracle.reshape_and_cache(b.key, b.value, kc, vc, b.slot_mapping)
+    return kc, vc
+
+
+@pytest.mark.parametrize("name", ["prefill", "prefill_gqa"])
+def test_prefill_full_size_sampled(torch, name):
+    """The bench workloads at full size: first / last / random rows of every
+    sequence against the oracle."""
+    b = make(name)
+    out, T, err = run_prefill(torch, b)
+    assert err == 0
+    kc, vc = cache_bits(T["k_cache"]), cache_bits(T["v_cache"])
+    rng = np.random.default_rng(6)
+    cu = b.cu_seqlens_q
+    rows = []
+    for s in range(b.num_seqs):
+        if cu[s + 1] > cu[s]:
+            rows += [cu[s], cu[s + 1] - 1] + list(rng.integers(cu[s], cu[s + 1], 2))
+    rows = np.unique(np.asarray(rows, dtype=np.int64))
+    ref = oracle_rows(b, kc, vc, rows)
+    assert_attention_close(out[torch.from_numpy(rows).cuda()], ref, "f32", name)
+    g = out.float()
+    assert bool(torch.isfinite(g).all())
+
+
+def test_prefill_one_token_tails_equal_decode(torch):
+    """A one-token tail is a decode step: pa_prefill and pa_decode agree."""
+    import paged_kv_cache_140_gb300 as pa
+    b = make("prefill_gqa", num_seqs=4, prefix_cap=3000, q_lens=[1, 1, 1, 1])
+    out, T, err = run_prefill(torch, b)
+    assert err == 0
+    dec = torch.empty_like(out)
+    pa.decode(dec, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"], float(b.scale),
+              max_context_len=int(b.context_lens.max()))
+    torch.cuda.synchronize()
+    assert float((dec - out).abs().max()) <= 2e-3
+
+
+def test_prefill_is_deterministic(torch):
+    b = make("prefill_gqa", num_seqs=2, prefix_cap=700, q_len_cap=120)
+    out1, T, _ = run_prefill(torch, b)
+    out2, _, _ = run_prefill(torch, b, dev=T)
+    assert torch.equal(out1, out2)
+
+
+def test_prefill_bad_block_id_is_flagged(torch):
+    """A block id outside the pool is not read: its query tiles give zero rows
+    and PA_FLAG_BAD_BLOCK_ID; other sequences are unaffected."""
+    import paged_kv_cache_140_gb300 as pa
+    b = make("prefill", num_seqs=2, prefix_lens=[200, 150], q_lens=[40, 60], num_heads=4, num_kv_heads=4)
+    ref, _, _ = oracle.prefill_step(b)
+    T = to_device(b)
+    T["block_tables"][0, 1] = b.num_blocks + 7
+    out, _, err = run_prefill(torch, b, dev=T)
+    assert err & pa.FLAG_BAD_BLOCK_ID
+    assert float(out[:40].abs().max()) == 0.0
+    assert_attention_close(out[40:], ref[40:], "f32", "good sequence")
+
+
+def test_prefill_rejects_bad_arguments(torch):
+    import paged_kv_cache_140_gb300 as pa
+    b = make("prefill", num_seqs=1, prefix_lens=[10], q_lens=[5], num_heads=4, num_kv_heads=4)
+    T = to_device(b)
+    cu = torch.from_numpy(b.cu_seqlens_q).cuda()
+    out = torch.empty(T["q"].shape, dtype=torch.float32, device="cuda")
+    with pytest.raises(pa.PagedAttentionError):
+        pa.prefill(out, T["q"], T["k_cache"], T["v_cache"], T["block_tables"], T["context_lens"], cu, -1.0,
+                   max_q_len=5)
+    q3 = half_tensor(np.zeros((5, 3, 128), np.uint16), "bf16")     # 3 heads over 4 KV heads
+    with pytest.raises(pa.PagedAttentionError):
+        pa.prefill(torch.empty(q3.shape, device="cuda"), q3, T["k_cache"], T["v_cache"], T["block_tables"],
+                   T["context_lens"], cu, 0.1, max_q_len=5)

@@ -91,3 +91,36 @@ def test_prefix_copy_on_write_structure():
     assert not set(b.block_mapping[:, 1].tolist()) & set(b.block_mapping[:, 0].tolist())
     assert np.all(b.context_lens >= P + 1) and np.all(b.context_lens <= P + 256 + 1)
     assert len(b.slot_mapping) == int((b.context_lens - P).sum())
+
+
+@pytest.mark.parametrize("name,kw", [("prefill", dict(num_seqs=3, prefix_cap=200, q_len_cap=70)),
+                                     ("prefill_gqa", dict(num_seqs=2, prefix_cap=300, q_len_cap=50)),
+                                     ("prefill", dict(prefix_lens=[0, 16, 5], q_lens=[3, 0, 17])),
+                                     ("prefix", dict(groups=1))])
+def test_prefill_batch_structure(name, kw):
+    """Tails of q_len new tokens after `ctx - q_len` cached ones: the cache
+    holds exactly the prefix, the step writes the tail's slots in sequence /
+    position order, and query rows follow cu_seqlens_q."""
+    b = W.make_prefill_batch(name, **kw)
+    b2 = W.make_prefill_batch(name, **kw)
+    assert np.array_equal(b.q, b2.q) and np.array_equal(b.k_cache, b2.k_cache)
+    B, bs = b.num_seqs, b.block_size
+    ql = b.q_lens
+    assert b.cu_seqlens_q[0] == 0 and np.all(ql >= 0) and b.max_q_len == ql.max()
+    assert b.q.shape == (b.num_tokens, b.num_heads, b.head_dim)
+    assert b.key.shape == (b.num_tokens, b.num_kv_heads, b.head_dim) and len(b.slot_mapping) == b.num_tokens
+    nan = W.NAN_BITS[b.dtype]
+    flat = b.k_cache.reshape(-1, b.num_kv_heads * b.head_dim)
+    expect = []
+    for s in range(B):
+        ctx, n = int(b.context_lens[s]), int(ql[s])
+        assert n <= ctx
+        p = np.arange(ctx)
+        slots = b.block_tables[s, p // bs].astype(np.int64) * bs + p % bs
+        prefix_slots, tail = slots[: ctx - n], slots[ctx - n:]
+        if len(b.block_mapping) == 0 or name != "prefix":
+            assert not np.any(flat[prefix_slots] == nan)
+        assert np.all(flat[tail] == nan)
+        expect.append(tail)
+    assert np.array_equal(np.concatenate(expect), b.slot_mapping)
+    assert len(np.unique(b.slot_mapping)) == len(b.slot_mapping)
