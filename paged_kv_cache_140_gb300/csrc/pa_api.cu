@@ -495,14 +495,8 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
 
     DeviceInfo dev;
     if (!device_info(dev)) return PA_ERR_CUDA;
-    // K/V ring depth: as deep as shared memory allows, at most 4
-    // (PA_PREFILL_STAGES overrides for tuning).
-    int stages = env_int("PA_PREFILL_STAGES", 1, 4);
-    if (stages == 0) stages = 4;
-    while (stages > 1 && pa::prefill_smem_bytes(head_dim, stages) + 512 > static_cast<size_t>(dev.smem_optin))
-        --stages;
-    const size_t smem = pa::prefill_smem_bytes(head_dim, stages);
-    if (smem + 512 > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
+    const size_t smem = pa::prefill_smem_bytes(head_dim);
+    if (smem + 4096 > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
     CUtensorMap tq, tk, tv;
     if (!encode_map_16(&tq, query, head_dim, num_heads, num_tokens, G, tokens_per_tile) ||
@@ -525,7 +519,6 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     p.block_size = block_size;
     p.num_blocks = num_blocks;
     p.tiles_per_seq = static_cast<int>(tiles);
-    p.stages = stages;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err_flag = err_flag;
     cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tq, tk, tv, smem,

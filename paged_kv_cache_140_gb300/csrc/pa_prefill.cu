@@ -9,22 +9,25 @@
 //
 // One CTA computes 128 query rows of one (sequence, KV head): 128/G tokens
 // times the G query heads that share the KV head, so every K/V tile read is
-// used by all of them.  Per 128-token KV tile:
-//   S = Q K^T   tcgen05.mma, Q and K tiles in shared memory (TMA, 128-byte
-//               swizzle), S in tensor memory (double-buffered);
-//   softmax     four warps, one query row per thread, read S from tensor
-//               memory, keep the running max / sum in registers (rescaling
-//               the output only when the max grows by more than 2^8) and
-//               write the weights P back over S as 16-bit pairs;
-//   O += P V    tcgen05.mma with P read from tensor memory and V (MN-major)
-//               from shared memory, O accumulated in tensor memory.
+// used by all of them.  Per 128-token KV tile j:
+//   S_j = Q K_j^T  tcgen05.mma, Q and K tiles in shared memory (TMA, 128-byte
+//                  swizzle), S in tensor memory, double-buffered; S_{j+2} is
+//                  issued as soon as the softmax has read S_j;
+//   softmax        eight warps, two threads per query row (64 columns each,
+//                  the row max traded through shared memory); running max and
+//                  sum in registers, the output rescaled only when the max
+//                  grows by more than 2^8; weights P written to their own
+//                  tensor-memory buffer as 16-bit pairs;
+//   O += P_j V_j   tcgen05.mma with P read from tensor memory and V (MN-major)
+//                  from shared memory, O accumulated in tensor memory.
 // bfloat16 weights carry only 8 significant bits, so for bf16 inputs P is
 // split into P_hi + P_lo (both bf16, P_lo = P - P_hi) and PV runs twice;
 // binary16 weights (11 bits) are used directly.
 //
-// Warp roles: warps 0-3 softmax + epilogue (warp w owns TMEM lanes 32w..),
-// warp 4 issues the TMA loads (block ids read through the block table), warp
-// 5 owns the tensor memory and one of its lanes issues every MMA.  Every
+// Warp roles: warps 0-7 softmax + epilogue (warp w reads TMEM lanes
+// 32 (w % 4).. and columns 64 (w / 4)..), warp 8 issues the TMA loads (block
+// ids read through the block table), warp 9 owns the tensor memory and one of
+// its lanes issues every MMA.  Every
 // mbarrier wait is bounded (2 s); a timeout sets PA_FLAG_TIMEOUT and the CTA
 // winds down without further MMAs.
 #include <math_constants.h>
@@ -39,15 +42,26 @@ namespace {
 
 constexpr int kTile = kPrefillTile;
 constexpr int kRegion = kTile * 128;     // 128 rows x 128 bytes: one swizzled operand region
-constexpr uint32_t kTmemCols = 512;      // S0 [0,128), S1 [128,256), O [256, 256 + D)
-constexpr int kMaxStages = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;            // S0 [0,128), S1 [128,256)
+constexpr uint32_t kColP = 256;          // P [256,384): hi halves, then (bf16) lo halves
+constexpr uint32_t kColO = 384;          // O [384, 384 + D)
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// K and V ring depths: K runs two tiles ahead of the PV products.
+template <int D> struct Rings;
+template <> struct Rings<128> { static constexpr int K = 3, V = 2; };
+template <> struct Rings<64> { static constexpr int K = 4, V = 3; };
 
 struct Shared {
     uint64_t q_full;
-    uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
-    uint64_t s_full[2], p_full[2], pv_done[2];
-    uint64_t done;
+    uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full, pv_done, done;
+    uint64_t pair[2][4];                 // [tile parity][lane quarter]: the two warps of a row pair
+    float red[2][2][kTile];              // [tile parity][column half][row]: partial max / sum
     uint32_t tmem_base;
     int abort;
     int bad;
@@ -70,15 +84,28 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Shared 
     }
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // Warp-uniform bounded wait: every lane waits, and the warp goes on only if
 // all of them saw the phase complete (so warp-collective tensor-memory
 // instructions after it are reached by the whole warp or by none of it).
 __device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Shared &sh, int *err_flag) {
     return __all_sync(0xffffffffu, wait_bar(bar, parity, sh, err_flag));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Trade a per-row value with the partner thread that holds the other half of
+// the row: publish `mine`, wait (bounded) for the pair's phase, read theirs.
+// `use` counts the exchanges of this pair (tile index, then one more).
+__device__ __forceinline__ bool pair_exchange(Shared &sh, int use, int q, int h, int row, float mine,
+                                              float &theirs, int *err_flag) {
+    const int b = use & 1;
+    sh.red[b][h][row] = mine;
+    mbar_arrive(&sh.pair[b][q]);
+    if (!warp_wait_bar(&sh.pair[b][q], (use >> 1) & 1, sh, err_flag)) return false;
+    theirs = sh.red[b][h ^ 1][row];
+    return true;
 }
 
 // 3-D tiled TMA load without an L2 hint (K/V tiles are re-read by the other
@@ -97,9 +124,42 @@ __device__ __forceinline__ void st_32x32b_x32(uint32_t taddr, const uint32_t (&r
     umma::st_32x32b_x16(taddr + 16, r + 16);
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
-    return pack2<BF16>(lo, hi);
+// ------------------------------------------------ packed fp32 pair arithmetic
+
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 unf2(uint64_t r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // One 32-column chunk of an output row -> global memory (out_dtype).
@@ -131,8 +191,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                          const __grid_constant__ CUtensorMap tv) {
     constexpr int R = D / 64;               // 128-byte regions per row
     constexpr int kOp = R * kRegion;        // one 128-row operand tile
+    constexpr int NK = Rings<D>::K, NV = Rings<D>::V;
     constexpr int kKSteps = D / 16;         // QK MMAs per tile (K = 16 each)
     constexpr int kPVSteps = kTile / 16;    // PV MMAs per tile and weight part
+    constexpr int kHalfD = D / 2;           // O columns per softmax thread
     constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kTile, false);
     constexpr uint32_t kIdescPV = umma::idesc_f16(BF16, kTile, D, true);
 
@@ -141,10 +203,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = base;
-    uint8_t *sKV = base + kOp;              // stage st: K at sKV + 2 st kOp, V right after
+    uint8_t *sK = base + kOp;               // K ring: NK tiles
+    uint8_t *sV = sK + NK * kOp;            // V ring: NV tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NS = p.stages;
 
     // ---- work unit: (sequence, KV head, query tile), heaviest tiles first
     const int tiles = p.tiles_per_seq;
@@ -167,21 +229,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     if (t0 >= ql) return;                   // no query tokens in this tile
     const int ntok = min(TT, ql - t0);
     const int ctx = __ldg(p.context_lens + s);
-    const int row = threadIdx.x;            // softmax threads: query row
+
+    // Softmax threads: query row `row` (token rtok, head kvh * G + row % G),
+    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O.
+    const int q4 = warp & 3, h = (warp >> 2) & 1;
+    const int row = 32 * q4 + lane;
     const int rtok = row >> lg;
-    // Output row of softmax thread `row` (token rtok, head kvh * G + row % G).
     const int64_t out_row = (static_cast<int64_t>(q0) + t0 + rtok) * p.num_heads +
                             static_cast<int64_t>(kvh) * G + (row & (G - 1));
 
     if (ctx < ql || static_cast<int64_t>(ctx) > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
         if (threadIdx.x == 0 && qt == 0 && kvh == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
-        if (row < kTile && rtok < ntok) {
+        if (warp < 8 && rtok < ntok) {
             float z[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-                store_chunk(p.out, p.out_dtype, out_row * D + c * 32, z);
+            for (int c = 0; c < kHalfD / 32; ++c)
+                store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, z);
         }
         return;
     }
@@ -191,22 +256,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&sh.q_full, 1);
-        for (int i = 0; i < kMaxStages; ++i) {
+        for (int i = 0; i < kMaxRing; ++i) {
             mbar_init(&sh.k_full[i], 1);
+            mbar_init(&sh.k_empty[i], 1);
             mbar_init(&sh.v_full[i], 1);
-            mbar_init(&sh.kv_empty[i], 1);
+            mbar_init(&sh.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i], kTile);
-            mbar_init(&sh.pv_done[i], 1);
+            mbar_init(&sh.s_free[i], 256);
+            for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][q], 64);
         }
+        mbar_init(&sh.p_full, 256);
+        mbar_init(&sh.pv_done, 1);
         mbar_init(&sh.done, 1);
         sh.abort = 0;
         sh.bad = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         umma::tmem_alloc(smem_addr(&sh.tmem_base), kTmemCols);
         umma::tmem_relinquish();
     }
@@ -214,10 +282,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sh.tmem_base;
-    const uint32_t tO = tmem + 256;
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         // ------------------------------------------------------ TMA producer
+        // Order K_0, (K_1, V_0), (K_2, V_1), ...: K runs one tile ahead of V.
         const int bs = p.block_size;
         const int bpt = kTile / bs;
         const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
@@ -230,114 +298,136 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int r = 0; r < R; ++r)
                 tma_load_3d_plain(sQ + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0);
         }
-        int st = 0, round = 0;
-        int issued = 0;
-        for (int j = 0; j < n_tiles; ++j) {
-            if (j >= NS && !warp_wait_bar(&sh.kv_empty[st], (round - 1) & 1, sh, p.err_flag)) break;
-            const int last = min(qpos_max, j * kTile + kTile - 1);
-            const int nb = (last - j * kTile) / bs + 1;
+        int prev_bid = -1;
+        bool prev_ok = false;
+        uint32_t prev_bytes = 0;
+        int k_issued = 0, v_issued = 0;
+        for (int t = 0; t <= n_tiles; ++t) {
             int bid = -1;
             bool ok = false;
-            if (lane < nb) {
-                bid = __ldg(table + j * bpt + lane);
-                ok = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
-            }
-            const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-            const unsigned want = (nb >= 32) ? 0xffffffffu : ((1u << nb) - 1u);
-            if (lane == 0) {
-                if (okmask != want) {
-                    report(p.err_flag, PA_FLAG_BAD_BLOCK_ID);
-                    sh.bad = 1;
+            uint32_t bytes = 0;
+            if (t < n_tiles) {
+                const int kst = t % NK;
+                if (t >= NK && !warp_wait_bar(&sh.k_empty[kst], ((t / NK) - 1) & 1, sh, p.err_flag)) break;
+                const int last = min(qpos_max, t * kTile + kTile - 1);
+                const int nb = (last - t * kTile) / bs + 1;
+                if (lane < nb) {
+                    bid = __ldg(table + t * bpt + lane);
+                    ok = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
                 }
-                const uint32_t bytes = static_cast<uint32_t>(__popc(okmask)) * bs * 128u * R;
-                mbar_arrive_expect_tx(&sh.k_full[st], bytes);
-                mbar_arrive_expect_tx(&sh.v_full[st], bytes);
-            }
-            __syncwarp();
-            if (ok) {
-                uint8_t *sK = sKV + static_cast<size_t>(st) * 2 * kOp;
-                uint8_t *sV = sK + kOp;
+                const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+                const unsigned want = (nb >= 32) ? 0xffffffffu : ((1u << nb) - 1u);
+                bytes = static_cast<uint32_t>(__popc(okmask)) * bs * 128u * R;
+                if (lane == 0) {
+                    if (okmask != want) {
+                        report(p.err_flag, PA_FLAG_BAD_BLOCK_ID);
+                        sh.bad = 1;
+                    }
+                    mbar_arrive_expect_tx(&sh.k_full[kst], bytes);
+                }
+                __syncwarp();
+                if (ok) {
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    tma_load_3d_plain(sK + r * kRegion + lane * bs * 128, &tk, &sh.k_full[st], r * 64,
-                                      kvh, bid * bs);
+                    for (int r = 0; r < R; ++r)
+                        tma_load_3d_plain(sK + kst * kOp + r * kRegion + lane * bs * 128, &tk, &sh.k_full[kst],
+                                          r * 64, kvh, bid * bs);
+                }
+                ++k_issued;
+            }
+            if (t >= 1) {
+                const int u = t - 1;
+                const int vst = u % NV;
+                if (u >= NV && !warp_wait_bar(&sh.v_empty[vst], ((u / NV) - 1) & 1, sh, p.err_flag)) break;
+                if (lane == 0) mbar_arrive_expect_tx(&sh.v_full[vst], prev_bytes);
+                __syncwarp();
+                if (prev_ok) {
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    tma_load_3d_plain(sV + r * kRegion + lane * bs * 128, &tv, &sh.v_full[st], r * 64,
-                                      kvh, bid * bs);
+                    for (int r = 0; r < R; ++r)
+                        tma_load_3d_plain(sV + vst * kOp + r * kRegion + lane * bs * 128, &tv, &sh.v_full[vst],
+                                          r * 64, kvh, prev_bid * bs);
+                }
+                ++v_issued;
             }
-            ++issued;
-            if (++st == NS) {
-                st = 0;
-                ++round;
-            }
+            prev_bid = bid;
+            prev_ok = ok;
+            prev_bytes = bytes;
         }
         // On an abort, let the copies still in flight land before the CTA exits.
         if (lane == 0 && sh.abort) {
-            for (int j = max(0, issued - NS); j < issued; ++j) {
-                const int s2 = j % NS;
-                mbar_wait_bounded(&sh.k_full[s2], (j / NS) & 1, kWaitLimitNs);
-                mbar_wait_bounded(&sh.v_full[s2], (j / NS) & 1, kWaitLimitNs);
-            }
+            for (int t = max(0, k_issued - NK); t < k_issued; ++t)
+                mbar_wait_bounded(&sh.k_full[t % NK], (t / NK) & 1, kWaitLimitNs);
+            for (int u = max(0, v_issued - NV); u < v_issued; ++u)
+                mbar_wait_bounded(&sh.v_full[u % NV], (u / NV) & 1, kWaitLimitNs);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t q_addr = smem_addr(sQ);
-            const uint32_t kv_addr = smem_addr(sKV);
+            const uint32_t k_addr = smem_addr(sK);
+            const uint32_t v_addr = smem_addr(sV);
             bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag);
-            auto issue_pv = [&](int i) -> bool {
-                const int b = i & 1;
-                const int st = i % NS;
-                if (!wait_bar(&sh.v_full[st], (i / NS) & 1, sh, p.err_flag)) return false;
-                if (!wait_bar(&sh.p_full[b], (i >> 1) & 1, sh, p.err_flag)) return false;
+            // S_t = Q K_t^T into S buffer t % 2 (its K tile already landed when `ready`).
+            auto issue_qk = [&](int t, bool ready) -> bool {
+                const int kst = t % NK;
+                if (!ready && !wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
                 umma::fence_after_sync();
-                const uint32_t v_addr = kv_addr + static_cast<uint32_t>((2 * st + 1) * kOp);
-                const uint32_t tP = tmem + 128u * b;
+                const uint32_t kt = k_addr + static_cast<uint32_t>(kst * kOp);
 #pragma unroll
-                for (int k = 0; k < kPVSteps; ++k)
-                    umma::mma_ts(tO, tP + 8u * k, umma::desc_sw128(v_addr + k * 2048, kRegion, 1024),
-                                 kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
-                if constexpr (BF16) {
-#pragma unroll
-                    for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tO, tP + 64u + 8u * k,
-                                     umma::desc_sw128(v_addr + k * 2048, kRegion, 1024), kIdescPV, 1u);
+                for (int k = 0; k < kKSteps; ++k) {
+                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+                    umma::mma_ss(tmem + kColS + 128u * (t & 1), umma::desc_sw128(q_addr + off, 16, 1024),
+                                 umma::desc_sw128(kt + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
                 }
-                umma::commit(smem_addr(&sh.pv_done[b]));
-                umma::commit(smem_addr(&sh.kv_empty[st]));
+                umma::commit(smem_addr(&sh.s_full[t & 1]));
+                umma::commit(smem_addr(&sh.k_empty[kst]));
                 return true;
             };
+            if (ok) ok = issue_qk(0, false);
+            if (ok && n_tiles > 1) ok = issue_qk(1, false);
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int b = j & 1;
-                const int st = j % NS;
-                if (!wait_bar(&sh.k_full[st], (j / NS) & 1, sh, p.err_flag)) { ok = false; break; }
-                if (j >= 2 && !wait_bar(&sh.pv_done[b], ((j - 2) >> 1) & 1, sh, p.err_flag)) {
+                bool pending = j + 2 < n_tiles;
+                if (pending) {
+                    if (!wait_bar(&sh.s_free[j & 1], (j >> 1) & 1, sh, p.err_flag)) { ok = false; break; }
+                    const int t = j + 2;
+                    if (mbar_try_wait(&sh.k_full[t % NK], (t / NK) & 1)) {
+                        ok = issue_qk(t, true);
+                        pending = false;
+                    }
+                }
+                // O += P_j V_j
+                const int vst = j % NV;
+                if (!wait_bar(&sh.p_full, j & 1, sh, p.err_flag) ||
+                    !wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) {
                     ok = false;
                     break;
                 }
                 umma::fence_after_sync();
-                const uint32_t k_addr = kv_addr + static_cast<uint32_t>(2 * st * kOp);
+                const uint32_t vt = v_addr + static_cast<uint32_t>(vst * kOp);
 #pragma unroll
-                for (int k = 0; k < kKSteps; ++k) {
-                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-                    umma::mma_ss(tmem + 128u * b, umma::desc_sw128(q_addr + off, 16, 1024),
-                                 umma::desc_sw128(k_addr + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+                for (int k = 0; k < kPVSteps; ++k)
+                    umma::mma_ts(tmem + kColO, tmem + kColP + 8u * k,
+                                 umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV,
+                                 (j > 0 || k > 0) ? 1u : 0u);
+                if constexpr (BF16) {
+#pragma unroll
+                    for (int k = 0; k < kPVSteps; ++k)
+                        umma::mma_ts(tmem + kColO, tmem + kColP + 64u + 8u * k,
+                                     umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV, 1u);
                 }
-                umma::commit(smem_addr(&sh.s_full[b]));
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                umma::commit(smem_addr(&sh.pv_done));
+                umma::commit(smem_addr(&sh.v_empty[vst]));
+                if (pending) ok = issue_qk(j + 2, false);
             }
-            if (ok) issue_pv(n_tiles - 1);
             umma::commit(smem_addr(&sh.done));
             mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
         }
         __syncwarp();
     } else {
         // ------------------------------------------- softmax and epilogue
-        const bool row_valid = rtok < ntok;
-        const int qpos = row_valid ? qstart + rtok : -1;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int qpos = rtok < ntok ? qstart + rtok : -1;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const float sl = p.scale_log2;
+        const uint64_t sl2 = f2(sl, sl);
         float m_run = -CUDART_INF_F;
         float l_run = 0.f;
         bool ok = true;
@@ -345,35 +435,55 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const int b = j & 1;
             if (!warp_wait_bar(&sh.s_full[b], (j >> 1) & 1, sh, p.err_flag)) { ok = false; break; }
             umma::fence_after_sync();
-            const uint32_t tS = tmem + 128u * b + lane_off;
-            uint32_t sv[kTile];
-#pragma unroll
-            for (int c = 0; c < kTile / 32; ++c)
-                umma::ld_32x32b_x32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+            uint32_t sv[64];
+            const uint32_t tS = tmem + kColS + 128u * b + lane_off + 64u * h;
+            umma::ld_32x32b_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
+            umma::ld_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
             umma::wait_ld();
-            const int lim = qpos - j * kTile;        // columns c <= lim are attended
-            float mx = -CUDART_INF_F;
+            umma::fence_before_sync();
+            mbar_arrive(&sh.s_free[b]);           // S_b may now be overwritten by S_{j+2}
+
+            const int lim = qpos - j * kTile - 64 * h;   // columns c <= lim are attended
+            if (!__all_sync(0xffffffffu, lim >= 63)) {
 #pragma unroll
-            for (int c = 0; c < kTile; ++c)
-                if (c <= lim) mx = fmaxf(mx, __uint_as_float(sv[c]));
+                for (int c = 0; c < 64; ++c)
+                    if (c > lim) sv[c] = 0xff800000u;     // -inf
+            }
+            float a0 = -CUDART_INF_F, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                a0 = max3(a0, __uint_as_float(sv[8 * i + 0]), __uint_as_float(sv[8 * i + 1]));
+                a1 = max3(a1, __uint_as_float(sv[8 * i + 2]), __uint_as_float(sv[8 * i + 3]));
+                a2 = max3(a2, __uint_as_float(sv[8 * i + 4]), __uint_as_float(sv[8 * i + 5]));
+                a3 = max3(a3, __uint_as_float(sv[8 * i + 6]), __uint_as_float(sv[8 * i + 7]));
+            }
+            float mx = max3(a0, a1, fmaxf(a2, a3));
+            float mx_other;
+            if (!pair_exchange(sh, j, q4, h, row, mx, mx_other, p.err_flag)) { ok = false; break; }
+            mx = fmaxf(mx, mx_other);
             const float x_tile = mx * sl;
             const bool need = x_tile > m_run + 8.f;
+            bool pv_seen = j == 0;
             if (__any_sync(0xffffffffu, need)) {
                 const float f = need ? fast_exp2(m_run - x_tile) : 1.f;
                 if (j > 0) {
-                    if (!warp_wait_bar(&sh.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, sh, p.err_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!warp_wait_bar(&sh.pv_done, (j - 1) & 1, sh, p.err_flag)) { ok = false; break; }
                     umma::fence_after_sync();
+                    pv_seen = true;
+                    const uint64_t f2x = f2(f, f);
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < kHalfD / 32; ++c) {
                         uint32_t o[32];
-                        umma::ld_32x32b_x32(tO + lane_off + 32 * c, o);
+                        const uint32_t tO = tmem + kColO + lane_off + kHalfD * h + 32 * c;
+                        umma::ld_32x32b_x32(tO, o);
                         umma::wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                        st_32x32b_x32(tO + lane_off + 32 * c, o);
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 v = unf2(mul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2x));
+                            o[2 * i] = __float_as_uint(v.x);
+                            o[2 * i + 1] = __float_as_uint(v.y);
+                        }
+                        st_32x32b_x32(tO, o);
                     }
                 }
                 if (need) {
@@ -381,40 +491,45 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     m_run = x_tile;
                 }
             }
-            // weights, written back over S as 16-bit pairs
-            float lsum = 0.f;
+            // weights p = 2^(s * scale_log2 - m), as 16-bit pairs
+            const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
+            const uint64_t nm2 = f2(-mref, -mref);
+            uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+            uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int c = 0; c < kTile / 32; ++c) {
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int k = 32 * c + 2 * i;
-                    const float p0 = (k <= lim) ? fast_exp2(fmaf(__uint_as_float(sv[k]), sl, -m_run)) : 0.f;
-                    const float p1 =
-                        (k + 1 <= lim) ? fast_exp2(fmaf(__uint_as_float(sv[k + 1]), sl, -m_run)) : 0.f;
-                    hi[i] = pack_pair<BF16>(p0, p1);
-                    const float2 h = Half2x<BF16>::to_float2(hi[i]);
-                    if constexpr (BF16) {
-                        lo[i] = pack_pair<true>(p0 - h.x, p1 - h.y);
-                        lsum += p0 + p1;
-                    } else {
-                        lsum += h.x + h.y;
-                    }
+            for (int i = 0; i < 32; ++i) {
+                const float2 x = unf2(fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2, nm2));
+                const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                hi[i] = pack2<BF16>(p0, p1);
+                const float2 hv = Half2x<BF16>::to_float2(hi[i]);
+                if constexpr (BF16) {
+                    const float2 lv = unf2(sub2(f2(p0, p1), f2(hv.x, hv.y)));
+                    lo[i] = pack2<true>(lv.x, lv.y);
+                    if (i & 1) acc1 = add2(acc1, f2(p0, p1)); else acc0 = add2(acc0, f2(p0, p1));
+                } else {
+                    if (i & 1) acc1 = add2(acc1, f2(hv.x, hv.y)); else acc0 = add2(acc0, f2(hv.x, hv.y));
                 }
-                umma::st_32x32b_x16(tS + 16 * c, hi);
-                if constexpr (BF16) umma::st_32x32b_x16(tS + 64 + 16 * c, lo);
             }
-            l_run += lsum;
+            const float2 acc = unf2(add2(acc0, acc1));
+            l_run += acc.x + acc.y;
+            if (!pv_seen) {                          // P_{j-1} must have been consumed
+                if (!warp_wait_bar(&sh.pv_done, (j - 1) & 1, sh, p.err_flag)) { ok = false; break; }
+                umma::fence_after_sync();
+            }
+            const uint32_t tP = tmem + kColP + lane_off + 32u * h;
+            st_32x32b_x32(tP, hi);
+            if constexpr (BF16) st_32x32b_x32(tP + 64, lo);
             if (j == n_tiles - 1 && j * kTile + kTile - 1 > qpos_max) {
                 // V rows past the last attended position hold stale or unloaded
                 // data; zero them so that 0-weights cannot meet NaNs.
-                const int st = j % NS;
-                if (!warp_wait_bar(&sh.v_full[st], (j / NS) & 1, sh, p.err_flag)) { ok = false; break; }
+                const int vst = j % NV;
+                if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
                 if (j * kTile + row > qpos_max) {
-                    uint8_t *sV = sKV + static_cast<size_t>(2 * st + 1) * kOp;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        uint4 *d = reinterpret_cast<uint4 *>(sV + r * kRegion + row * 128);
+                        if ((r & 1) != h && R > 1) continue;
+                        if (R == 1 && h == 1) continue;
+                        uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + r * kRegion + row * 128);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -423,28 +538,31 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             }
             umma::wait_st();
             umma::fence_before_sync();
-            mbar_arrive(&sh.p_full[b]);
+            mbar_arrive(&sh.p_full);
         }
-        if (ok && warp_wait_bar(&sh.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, sh, p.err_flag)) {
+        if (ok && warp_wait_bar(&sh.pv_done, (n_tiles - 1) & 1, sh, p.err_flag)) {
             umma::fence_after_sync();
+            float l_other = 0.f;
+            const bool have = pair_exchange(sh, n_tiles, q4, h, row, l_run, l_other, p.err_flag);
+            const float l = l_run + l_other;
             const bool zero = *reinterpret_cast<volatile int *>(&sh.bad) != 0;
-            const float inv = (l_run > 0.f && !zero) ? 1.f / l_run : 0.f;
+            const float inv = (l > 0.f && !zero && have) ? 1.f / l : 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < kHalfD / 32; ++c) {
                 uint32_t o[32];
-                umma::ld_32x32b_x32(tO + lane_off + 32 * c, o);
+                umma::ld_32x32b_x32(tmem + kColO + lane_off + kHalfD * h + 32 * c, o);
                 umma::wait_ld();
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : __uint_as_float(o[i]) * inv;
-                if (row_valid) store_chunk(p.out, p.out_dtype, out_row * D + c * 32, v);
+                if (qpos >= 0) store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, v);
             }
         }
     }
 
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         umma::fence_after_sync();
         umma::tmem_dealloc(tmem, kTmemCols);
     }
@@ -464,15 +582,15 @@ cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtens
 
 }  // namespace
 
-size_t prefill_smem_bytes(int head_dim, int stages) {
+size_t prefill_smem_bytes(int head_dim) {
     const size_t op = static_cast<size_t>(head_dim / 64) * kRegion;
-    return 1024 + op + static_cast<size_t>(stages) * 2 * op;
+    const int rings = head_dim == 128 ? Rings<128>::K + Rings<128>::V : Rings<64>::K + Rings<64>::V;
+    return 1024 + op * (1 + rings);
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
                            const CUtensorMap &tk, const CUtensorMap &tv, size_t smem,
                            cudaStream_t stream) {
-    if (p.stages < 1 || p.stages > kMaxStages) return cudaErrorInvalidValue;
     if (head_dim == 128)
         return bf16 ? launch_t<128, true>(p, tq, tk, tv, smem, stream)
                     : launch_t<128, false>(p, tq, tk, tv, smem, stream);

@@ -10,7 +10,7 @@
 namespace pa {
 
 constexpr int kPrefillTile = 128;       // query rows per CTA = KV tokens per stage
-constexpr int kPrefillThreads = 192;    // 4 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kPrefillThreads = 320;    // 8 softmax warps, 1 TMA warp, 1 MMA warp
 
 struct PrefillParams {
     void *out;
@@ -27,13 +27,12 @@ struct PrefillParams {
     int block_size;
     int64_t num_blocks;
     int tiles_per_seq;              // ceil(max_q_len * group / 128)
-    int stages;                     // K/V ring depth
     float scale_log2;               // softmax scale * log2(e)
     int *err_flag;
 };
 
 // Dynamic shared memory of one prefill CTA.
-size_t prefill_smem_bytes(int head_dim, int stages);
+size_t prefill_smem_bytes(int head_dim);
 
 // query: [num_tokens, Hq, D] through `tq` (box 64 x G x 128/G); caches
 // [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); 128-byte swizzle.
