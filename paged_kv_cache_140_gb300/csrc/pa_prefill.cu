@@ -11,15 +11,18 @@
 // times the G query heads that share the KV head, so every K/V tile read is
 // used by all of them.  Per 128-token KV tile j:
 //   S_j = Q K_j^T  tcgen05.mma, Q and K tiles in shared memory (TMA, 128-byte
-//                  swizzle), S in tensor memory, double-buffered; S_{j+2} is
-//                  issued as soon as the softmax has read S_j;
+//                  swizzle), S in tensor memory, double-buffered;
 //   softmax        eight warps, two threads per query row (64 columns each,
 //                  the row max traded through shared memory); running max and
 //                  sum in registers, the output rescaled only when the max
-//                  grows by more than 2^8; weights P written to their own
-//                  tensor-memory buffer as 16-bit pairs;
+//                  grows by more than 2^8; weights P written as 16-bit pairs
+//                  over S_j's own columns;
 //   O += P_j V_j   tcgen05.mma with P read from tensor memory and V (MN-major)
 //                  from shared memory, O accumulated in tensor memory.
+// The MMA stream runs ... PV_j, QK_{j+2}, PV_{j+1}, QK_{j+3} ...: QK_{j+2}
+// reuses S_j's columns right after PV_j has read P_j from them (tcgen05
+// operations of one thread execute in issue order), so the softmax of tile
+// j+1 never waits for PV_j and the tensor pipe always has the next product.
 // bfloat16 weights carry only 8 significant bits, so for bf16 inputs P is
 // split into P_hi + P_lo (both bf16, P_lo = P - P_hi) and PV runs twice;
 // binary16 weights (11 bits) are used directly.
@@ -43,9 +46,8 @@ namespace {
 constexpr int kTile = kPrefillTile;
 constexpr int kRegion = kTile * 128;     // 128 rows x 128 bytes: one swizzled operand region
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;            // S0 [0,128), S1 [128,256)
-constexpr uint32_t kColP = 256;          // P [256,384): hi halves, then (bf16) lo halves
-constexpr uint32_t kColO = 384;          // O [384, 384 + D)
+constexpr uint32_t kColS = 0;            // S/P buffers [0,128), [128,256); P: hi halves, then (bf16) lo halves
+constexpr uint32_t kColO = 256;          // O [256, 256 + D)
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -58,8 +60,8 @@ template <> struct Rings<64> { static constexpr int K = 4, V = 3; };
 struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, pv_done, done;
+    uint64_t s_full[2], p_full[2];
+    uint64_t pv_done, done;
     uint64_t pair[2][4];                 // [tile parity][lane quarter]: the two warps of a row pair
     float red[2][2][kTile];              // [tile parity][column half][row]: partial max / sum
     uint32_t tmem_base;
@@ -264,10 +266,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.s_free[i], 256);
+            mbar_init(&sh.p_full[i], 256);
             for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][q], 64);
         }
-        mbar_init(&sh.p_full, 256);
         mbar_init(&sh.pv_done, 1);
         mbar_init(&sh.done, 1);
         sh.abort = 0;
@@ -366,10 +367,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const uint32_t k_addr = smem_addr(sK);
             const uint32_t v_addr = smem_addr(sV);
             bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag);
-            // S_t = Q K_t^T into S buffer t % 2 (its K tile already landed when `ready`).
-            auto issue_qk = [&](int t, bool ready) -> bool {
+            // S_t = Q K_t^T into S buffer t % 2.
+            auto issue_qk = [&](int t, bool) -> bool {
                 const int kst = t % NK;
-                if (!ready && !wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
                 umma::fence_after_sync();
                 const uint32_t kt = k_addr + static_cast<uint32_t>(kst * kOp);
 #pragma unroll
@@ -385,38 +386,31 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             if (ok) ok = issue_qk(0, false);
             if (ok && n_tiles > 1) ok = issue_qk(1, false);
             for (int j = 0; ok && j < n_tiles; ++j) {
-                bool pending = j + 2 < n_tiles;
-                if (pending) {
-                    if (!wait_bar(&sh.s_free[j & 1], (j >> 1) & 1, sh, p.err_flag)) { ok = false; break; }
-                    const int t = j + 2;
-                    if (mbar_try_wait(&sh.k_full[t % NK], (t / NK) & 1)) {
-                        ok = issue_qk(t, true);
-                        pending = false;
-                    }
-                }
-                // O += P_j V_j
+                // O += P_j V_j, P_j in S buffer j % 2
+                const int b = j & 1;
                 const int vst = j % NV;
-                if (!wait_bar(&sh.p_full, j & 1, sh, p.err_flag) ||
+                if (!wait_bar(&sh.p_full[b], (j >> 1) & 1, sh, p.err_flag) ||
                     !wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) {
                     ok = false;
                     break;
                 }
                 umma::fence_after_sync();
                 const uint32_t vt = v_addr + static_cast<uint32_t>(vst * kOp);
+                const uint32_t tP = tmem + kColS + 128u * b;
 #pragma unroll
                 for (int k = 0; k < kPVSteps; ++k)
-                    umma::mma_ts(tmem + kColO, tmem + kColP + 8u * k,
-                                 umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV,
-                                 (j > 0 || k > 0) ? 1u : 0u);
+                    umma::mma_ts(tmem + kColO, tP + 8u * k, umma::desc_sw128(vt + k * 2048, kRegion, 1024),
+                                 kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
                 if constexpr (BF16) {
 #pragma unroll
                     for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tmem + kColO, tmem + kColP + 64u + 8u * k,
+                        umma::mma_ts(tmem + kColO, tP + 64u + 8u * k,
                                      umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV, 1u);
                 }
                 umma::commit(smem_addr(&sh.pv_done));
                 umma::commit(smem_addr(&sh.v_empty[vst]));
-                if (pending) ok = issue_qk(j + 2, false);
+                // S_{j+2} into the same columns, after PV_j in the MMA stream
+                if (j + 2 < n_tiles) ok = issue_qk(j + 2, false);
             }
             umma::commit(smem_addr(&sh.done));
             mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
@@ -440,8 +434,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             umma::ld_32x32b_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
             umma::ld_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
             umma::wait_ld();
-            umma::fence_before_sync();
-            mbar_arrive(&sh.s_free[b]);           // S_b may now be overwritten by S_{j+2}
 
             const int lim = qpos - j * kTile - 64 * h;   // columns c <= lim are attended
             if (!__all_sync(0xffffffffu, lim >= 63)) {
@@ -459,17 +451,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             }
             float mx = max3(a0, a1, fmaxf(a2, a3));
             float mx_other;
+            // The exchange also orders both halves' reads of S_j before either
+            // writes P_j over it.
+            umma::fence_before_sync();
             if (!pair_exchange(sh, j, q4, h, row, mx, mx_other, p.err_flag)) { ok = false; break; }
+            umma::fence_after_sync();
             mx = fmaxf(mx, mx_other);
             const float x_tile = mx * sl;
             const bool need = x_tile > m_run + 8.f;
-            bool pv_seen = j == 0;
             if (__any_sync(0xffffffffu, need)) {
                 const float f = need ? fast_exp2(m_run - x_tile) : 1.f;
                 if (j > 0) {
+                    // PV_{j-2} completed before S_j was issued; wait for PV_{j-1}.
                     if (!warp_wait_bar(&sh.pv_done, (j - 1) & 1, sh, p.err_flag)) { ok = false; break; }
                     umma::fence_after_sync();
-                    pv_seen = true;
                     const uint64_t f2x = f2(f, f);
 #pragma unroll
                     for (int c = 0; c < kHalfD / 32; ++c) {
@@ -512,11 +507,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             }
             const float2 acc = unf2(add2(acc0, acc1));
             l_run += acc.x + acc.y;
-            if (!pv_seen) {                          // P_{j-1} must have been consumed
-                if (!warp_wait_bar(&sh.pv_done, (j - 1) & 1, sh, p.err_flag)) { ok = false; break; }
-                umma::fence_after_sync();
-            }
-            const uint32_t tP = tmem + kColP + lane_off + 32u * h;
+            const uint32_t tP = tmem + kColS + 128u * b + lane_off + 32u * h;
             st_32x32b_x32(tP, hi);
             if constexpr (BF16) st_32x32b_x32(tP + 64, lo);
             if (j == n_tiles - 1 && j * kTile + kTile - 1 > qpos_max) {
@@ -538,9 +529,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             }
             umma::wait_st();
             umma::fence_before_sync();
-            mbar_arrive(&sh.p_full);
+            mbar_arrive(&sh.p_full[b]);
         }
-        if (ok && warp_wait_bar(&sh.pv_done, (n_tiles - 1) & 1, sh, p.err_flag)) {
+        // `done` completes once every MMA of the CTA (the last PV included) has.
+        if (ok && warp_wait_bar(&sh.done, 0, sh, p.err_flag)) {
             umma::fence_after_sync();
             float l_other = 0.f;
             const bool have = pair_exchange(sh, n_tiles, q4, h, row, l_run, l_other, p.err_flag);
