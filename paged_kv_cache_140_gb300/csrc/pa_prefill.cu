@@ -9,9 +9,11 @@
 //
 // One CTA computes 128 query rows of one (sequence, KV head): 128/G tokens
 // times the G query heads that share the KV head, so every K/V tile read is
-// used by all of them.  Per 128-token KV tile j:
-//   S_j = Q K_j^T  tcgen05.mma, Q and K tiles in shared memory (TMA, 128-byte
-//                  swizzle), S in tensor memory, double-buffered;
+// used by all of them.  The query tile sits in tensor memory for the whole
+// CTA.  Per 128-token KV tile j:
+//   S_j = Q K_j^T  tcgen05.mma, Q from tensor memory, K from shared memory
+//                  (TMA, 128-byte swizzle), S in tensor memory,
+//                  double-buffered;
 //   softmax        eight warps, two threads per query row (64 columns each,
 //                  the row max traded through shared memory); running max and
 //                  sum in registers, the output rescaled only when the max
@@ -27,10 +29,11 @@
 // split into P_hi + P_lo (both bf16, P_lo = P - P_hi) and PV runs twice;
 // binary16 weights (11 bits) are used directly.
 //
-// Warp roles: warps 0-7 softmax + epilogue (warp w reads TMEM lanes
-// 32 (w % 4).. and columns 64 (w / 4)..), warp 8 issues the TMA loads (block
-// ids read through the block table), warp 9 owns the tensor memory and one of
-// its lanes issues every MMA.  Every
+// Warp roles: warps 0-7 load the query tile, run the softmax and the
+// epilogue (warp w reads TMEM lanes 32 (w % 4).. and columns 64 (w / 4)..);
+// warp 8 issues the K tile loads and warp 10 the V tile loads (each reads
+// the block table 32 entries at a time); warp 9 owns the tensor memory and one
+// of its lanes issues every MMA.  Every
 // mbarrier wait is bounded (2 s); a timeout sets PA_FLAG_TIMEOUT and the CTA
 // winds down without further MMAs.
 #include <math_constants.h>
@@ -48,22 +51,23 @@ constexpr int kRegion = kTile * 128;     // 128 rows x 128 bytes: one swizzled o
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;            // S/P buffers [0,128), [128,256); P: hi halves, then (bf16) lo halves
 constexpr uint32_t kColO = 256;          // O [256, 256 + D)
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr uint32_t kColQ = 384;          // Q [384, 384 + D/2): 16-bit pairs
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
 constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// K and V ring depths: K runs two tiles ahead of the PV products.
+// K and V ring depths (tiles of 128 tokens).
 template <int D> struct Rings;
-template <> struct Rings<128> { static constexpr int K = 3, V = 2; };
-template <> struct Rings<64> { static constexpr int K = 4, V = 3; };
+template <> struct Rings<128> { static constexpr int K = 3, V = 3; };
+template <> struct Rings<64> { static constexpr int K = 4, V = 4; };
 
 struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
     uint64_t s_full[2], p_full[2];
     uint64_t pv_done, done;
-    uint64_t pair[2][4];                 // [tile parity][lane quarter]: the two warps of a row pair
-    float red[2][2][kTile];              // [tile parity][column half][row]: partial max / sum
+    uint64_t pair[2][4];                 // [use parity][lane quarter]: the two warps of a row pair
+    float red[2][2][kTile];              // [use parity][column half][row]: partial max / sum
     uint32_t tmem_base;
     int abort;
     int bad;
@@ -185,10 +189,64 @@ __device__ __forceinline__ void store_chunk(void *out, int out_dtype, int64_t el
     }
 }
 
+// A loader warp's view of the block table: 32 consecutive entries, one per
+// lane, with the next 32 already requested (tiles never straddle two groups:
+// 128 / bs divides 32).
+struct TableWindow {
+    const int32_t *table;
+    int needed;          // entries that may be read: blocks holding positions <= qpos_max
+    int base = -64;
+    int32_t cur = -1, nxt = -1;
+    __device__ int32_t fetch(int b, int lane) const {
+        return (b + lane < needed) ? __ldg(table + b + lane) : -1;
+    }
+    // Block id of entry `entry + i` (entry = the tile's first entry, i < 32 - entry % 32).
+    __device__ int32_t id_for(int entry, int i, int lane) {
+        const int b = entry & ~31;
+        if (b != base) {
+            if (b == base + 32) {
+                cur = nxt;
+            } else {
+                cur = fetch(b, lane);
+            }
+            nxt = fetch(b + 32, lane);
+            base = b;
+        }
+        return __shfl_sync(0xffffffffu, cur, (entry & 31) + i);
+    }
+};
+
+// Issue one 128-token K or V tile (8 blocks of 16 tokens for bs = 16, two
+// 64-column boxes each); returns false on an abort.
+template <int R>
+__device__ __forceinline__ void load_tile(TableWindow &win, int t, int bs, int qpos_max, int kvh, int64_t num_blocks,
+                                          uint8_t *dst, const CUtensorMap *map, uint64_t *full, int lane,
+                                          Shared &sh, int *err_flag) {
+    const int bpt = kTile / bs;
+    const int last = min(qpos_max, t * kTile + kTile - 1);
+    const int nb = (last - t * kTile) / bs + 1;
+    const int32_t bid = win.id_for(t * bpt, lane < nb ? lane : 0, lane);
+    const bool ok = lane < nb && bid >= 0 && static_cast<int64_t>(bid) < num_blocks;
+    const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+    const unsigned want = (nb >= 32) ? 0xffffffffu : ((1u << nb) - 1u);
+    if (lane == 0) {
+        if (okmask != want) {
+            report(err_flag, PA_FLAG_BAD_BLOCK_ID);
+            sh.bad = 1;
+        }
+        mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(okmask)) * bs * 128u * R);
+    }
+    __syncwarp();
+    if (ok) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            tma_load_3d_plain(dst + r * kRegion + lane * bs * 128, map, full, r * 64, kvh, bid * bs);
+    }
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     paged_prefill_kernel(const __grid_constant__ PrefillParams p,
-                         const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv) {
     constexpr int R = D / 64;               // 128-byte regions per row
@@ -196,7 +254,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     constexpr int NK = Rings<D>::K, NV = Rings<D>::V;
     constexpr int kKSteps = D / 16;         // QK MMAs per tile (K = 16 each)
     constexpr int kPVSteps = kTile / 16;    // PV MMAs per tile and weight part
-    constexpr int kHalfD = D / 2;           // O columns per softmax thread
+    constexpr int kHalfD = D / 2;           // O columns (and Q dims) per softmax thread
     constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kTile, false);
     constexpr uint32_t kIdescPV = umma::idesc_f16(BF16, kTile, D, true);
 
@@ -204,8 +262,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = base;
-    uint8_t *sK = base + kOp;               // K ring: NK tiles
+    uint8_t *sK = base;                     // K ring: NK tiles
     uint8_t *sV = sK + NK * kOp;            // V ring: NV tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -233,7 +290,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int ctx = __ldg(p.context_lens + s);
 
     // Softmax threads: query row `row` (token rtok, head kvh * G + row % G),
-    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O.
+    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O and Q.
     const int q4 = warp & 3, h = (warp >> 2) & 1;
     const int row = 32 * q4 + lane;
     const int rtok = row >> lg;
@@ -257,7 +314,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int n_tiles = qpos_max / kTile + 1;
 
     if (threadIdx.x == 0) {
-        mbar_init(&sh.q_full, 1);
+        mbar_init(&sh.q_full, 256);
         for (int i = 0; i < kMaxRing; ++i) {
             mbar_init(&sh.k_full[i], 1);
             mbar_init(&sh.k_empty[i], 1);
@@ -284,107 +341,54 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     umma::fence_after_sync();
     const uint32_t tmem = sh.tmem_base;
 
-    if (warp == kWarpTma) {
-        // ------------------------------------------------------ TMA producer
-        // Order K_0, (K_1, V_0), (K_2, V_1), ...: K runs one tile ahead of V.
-        const int bs = p.block_size;
-        const int bpt = kTile / bs;
-        const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
-        if (lane == 0) {
-            prefetch_tensormap(&tq);
-            prefetch_tensormap(&tk);
-            prefetch_tensormap(&tv);
-            mbar_arrive_expect_tx(&sh.q_full, kOp);
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                tma_load_3d_plain(sQ + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0);
-        }
-        int prev_bid = -1;
-        bool prev_ok = false;
-        uint32_t prev_bytes = 0;
-        int k_issued = 0, v_issued = 0;
-        for (int t = 0; t <= n_tiles; ++t) {
-            int bid = -1;
-            bool ok = false;
-            uint32_t bytes = 0;
-            if (t < n_tiles) {
-                const int kst = t % NK;
-                if (t >= NK && !warp_wait_bar(&sh.k_empty[kst], ((t / NK) - 1) & 1, sh, p.err_flag)) break;
-                const int last = min(qpos_max, t * kTile + kTile - 1);
-                const int nb = (last - t * kTile) / bs + 1;
-                if (lane < nb) {
-                    bid = __ldg(table + t * bpt + lane);
-                    ok = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
-                }
-                const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-                const unsigned want = (nb >= 32) ? 0xffffffffu : ((1u << nb) - 1u);
-                bytes = static_cast<uint32_t>(__popc(okmask)) * bs * 128u * R;
-                if (lane == 0) {
-                    if (okmask != want) {
-                        report(p.err_flag, PA_FLAG_BAD_BLOCK_ID);
-                        sh.bad = 1;
-                    }
-                    mbar_arrive_expect_tx(&sh.k_full[kst], bytes);
-                }
-                __syncwarp();
-                if (ok) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        tma_load_3d_plain(sK + kst * kOp + r * kRegion + lane * bs * 128, &tk, &sh.k_full[kst],
-                                          r * 64, kvh, bid * bs);
-                }
-                ++k_issued;
-            }
-            if (t >= 1) {
-                const int u = t - 1;
-                const int vst = u % NV;
-                if (u >= NV && !warp_wait_bar(&sh.v_empty[vst], ((u / NV) - 1) & 1, sh, p.err_flag)) break;
-                if (lane == 0) mbar_arrive_expect_tx(&sh.v_full[vst], prev_bytes);
-                __syncwarp();
-                if (prev_ok) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        tma_load_3d_plain(sV + vst * kOp + r * kRegion + lane * bs * 128, &tv, &sh.v_full[vst],
-                                          r * 64, kvh, prev_bid * bs);
-                }
-                ++v_issued;
-            }
-            prev_bid = bid;
-            prev_ok = ok;
-            prev_bytes = bytes;
+    if (warp == kWarpK || warp == kWarpV) {
+        // ---------------------------------------------------- TMA loaders
+        const bool is_k = warp == kWarpK;
+        const CUtensorMap *map = is_k ? &tk : &tv;
+        const int NR = is_k ? NK : NV;
+        uint64_t *full = is_k ? sh.k_full : sh.v_full;
+        uint64_t *empty = is_k ? sh.k_empty : sh.v_empty;
+        uint8_t *ring = is_k ? sK : sV;
+        if (lane == 0) prefetch_tensormap(map);
+        TableWindow win{p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq,
+                        qpos_max / p.block_size + 1};
+        int issued = 0;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % NR;
+            if (t >= NR && !warp_wait_bar(&empty[st], ((t / NR) - 1) & 1, sh, p.err_flag)) break;
+            load_tile<R>(win, t, p.block_size, qpos_max, kvh, p.num_blocks, ring + st * kOp, map, &full[st], lane,
+                         sh, p.err_flag);
+            ++issued;
         }
         // On an abort, let the copies still in flight land before the CTA exits.
         if (lane == 0 && sh.abort) {
-            for (int t = max(0, k_issued - NK); t < k_issued; ++t)
-                mbar_wait_bounded(&sh.k_full[t % NK], (t / NK) & 1, kWaitLimitNs);
-            for (int u = max(0, v_issued - NV); u < v_issued; ++u)
-                mbar_wait_bounded(&sh.v_full[u % NV], (u / NV) & 1, kWaitLimitNs);
+            for (int t = max(0, issued - NR); t < issued; ++t)
+                mbar_wait_bounded(&full[t % NR], (t / NR) & 1, kWaitLimitNs);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t q_addr = smem_addr(sQ);
             const uint32_t k_addr = smem_addr(sK);
             const uint32_t v_addr = smem_addr(sV);
+            const uint32_t tQ = tmem + kColQ;
             bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag);
             // S_t = Q K_t^T into S buffer t % 2.
-            auto issue_qk = [&](int t, bool) -> bool {
+            auto issue_qk = [&](int t) -> bool {
                 const int kst = t % NK;
                 if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
                 umma::fence_after_sync();
                 const uint32_t kt = k_addr + static_cast<uint32_t>(kst * kOp);
 #pragma unroll
-                for (int k = 0; k < kKSteps; ++k) {
-                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-                    umma::mma_ss(tmem + kColS + 128u * (t & 1), umma::desc_sw128(q_addr + off, 16, 1024),
-                                 umma::desc_sw128(kt + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
-                }
+                for (int k = 0; k < kKSteps; ++k)
+                    umma::mma_ts(tmem + kColS + 128u * (t & 1), tQ + 8u * k,
+                                 umma::desc_sw128(kt + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024), kIdescQK,
+                                 k > 0 ? 1u : 0u);
                 umma::commit(smem_addr(&sh.s_full[t & 1]));
                 umma::commit(smem_addr(&sh.k_empty[kst]));
                 return true;
             };
-            if (ok) ok = issue_qk(0, false);
-            if (ok && n_tiles > 1) ok = issue_qk(1, false);
+            if (ok) ok = issue_qk(0);
+            if (ok && n_tiles > 1) ok = issue_qk(1);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 // O += P_j V_j, P_j in S buffer j % 2
                 const int b = j & 1;
@@ -410,16 +414,41 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 umma::commit(smem_addr(&sh.pv_done));
                 umma::commit(smem_addr(&sh.v_empty[vst]));
                 // S_{j+2} into the same columns, after PV_j in the MMA stream
-                if (j + 2 < n_tiles) ok = issue_qk(j + 2, false);
+                if (j + 2 < n_tiles) ok = issue_qk(j + 2);
             }
             umma::commit(smem_addr(&sh.done));
             mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------- softmax and epilogue
+        // -------------------------------------- query tile, softmax, epilogue
         const int qpos = rtok < ntok ? qstart + rtok : -1;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        {
+            // This thread's half of its query row -> Q columns [D/4 h, D/4 h + D/4).
+            uint32_t qw[kHalfD / 2];
+            if (qpos >= 0) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
+                                                                   out_row * D + kHalfD * h);
+#pragma unroll
+                for (int i = 0; i < kHalfD / 8; ++i) {
+                    const uint4 v = __ldg(src + i);
+                    qw[4 * i] = v.x;
+                    qw[4 * i + 1] = v.y;
+                    qw[4 * i + 2] = v.z;
+                    qw[4 * i + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kHalfD / 2; ++i) qw[i] = 0u;
+            }
+#pragma unroll
+            for (int c = 0; c < kHalfD / 32; ++c)
+                umma::st_32x32b_x16(tmem + kColQ + lane_off + (kHalfD / 2) * h + 16 * c, qw + 16 * c);
+            umma::wait_st();
+            umma::fence_before_sync();
+            mbar_arrive(&sh.q_full);
+        }
         const float sl = p.scale_log2;
         const uint64_t sl2 = f2(sl, sl);
         float m_run = -CUDART_INF_F;
@@ -518,8 +547,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 if (j * kTile + row > qpos_max) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        if ((r & 1) != h && R > 1) continue;
-                        if (R == 1 && h == 1) continue;
+                        if ((R > 1 && r != h) || (R == 1 && h == 1)) continue;
                         uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + r * kRegion + row * 128);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -561,14 +589,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 }
 
 template <int D, bool BF16>
-cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, size_t smem, cudaStream_t stream) {
+cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tk, const CUtensorMap &tv, size_t smem,
+                     cudaStream_t stream) {
     auto kern = paged_prefill_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.tiles_per_seq;
-    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tq, tk, tv);
+    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tk, tv);
     return cudaGetLastError();
 }
 
@@ -577,18 +605,15 @@ cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtens
 size_t prefill_smem_bytes(int head_dim) {
     const size_t op = static_cast<size_t>(head_dim / 64) * kRegion;
     const int rings = head_dim == 128 ? Rings<128>::K + Rings<128>::V : Rings<64>::K + Rings<64>::V;
-    return 1024 + op * (1 + rings);
+    return 1024 + op * rings;
 }
 
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
-                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem,
-                           cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tk,
+                           const CUtensorMap &tv, size_t smem, cudaStream_t stream) {
     if (head_dim == 128)
-        return bf16 ? launch_t<128, true>(p, tq, tk, tv, smem, stream)
-                    : launch_t<128, false>(p, tq, tk, tv, smem, stream);
+        return bf16 ? launch_t<128, true>(p, tk, tv, smem, stream) : launch_t<128, false>(p, tk, tv, smem, stream);
     if (head_dim == 64)
-        return bf16 ? launch_t<64, true>(p, tq, tk, tv, smem, stream)
-                    : launch_t<64, false>(p, tq, tk, tv, smem, stream);
+        return bf16 ? launch_t<64, true>(p, tk, tv, smem, stream) : launch_t<64, false>(p, tk, tv, smem, stream);
     return cudaErrorInvalidValue;
 }
 

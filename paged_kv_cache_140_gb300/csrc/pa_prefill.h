@@ -10,9 +10,10 @@
 namespace pa {
 
 constexpr int kPrefillTile = 128;       // query rows per CTA = KV tokens per stage
-constexpr int kPrefillThreads = 320;    // 8 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kPrefillThreads = 352;    // 8 softmax warps, K loader, MMA issuer, V loader
 
 struct PrefillParams {
+    const void *q;                  // [num_tokens, num_heads, head_dim]
     void *out;
     int out_dtype;                  // pa_dtype of out
     const int32_t *block_tables;    // [B, max_blocks_per_seq]
@@ -34,10 +35,9 @@ struct PrefillParams {
 // Dynamic shared memory of one prefill CTA.
 size_t prefill_smem_bytes(int head_dim);
 
-// query: [num_tokens, Hq, D] through `tq` (box 64 x G x 128/G); caches
-// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); 128-byte swizzle.
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
-                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem,
-                           cudaStream_t stream);
+// Caches [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs, 128-byte
+// swizzle).
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tk,
+                           const CUtensorMap &tv, size_t smem, cudaStream_t stream);
 
 }  // namespace pa
