@@ -485,7 +485,7 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     while ((1 << lg) < G) ++lg;
     const int tokens_per_tile = pa::kPrefillTile / G;
     const int64_t tiles = (static_cast<int64_t>(max_q_len) + tokens_per_tile - 1) / tokens_per_tile;
-    const int64_t grid = static_cast<int64_t>(num_seqs) * num_kv_heads * tiles;
+    const int64_t grid = static_cast<int64_t>(num_seqs) * num_kv_heads * ((tiles + 1) / 2);
     if (grid >= (int64_t{1} << 31)) return PA_ERR_UNSUPPORTED;
     if (grid == 0 || num_tokens == 0) return PA_OK;
     if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || !cu_seqlens_q)
@@ -498,8 +498,9 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     const size_t smem = pa::prefill_smem_bytes(head_dim);
     if (smem + 4096 > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
-    CUtensorMap tk, tv;
-    if (!encode_map_16(&tk, k_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
+    CUtensorMap tq, tk, tv;
+    if (!encode_map_16(&tq, query, head_dim, num_heads, num_tokens, G, tokens_per_tile) ||
+        !encode_map_16(&tk, k_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
         !encode_map_16(&tv, v_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size))
         return PA_ERR_CUDA;
 
@@ -519,9 +520,10 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     p.block_size = block_size;
     p.num_blocks = num_blocks;
     p.tiles_per_seq = static_cast<int>(tiles);
+    p.pairs_per_seq = static_cast<int>((tiles + 1) / 2);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err_flag = err_flag;
-    cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tk, tv, smem,
+    cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tq, tk, tv, smem,
                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -7,35 +7,34 @@
 // with q_len new tokens and ctx total tokens sits at position
 // ctx - q_len + i and attends positions 0 .. that position.
 //
-// One CTA computes 128 query rows of one (sequence, KV head): 128/G tokens
-// times the G query heads that share the KV head, so every K/V tile read is
-// used by all of them.  The query tile sits in tensor memory for the whole
-// CTA.  Per 128-token KV tile j:
-//   S_j = Q K_j^T  tcgen05.mma, Q from tensor memory, K from shared memory
-//                  (TMA, 128-byte swizzle), S in tensor memory,
-//                  double-buffered;
-//   softmax        eight warps, two threads per query row (64 columns each,
-//                  the row max traded through shared memory); running max and
-//                  sum in registers, the output rescaled only when the max
-//                  grows by more than 2^8; weights P written as 16-bit pairs
-//                  over S_j's own columns;
-//   O += P_j V_j   tcgen05.mma with P read from tensor memory and V (MN-major)
-//                  from shared memory, O accumulated in tensor memory.
-// The MMA stream runs ... PV_j, QK_{j+2}, PV_{j+1}, QK_{j+3} ...: QK_{j+2}
-// reuses S_j's columns right after PV_j has read P_j from them (tcgen05
-// operations of one thread execute in issue order), so the softmax of tile
-// j+1 never waits for PV_j and the tensor pipe always has the next product.
-// bfloat16 weights carry only 8 significant bits, so for bf16 inputs P is
-// split into P_hi + P_lo (both bf16, P_lo = P - P_hi) and PV runs twice;
-// binary16 weights (11 bits) are used directly.
+// A query tile is 128 rows of one (sequence, KV head): 128/G tokens times the
+// G query heads that share the KV head.  One CTA runs two consecutive query
+// tiles, X = A and B, against every 128-token K/V tile it loads, so each K/V
+// byte brought into shared memory feeds 256 query rows (the SM's intake of
+// K/V, not the tensor cores, is what a single tile would be limited by).
+// Per K/V tile j and query tile X:
+//   S_X = Q_X K_j^T   tcgen05.mma, Q and K tiles in shared memory (TMA,
+//                     128-byte swizzle), S in tensor memory;
+//   softmax           eight warps per query tile, two threads per row (64
+//                     columns each, the row max traded through shared memory);
+//                     running max and sum in registers, the output rescaled
+//                     only when the max grows by more than 2^8; the weights P
+//                     written as 16-bit pairs over the S columns they came from;
+//   O_X += P_X V_j    tcgen05.mma with P read from tensor memory and V
+//                     (MN-major) from shared memory, O in tensor memory.
+// The MMA stream runs ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...; tcgen05
+// operations of one thread execute in issue order, so QK_X(j+1) overwrites
+// S_X only after PV_X(j) has read P_X from it, and when the softmax of tile
+// j+1 starts, O_X already holds tile j.  bfloat16 weights carry only 8
+// significant bits, so for bf16 inputs P is split into P_hi + P_lo (both
+// bf16, P_lo = P - P_hi) and PV runs twice; binary16 weights are used as is.
 //
-// Warp roles: warps 0-7 load the query tile, run the softmax and the
-// epilogue (warp w reads TMEM lanes 32 (w % 4).. and columns 64 (w / 4)..);
-// warp 8 issues the K tile loads and warp 10 the V tile loads (each reads
-// the block table 32 entries at a time); warp 9 owns the tensor memory and one
-// of its lanes issues every MMA.  Every
-// mbarrier wait is bounded (2 s); a timeout sets PA_FLAG_TIMEOUT and the CTA
-// winds down without further MMAs.
+// Warp roles: warps 0-15 run the softmax and the epilogue (warp w: query tile
+// w / 8, column half (w / 4) % 2, TMEM lanes 32 (w % 4)..); warp 16 loads the
+// query tiles and the K tiles, warp 18 the V tiles (both read the block table
+// 32 entries at a time); warp 17 owns the tensor memory and one of its lanes
+// issues every MMA.  Every mbarrier wait is bounded (2 s); a timeout sets
+// PA_FLAG_TIMEOUT and the CTA winds down without further MMAs.
 #include <math_constants.h>
 
 #include "pa.h"
@@ -49,25 +48,26 @@ namespace {
 constexpr int kTile = kPrefillTile;
 constexpr int kRegion = kTile * 128;     // 128 rows x 128 bytes: one swizzled operand region
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;            // S/P buffers [0,128), [128,256); P: hi halves, then (bf16) lo halves
-constexpr uint32_t kColO = 256;          // O [256, 256 + D)
-constexpr uint32_t kColQ = 384;          // Q [384, 384 + D/2): 16-bit pairs
-constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+// Tensor memory: S/P of query tile X at columns 128 X, O of X at 256 + 128 X.
+// P of a 32-key chunk sits in that chunk's own S columns: 16 columns of hi
+// pairs, then (bf16) 16 columns of lo pairs.
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18;
 constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // K and V ring depths (tiles of 128 tokens).
 template <int D> struct Rings;
-template <> struct Rings<128> { static constexpr int K = 3, V = 3; };
+template <> struct Rings<128> { static constexpr int K = 2, V = 2; };
 template <> struct Rings<64> { static constexpr int K = 4, V = 4; };
 
 struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
-    uint64_t s_full[2], p_full[2];
-    uint64_t pv_done, done;
-    uint64_t pair[2][4];                 // [use parity][lane quarter]: the two warps of a row pair
-    float red[2][2][kTile];              // [use parity][column half][row]: partial max / sum
+    uint64_t s_full[2], p_full[2];       // per query tile
+    uint64_t done;
+    uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
+    float red[2][2][2][kTile];           // [use parity][query tile][column half][row]
     uint32_t tmem_base;
     int abort;
     int bad;
@@ -103,14 +103,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 
 // Trade a per-row value with the partner thread that holds the other half of
 // the row: publish `mine`, wait (bounded) for the pair's phase, read theirs.
-// `use` counts the exchanges of this pair (tile index, then one more).
-__device__ __forceinline__ bool pair_exchange(Shared &sh, int use, int q, int h, int row, float mine,
+// `use` counts the exchanges of this pair (K/V tile index, then one more).
+__device__ __forceinline__ bool pair_exchange(Shared &sh, int use, int x, int q, int h, int row, float mine,
                                               float &theirs, int *err_flag) {
     const int b = use & 1;
-    sh.red[b][h][row] = mine;
-    mbar_arrive(&sh.pair[b][q]);
-    if (!warp_wait_bar(&sh.pair[b][q], (use >> 1) & 1, sh, err_flag)) return false;
-    theirs = sh.red[b][h ^ 1][row];
+    sh.red[b][x][h][row] = mine;
+    mbar_arrive(&sh.pair[b][x][q]);
+    if (!warp_wait_bar(&sh.pair[b][x][q], (use >> 1) & 1, sh, err_flag)) return false;
+    theirs = sh.red[b][x][h ^ 1][row];
     return true;
 }
 
@@ -247,6 +247,7 @@ __device__ __forceinline__ void load_tile(TableWindow &win, int t, int bs, int q
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     paged_prefill_kernel(const __grid_constant__ PrefillParams p,
+                         const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv) {
     constexpr int R = D / 64;               // 128-byte regions per row
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     constexpr int NK = Rings<D>::K, NV = Rings<D>::V;
     constexpr int kKSteps = D / 16;         // QK MMAs per tile (K = 16 each)
     constexpr int kPVSteps = kTile / 16;    // PV MMAs per tile and weight part
-    constexpr int kHalfD = D / 2;           // O columns (and Q dims) per softmax thread
+    constexpr int kHalfD = D / 2;           // O columns per softmax thread
     constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kTile, false);
     constexpr uint32_t kIdescPV = umma::idesc_f16(BF16, kTile, D, true);
 
@@ -262,15 +263,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sK = base;                     // K ring: NK tiles
+    uint8_t *sQ = base;                     // query tiles A, B
+    uint8_t *sK = sQ + 2 * kOp;             // K ring: NK tiles
     uint8_t *sV = sK + NK * kOp;            // V ring: NV tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work unit: (sequence, KV head, query tile), heaviest tiles first
-    const int tiles = p.tiles_per_seq;
-    const int qt = tiles - 1 - static_cast<int>(blockIdx.x % tiles);
-    const int sk = static_cast<int>(blockIdx.x / tiles);
+    // ---- work unit: (sequence, KV head, pair of query tiles), heaviest first
+    const int pairs = p.pairs_per_seq;
+    const int pi = pairs - 1 - static_cast<int>(blockIdx.x % pairs);
+    const int sk = static_cast<int>(blockIdx.x / pairs);
     const int kvh = sk % p.num_kv_heads;
     const int s = sk / p.num_kv_heads;
     const int lg = p.log2_group;
@@ -279,27 +281,30 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     const int q0 = __ldg(p.cu_seqlens_q + s), q1 = __ldg(p.cu_seqlens_q + s + 1);
     if (q0 < 0 || q1 < q0 || static_cast<int64_t>(q1) > p.num_tokens) {
-        if (threadIdx.x == 0 && qt == 0 && kvh == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
+        if (threadIdx.x == 0 && pi == 0 && kvh == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
         return;
     }
     const int ql = q1 - q0;
-    if (ql > tiles * TT && qt == 0 && kvh == 0 && threadIdx.x == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
-    const int t0 = qt * TT;
-    if (t0 >= ql) return;                   // no query tokens in this tile
-    const int ntok = min(TT, ql - t0);
+    if (ql > p.tiles_per_seq * TT && pi == 0 && kvh == 0 && threadIdx.x == 0)
+        report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
+    const int t0A = 2 * pi * TT;            // first token of query tile A (B follows)
+    if (t0A >= ql) return;
+    const bool hasB = t0A + TT < ql;
     const int ctx = __ldg(p.context_lens + s);
 
-    // Softmax threads: query row `row` (token rtok, head kvh * G + row % G),
-    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O and Q.
-    const int q4 = warp & 3, h = (warp >> 2) & 1;
+    // Softmax threads: query tile x, row `row` (token rtok, head kvh * G + row % G),
+    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O.
+    const int x = (warp >> 3) & 1, q4 = warp & 3, h = (warp >> 2) & 1;
     const int row = 32 * q4 + lane;
     const int rtok = row >> lg;
-    const int64_t out_row = (static_cast<int64_t>(q0) + t0 + rtok) * p.num_heads +
+    const int t0x = t0A + x * TT;
+    const int ntokx = max(0, min(TT, ql - t0x));
+    const int64_t out_row = (static_cast<int64_t>(q0) + t0x + rtok) * p.num_heads +
                             static_cast<int64_t>(kvh) * G + (row & (G - 1));
 
     if (ctx < ql || static_cast<int64_t>(ctx) > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
-        if (threadIdx.x == 0 && qt == 0 && kvh == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
-        if (warp < 8 && rtok < ntok) {
+        if (threadIdx.x == 0 && pi == 0 && kvh == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
+        if (warp < 16 && rtok < ntokx) {
             float z[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0.f;
@@ -309,12 +314,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         return;
     }
-    const int qstart = ctx - ql + t0;       // position of the tile's first query token
-    const int qpos_max = qstart + ntok - 1;
-    const int n_tiles = qpos_max / kTile + 1;
+    const int qstartA = ctx - ql + t0A;     // position of tile A's first query token
+    const int nA = (qstartA + min(TT, ql - t0A) - 1) / kTile + 1;
+    const int qpos_max = qstartA + (hasB ? TT + min(TT, ql - t0A - TT) : min(TT, ql - t0A)) - 1;
+    const int nB = hasB ? qpos_max / kTile + 1 : 0;
+    const int n_tiles = hasB ? nB : nA;     // K/V tiles loaded (nB >= nA)
 
     if (threadIdx.x == 0) {
-        mbar_init(&sh.q_full, 256);
+        mbar_init(&sh.q_full, 1);
         for (int i = 0; i < kMaxRing; ++i) {
             mbar_init(&sh.k_full[i], 1);
             mbar_init(&sh.k_empty[i], 1);
@@ -324,9 +331,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.s_full[i], 1);
             mbar_init(&sh.p_full[i], 256);
-            for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][q], 64);
+            for (int y = 0; y < 2; ++y)
+                for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][y][q], 64);
         }
-        mbar_init(&sh.pv_done, 1);
         mbar_init(&sh.done, 1);
         sh.abort = 0;
         sh.bad = 0;
@@ -349,7 +356,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         uint64_t *full = is_k ? sh.k_full : sh.v_full;
         uint64_t *empty = is_k ? sh.k_empty : sh.v_empty;
         uint8_t *ring = is_k ? sK : sV;
-        if (lane == 0) prefetch_tensormap(map);
+        if (lane == 0) {
+            prefetch_tensormap(map);
+            if (is_k) {
+                prefetch_tensormap(&tq);
+                mbar_arrive_expect_tx(&sh.q_full, kOp * (hasB ? 2 : 1));
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    tma_load_3d_plain(sQ + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A);
+                    if (hasB)
+                        tma_load_3d_plain(sQ + kOp + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A + TT);
+                }
+            }
+        }
         TableWindow win{p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq,
                         qpos_max / p.block_size + 1};
         int issued = 0;
@@ -364,142 +383,130 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (lane == 0 && sh.abort) {
             for (int t = max(0, issued - NR); t < issued; ++t)
                 mbar_wait_bounded(&full[t % NR], (t / NR) & 1, kWaitLimitNs);
+            if (is_k) mbar_wait_bounded(&sh.q_full, 0, kWaitLimitNs);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            const uint32_t q_addr = smem_addr(sQ);
             const uint32_t k_addr = smem_addr(sK);
             const uint32_t v_addr = smem_addr(sV);
-            const uint32_t tQ = tmem + kColQ;
+            const int nx[2] = {nA, nB};
             bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag);
-            // S_t = Q K_t^T into S buffer t % 2.
-            auto issue_qk = [&](int t) -> bool {
+            int k_ready = -1;                  // last K tile known to have landed
+            auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
                 const int kst = t % NK;
-                if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                if (k_ready < t) {
+                    if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                    k_ready = t;
+                }
                 umma::fence_after_sync();
                 const uint32_t kt = k_addr + static_cast<uint32_t>(kst * kOp);
+                const uint32_t qx = q_addr + static_cast<uint32_t>(xx * kOp);
 #pragma unroll
-                for (int k = 0; k < kKSteps; ++k)
-                    umma::mma_ts(tmem + kColS + 128u * (t & 1), tQ + 8u * k,
-                                 umma::desc_sw128(kt + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024), kIdescQK,
-                                 k > 0 ? 1u : 0u);
-                umma::commit(smem_addr(&sh.s_full[t & 1]));
-                umma::commit(smem_addr(&sh.k_empty[kst]));
+                for (int k = 0; k < kKSteps; ++k) {
+                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+                    umma::mma_ss(tmem + kColS + 128u * xx, umma::desc_sw128(qx + off, 16, 1024),
+                                 umma::desc_sw128(kt + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+                }
+                umma::commit(smem_addr(&sh.s_full[xx]));
                 return true;
             };
-            if (ok) ok = issue_qk(0);
-            if (ok && n_tiles > 1) ok = issue_qk(1);
+            if (ok) ok = qk(0, 0);
+            if (ok && hasB) ok = qk(1, 0);
+            if (ok) umma::commit(smem_addr(&sh.k_empty[0]));
             for (int j = 0; ok && j < n_tiles; ++j) {
-                // O += P_j V_j, P_j in S buffer j % 2
-                const int b = j & 1;
                 const int vst = j % NV;
-                if (!wait_bar(&sh.p_full[b], (j >> 1) & 1, sh, p.err_flag) ||
-                    !wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) {
+                const bool last = j == n_tiles - 1;
+                // On the last tile the zeroing of stale V rows (done by the
+                // softmax of the tile that reaches furthest) precedes every PV.
+                if (last && hasB && nA == n_tiles && !wait_bar(&sh.p_full[1], j & 1, sh, p.err_flag)) {
                     ok = false;
                     break;
                 }
-                umma::fence_after_sync();
-                const uint32_t vt = v_addr + static_cast<uint32_t>(vst * kOp);
-                const uint32_t tP = tmem + kColS + 128u * b;
-#pragma unroll
-                for (int k = 0; k < kPVSteps; ++k)
-                    umma::mma_ts(tmem + kColO, tP + 8u * k, umma::desc_sw128(vt + k * 2048, kRegion, 1024),
-                                 kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-                if constexpr (BF16) {
+                if (!wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
+                for (int xx = 0; ok && xx < 2; ++xx) {
+                    if (j >= nx[xx]) continue;
+                    if (!wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) { ok = false; break; }
+                    umma::fence_after_sync();
+                    const uint32_t vt = v_addr + static_cast<uint32_t>(vst * kOp);
+                    const uint32_t tP = tmem + kColS + 128u * xx;
+                    const uint32_t tO = tmem + kColO + 128u * xx;
 #pragma unroll
                     for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tmem + kColO, tP + 64u + 8u * k,
-                                     umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV, 1u);
+                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1),
+                                     umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV,
+                                     (j > 0 || k > 0) ? 1u : 0u);
+                    if constexpr (BF16) {
+#pragma unroll
+                        for (int k = 0; k < kPVSteps; ++k)
+                            umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
+                                         umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV, 1u);
+                    }
+                    if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
                 }
-                umma::commit(smem_addr(&sh.pv_done));
+                if (!ok) break;
                 umma::commit(smem_addr(&sh.v_empty[vst]));
-                // S_{j+2} into the same columns, after PV_j in the MMA stream
-                if (j + 2 < n_tiles) ok = issue_qk(j + 2);
+                if (j + 1 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 1) % NK]));
             }
             umma::commit(smem_addr(&sh.done));
             mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else {
-        // -------------------------------------- query tile, softmax, epilogue
-        const int qpos = rtok < ntok ? qstart + rtok : -1;
+    } else if (warp < 16 && (x == 0 || hasB)) {
+        // ------------------------------------------- softmax and epilogue
+        const int nx = x == 0 ? nA : nB;
+        const int qpos = rtok < ntokx ? qstartA + x * TT + rtok : -1;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-        {
-            // This thread's half of its query row -> Q columns [D/4 h, D/4 h + D/4).
-            uint32_t qw[kHalfD / 2];
-            if (qpos >= 0) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
-                                                                   out_row * D + kHalfD * h);
-#pragma unroll
-                for (int i = 0; i < kHalfD / 8; ++i) {
-                    const uint4 v = __ldg(src + i);
-                    qw[4 * i] = v.x;
-                    qw[4 * i + 1] = v.y;
-                    qw[4 * i + 2] = v.z;
-                    qw[4 * i + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kHalfD / 2; ++i) qw[i] = 0u;
-            }
-#pragma unroll
-            for (int c = 0; c < kHalfD / 32; ++c)
-                umma::st_32x32b_x16(tmem + kColQ + lane_off + (kHalfD / 2) * h + 16 * c, qw + 16 * c);
-            umma::wait_st();
-            umma::fence_before_sync();
-            mbar_arrive(&sh.q_full);
-        }
+        const uint32_t tS = tmem + kColS + 128u * x + lane_off + 64u * h;
+        const uint32_t tO = tmem + kColO + 128u * x + lane_off + kHalfD * h;
+        // The tile that reaches furthest zeroes the stale V rows of the last K/V tile.
+        const bool zeroer = x == (hasB ? 1 : 0) && n_tiles * kTile - 1 > qpos_max;
         const float sl = p.scale_log2;
         const uint64_t sl2 = f2(sl, sl);
         float m_run = -CUDART_INF_F;
         float l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1;
-            if (!warp_wait_bar(&sh.s_full[b], (j >> 1) & 1, sh, p.err_flag)) { ok = false; break; }
+        for (int j = 0; j < nx; ++j) {
+            if (!warp_wait_bar(&sh.s_full[x], j & 1, sh, p.err_flag)) { ok = false; break; }
             umma::fence_after_sync();
-            uint32_t sv[64];
-            const uint32_t tS = tmem + kColS + 128u * b + lane_off + 64u * h;
-            umma::ld_32x32b_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
-            umma::ld_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-            umma::wait_ld();
-
             const int lim = qpos - j * kTile - 64 * h;   // columns c <= lim are attended
-            if (!__all_sync(0xffffffffu, lim >= 63)) {
+            const bool masked = !__all_sync(0xffffffffu, lim >= 63);
+            float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c > lim) sv[c] = 0xff800000u;     // -inf
-            }
-            float a0 = -CUDART_INF_F, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                umma::ld_32x32b_x32(tS + 32 * c, v);
+                umma::wait_ld();
+                if (masked) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                a0 = max3(a0, __uint_as_float(sv[8 * i + 0]), __uint_as_float(sv[8 * i + 1]));
-                a1 = max3(a1, __uint_as_float(sv[8 * i + 2]), __uint_as_float(sv[8 * i + 3]));
-                a2 = max3(a2, __uint_as_float(sv[8 * i + 4]), __uint_as_float(sv[8 * i + 5]));
-                a3 = max3(a3, __uint_as_float(sv[8 * i + 6]), __uint_as_float(sv[8 * i + 7]));
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i > lim) v[i] = 0xff800000u;     // -inf
+                }
+                float a0 = mx, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    a0 = max3(a0, __uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
+                    a1 = max3(a1, __uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+                    a2 = max3(a2, __uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+                    a3 = max3(a3, __uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+                }
+                mx = max3(a0, a1, fmaxf(a2, a3));
             }
-            float mx = max3(a0, a1, fmaxf(a2, a3));
             float mx_other;
-            // The exchange also orders both halves' reads of S_j before either
-            // writes P_j over it.
-            umma::fence_before_sync();
-            if (!pair_exchange(sh, j, q4, h, row, mx, mx_other, p.err_flag)) { ok = false; break; }
-            umma::fence_after_sync();
+            if (!pair_exchange(sh, j, x, q4, h, row, mx, mx_other, p.err_flag)) { ok = false; break; }
             mx = fmaxf(mx, mx_other);
             const float x_tile = mx * sl;
             const bool need = x_tile > m_run + 8.f;
             if (__any_sync(0xffffffffu, need)) {
+                // O_x already holds tile j-1: PV(j-1) preceded QK(j) in the MMA stream.
                 const float f = need ? fast_exp2(m_run - x_tile) : 1.f;
                 if (j > 0) {
-                    // PV_{j-2} completed before S_j was issued; wait for PV_{j-1}.
-                    if (!warp_wait_bar(&sh.pv_done, (j - 1) & 1, sh, p.err_flag)) { ok = false; break; }
-                    umma::fence_after_sync();
                     const uint64_t f2x = f2(f, f);
 #pragma unroll
                     for (int c = 0; c < kHalfD / 32; ++c) {
                         uint32_t o[32];
-                        const uint32_t tO = tmem + kColO + lane_off + kHalfD * h + 32 * c;
-                        umma::ld_32x32b_x32(tO, o);
+                        umma::ld_32x32b_x32(tO + 32 * c, o);
                         umma::wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -507,7 +514,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                             o[2 * i] = __float_as_uint(v.x);
                             o[2 * i + 1] = __float_as_uint(v.y);
                         }
-                        st_32x32b_x32(tO, o);
+                        st_32x32b_x32(tO + 32 * c, o);
                     }
                 }
                 if (need) {
@@ -515,62 +522,69 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     m_run = x_tile;
                 }
             }
-            // weights p = 2^(s * scale_log2 - m), as 16-bit pairs
+            // weights p = 2^(s * scale_log2 - m) as 16-bit pairs, each 32-key
+            // chunk written over its own S columns
             const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
             const uint64_t nm2 = f2(-mref, -mref);
             uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
-            uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float2 x = unf2(fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2, nm2));
-                const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                hi[i] = pack2<BF16>(p0, p1);
-                const float2 hv = Half2x<BF16>::to_float2(hi[i]);
-                if constexpr (BF16) {
-                    const float2 lv = unf2(sub2(f2(p0, p1), f2(hv.x, hv.y)));
-                    lo[i] = pack2<true>(lv.x, lv.y);
-                    if (i & 1) acc1 = add2(acc1, f2(p0, p1)); else acc0 = add2(acc0, f2(p0, p1));
-                } else {
-                    if (i & 1) acc1 = add2(acc1, f2(hv.x, hv.y)); else acc0 = add2(acc0, f2(hv.x, hv.y));
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                umma::ld_32x32b_x32(tS + 32 * c, v);
+                umma::wait_ld();
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i > lim) v[i] = 0xff800000u;
                 }
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float2 xv = unf2(fma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2, nm2));
+                    const float p0 = fast_exp2(xv.x), p1 = fast_exp2(xv.y);
+                    hi[i] = pack2<BF16>(p0, p1);
+                    const float2 hv = Half2x<BF16>::to_float2(hi[i]);
+                    if constexpr (BF16) {
+                        const float2 lv = unf2(sub2(f2(p0, p1), f2(hv.x, hv.y)));
+                        lo[i] = pack2<true>(lv.x, lv.y);
+                        if (i & 1) acc1 = add2(acc1, f2(p0, p1)); else acc0 = add2(acc0, f2(p0, p1));
+                    } else {
+                        if (i & 1) acc1 = add2(acc1, f2(hv.x, hv.y)); else acc0 = add2(acc0, f2(hv.x, hv.y));
+                    }
+                }
+                umma::st_32x32b_x16(tS + 32 * c, hi);
+                if constexpr (BF16) umma::st_32x32b_x16(tS + 32 * c + 16, lo);
             }
             const float2 acc = unf2(add2(acc0, acc1));
             l_run += acc.x + acc.y;
-            const uint32_t tP = tmem + kColS + 128u * b + lane_off + 32u * h;
-            st_32x32b_x32(tP, hi);
-            if constexpr (BF16) st_32x32b_x32(tP + 64, lo);
-            if (j == n_tiles - 1 && j * kTile + kTile - 1 > qpos_max) {
+            if (zeroer && j == nx - 1) {
                 // V rows past the last attended position hold stale or unloaded
                 // data; zero them so that 0-weights cannot meet NaNs.
                 const int vst = j % NV;
                 if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-                if (j * kTile + row > qpos_max) {
+                if (j * kTile + row > qpos_max && (R > 1 || h == 0)) {
+                    uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + (R > 1 ? h : 0) * kRegion + row * 128);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        if ((R > 1 && r != h) || (R == 1 && h == 1)) continue;
-                        uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + r * kRegion + row * 128);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }
             umma::wait_st();
             umma::fence_before_sync();
-            mbar_arrive(&sh.p_full[b]);
+            mbar_arrive(&sh.p_full[x]);
         }
         // `done` completes once every MMA of the CTA (the last PV included) has.
         if (ok && warp_wait_bar(&sh.done, 0, sh, p.err_flag)) {
             umma::fence_after_sync();
             float l_other = 0.f;
-            const bool have = pair_exchange(sh, n_tiles, q4, h, row, l_run, l_other, p.err_flag);
+            const bool have = pair_exchange(sh, nx, x, q4, h, row, l_run, l_other, p.err_flag);
             const float l = l_run + l_other;
             const bool zero = *reinterpret_cast<volatile int *>(&sh.bad) != 0;
             const float inv = (l > 0.f && !zero && have) ? 1.f / l : 0.f;
 #pragma unroll
             for (int c = 0; c < kHalfD / 32; ++c) {
                 uint32_t o[32];
-                umma::ld_32x32b_x32(tmem + kColO + lane_off + kHalfD * h + 32 * c, o);
+                umma::ld_32x32b_x32(tO + 32 * c, o);
                 umma::wait_ld();
                 float v[32];
 #pragma unroll
@@ -589,14 +603,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 }
 
 template <int D, bool BF16>
-cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tk, const CUtensorMap &tv, size_t smem,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                     size_t smem, cudaStream_t stream) {
     auto kern = paged_prefill_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t grid = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.tiles_per_seq;
-    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tk, tv);
+    const int64_t grid = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.pairs_per_seq;
+    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
@@ -605,15 +619,17 @@ cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tk, const CUtens
 size_t prefill_smem_bytes(int head_dim) {
     const size_t op = static_cast<size_t>(head_dim / 64) * kRegion;
     const int rings = head_dim == 128 ? Rings<128>::K + Rings<128>::V : Rings<64>::K + Rings<64>::V;
-    return 1024 + op * rings;
+    return 1024 + op * (2 + rings);
 }
 
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tk,
-                           const CUtensorMap &tv, size_t smem, cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
+                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem, cudaStream_t stream) {
     if (head_dim == 128)
-        return bf16 ? launch_t<128, true>(p, tk, tv, smem, stream) : launch_t<128, false>(p, tk, tv, smem, stream);
+        return bf16 ? launch_t<128, true>(p, tq, tk, tv, smem, stream)
+                    : launch_t<128, false>(p, tq, tk, tv, smem, stream);
     if (head_dim == 64)
-        return bf16 ? launch_t<64, true>(p, tk, tv, smem, stream) : launch_t<64, false>(p, tk, tv, smem, stream);
+        return bf16 ? launch_t<64, true>(p, tq, tk, tv, smem, stream)
+                    : launch_t<64, false>(p, tq, tk, tv, smem, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -9,8 +9,8 @@
 
 namespace pa {
 
-constexpr int kPrefillTile = 128;       // query rows per CTA = KV tokens per stage
-constexpr int kPrefillThreads = 352;    // 8 softmax warps, K loader, MMA issuer, V loader
+constexpr int kPrefillTile = 128;       // rows of a query tile = KV tokens per stage
+constexpr int kPrefillThreads = 608;    // 16 softmax warps, K/Q loader, MMA issuer, V loader
 
 struct PrefillParams {
     const void *q;                  // [num_tokens, num_heads, head_dim]
@@ -27,7 +27,8 @@ struct PrefillParams {
     int log2_group;                 // log2(num_heads / num_kv_heads)
     int block_size;
     int64_t num_blocks;
-    int tiles_per_seq;              // ceil(max_q_len * group / 128)
+    int tiles_per_seq;              // query tiles per sequence: ceil(max_q_len * group / 128)
+    int pairs_per_seq;              // CTAs per (sequence, KV head): ceil(tiles_per_seq / 2)
     float scale_log2;               // softmax scale * log2(e)
     int *err_flag;
 };
@@ -35,9 +36,9 @@ struct PrefillParams {
 // Dynamic shared memory of one prefill CTA.
 size_t prefill_smem_bytes(int head_dim);
 
-// Caches [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs, 128-byte
-// swizzle).
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tk,
-                           const CUtensorMap &tv, size_t smem, cudaStream_t stream);
+// query [num_tokens, Hq, D] through `tq` (box 64 x G x 128/G); caches
+// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); 128-byte swizzle.
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
+                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem, cudaStream_t stream);
 
 }  // namespace pa
