@@ -9,7 +9,8 @@
 
 namespace pa {
 
-constexpr int kPrefillTile = 128;       // rows of a query tile = KV tokens per stage
+constexpr int kPrefillTile = 128;       // rows of a query tile
+constexpr int kPrefillKV = 64;          // K/V tokens per pipeline stage
 constexpr int kPrefillThreads = 608;    // 16 softmax warps, K/Q loader, MMA issuer, V loader
 
 struct PrefillParams {
@@ -36,9 +37,9 @@ struct PrefillParams {
 // Dynamic shared memory of one prefill CTA.
 size_t prefill_smem_bytes(int head_dim);
 
-// query [num_tokens, Hq, D] through `tq` (box 64 x G x 128/G); caches
-// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); 128-byte swizzle.
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
-                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem, cudaStream_t stream);
+// Caches [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x min(bs, 64),
+// 128-byte swizzle).
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tk,
+                           const CUtensorMap &tv, size_t smem, cudaStream_t stream);
 
 }  // namespace pa
