@@ -24,18 +24,20 @@
 //                     written as 16-bit pairs over the S columns they came from;
 //   O_X += P_X V_j    tcgen05.mma with P read from tensor memory and V
 //                     (MN-major) from shared memory, O in tensor memory.
-// The MMA stream runs ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...; tcgen05
-// operations of one thread execute in issue order, so QK_X(j+1) overwrites
-// S_X only after PV_X(j) has read P_X from it, and when the softmax of tile
-// j+1 starts, O_X already holds tile j.  bfloat16 weights carry only 8
+// Each query tile has its own MMA-issuing thread, whose stream runs ...
+// PV_X(j), QK_X(j+1), PV_X(j+1) ...; tcgen05 operations of one thread execute
+// in issue order, so QK_X(j+1) overwrites S_X only after PV_X(j) has read P_X
+// from it, and when the softmax of tile j+1 starts, O_X already holds tile j.
+// Two issuers keep the tensor pipe fed while either one waits or commits.  bfloat16 weights carry only 8
 // significant bits, so for bf16 inputs P is split into P_hi + P_lo (both
 // bf16, P_lo = P - P_hi) and PV runs twice; binary16 weights are used as is.
 //
 // Warp roles: warps 0-15 load the query tiles into tensor memory and run the
 // softmax and the epilogue (warp w: query tile w / 8, column half (w / 4) % 2,
 // TMEM lanes 32 (w % 4)..); warp 16 loads the K tiles and warp 18 the V tiles
-// (both read the block table 32 entries at a time); warp 17 owns the tensor
-// memory and one of its lanes issues every MMA.  Every mbarrier wait is bounded (2 s); a timeout sets
+// (both read the block table 32 entries at a time); one lane of warp 17 issues
+// query tile A's MMAs (warp 17 also owns the tensor memory) and one lane of
+// warp 19 query tile B's.  Every mbarrier wait is bounded (2 s); a timeout sets
 // PA_FLAG_TIMEOUT and the CTA winds down without further MMAs.
 #include <math_constants.h>
 
@@ -55,7 +57,7 @@ constexpr uint32_t kTmemCols = 512;
 // at 128 + 64 X, O of X at 256 + 128 X.  P of a 32-key chunk sits in that
 // chunk's own S columns: 16 columns of hi pairs, then (bf16) 16 of lo pairs.
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
-constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18;
+constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18, kWarpMmaB = 19;
 constexpr int kMaxRing = 8;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -68,7 +70,8 @@ struct Shared {
     uint64_t q_full[2];                  // per query tile
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
     uint64_t s_full[2], p_full[2];       // per query tile
-    uint64_t done;
+    uint64_t done[2];                    // per query tile: all of its MMAs complete
+    uint64_t zeroed;                     // once: stale V rows of the last K/V tile zeroed
     uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
     float red[2][2][2][kTile];           // [use parity][query tile][column half][row]
     uint32_t tmem_base;
@@ -319,13 +322,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int qpos_max = qstartA + (hasB ? TT + min(TT, ql - t0A - TT) : min(TT, ql - t0A)) - 1;
     const int nB = hasB ? qpos_max / kKV + 1 : 0;
     const int n_tiles = hasB ? nB : nA;     // K/V tiles loaded (nB >= nA)
+    // The last K/V tile reaches past the last attended position: its stale or
+    // unloaded V rows are zeroed (by the query tile that reaches furthest)
+    // before any PV reads it, so that 0-weights cannot meet NaNs.
+    const bool zero_tail = n_tiles * kKV - 1 > qpos_max;
 
     if (threadIdx.x == 0) {
+        // A ring slot is free once every active query tile's issuer has
+        // released it (its MMAs reading the slot completed).
+        const uint32_t users = hasB ? 2u : 1u;
         for (int i = 0; i < kMaxRing; ++i) {
             mbar_init(&sh.k_full[i], 1);
-            mbar_init(&sh.k_empty[i], 1);
+            mbar_init(&sh.k_empty[i], users);
             mbar_init(&sh.v_full[i], 1);
-            mbar_init(&sh.v_empty[i], 1);
+            mbar_init(&sh.v_empty[i], users);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.q_full[i], 256);
@@ -334,7 +344,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int y = 0; y < 2; ++y)
                 for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][y][q], 64);
         }
-        mbar_init(&sh.done, 1);
+        mbar_init(&sh.done[0], 1);
+        mbar_init(&sh.done[1], 1);
+        mbar_init(&sh.zeroed, 256);
         sh.abort = 0;
         sh.bad = 0;
         fence_barrier_init();
@@ -372,91 +384,75 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int t = max(0, issued - NR); t < issued; ++t)
                 mbar_wait_bounded(&full[t % NR], (t / NR) & 1, kWaitLimitNs);
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+    } else if (warp == kWarpMma || warp == kWarpMmaB) {
+        // ------------------------------------------- MMA issuer of one query tile
+        const int xx = warp == kWarpMma ? 0 : 1;
+        if (lane == 0 && (xx == 0 || hasB)) {
             // Descriptors are built once; a stage or k-step only adds its byte
             // offset >> 4 to the 14-bit start-address field (shared addresses
             // stay below 256 KB, so the field never carries).
             const uint64_t kd0 = umma::desc_sw128(smem_addr(sK), 16, 1024);
             const uint64_t vd0 = umma::desc_sw128(smem_addr(sV), kRegion, 1024);
             constexpr uint32_t kOpDesc = kOp >> 4;
-            const int nx[2] = {nA, nB};
-            bool ok = true;
-            int k_ready = -1;                  // last K tile known to have landed
-            auto k_landed = [&](int t) -> bool {
-                if (k_ready >= t) return true;
-                if (!mbar_try_wait(&sh.k_full[t % NK], (t / NK) & 1)) return false;
-                k_ready = t;
-                return true;
-            };
-            auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
+            const int nx = xx == 0 ? nA : nB;
+            const uint32_t tq = tmem + kColQ + 64u * xx;
+            const uint32_t ts = tmem + kColS + 64u * xx;
+            const uint32_t tO = tmem + kColO + 128u * xx;
+            auto qk = [&](int t) -> bool {          // S_xx = Q_xx K_t^T, then release K_t
                 const int kst = t % NK;
-                if (k_ready < t) {
-                    if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
-                    k_ready = t;
-                }
+                if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
                 umma::fence_after_sync();
                 const uint64_t kd = kd0 + static_cast<uint64_t>(kst) * kOpDesc;
-                const uint32_t tq = tmem + kColQ + 64u * xx;
-                const uint32_t ts = tmem + kColS + 64u * xx;
 #pragma unroll
                 for (int k = 0; k < kKSteps; ++k)
                     umma::mma_ts(ts, tq + 8u * k, kd + static_cast<uint32_t>(((k >> 2) * kRegion + (k & 3) * 32) >> 4),
                                  kIdescQK, k > 0 ? 1u : 0u);
                 umma::commit(smem_addr(&sh.s_full[xx]));
+                umma::commit(smem_addr(&sh.k_empty[kst]));
                 return true;
             };
-            ok = wait_bar(&sh.q_full[0], 0, sh, p.err_flag) && qk(0, 0);
-            if (ok && hasB) ok = wait_bar(&sh.q_full[1], 0, sh, p.err_flag) && qk(1, 0);
-            if (ok) umma::commit(smem_addr(&sh.k_empty[0]));
+            bool ok = wait_bar(&sh.q_full[xx], 0, sh, p.err_flag) && qk(0);
             int vst = 0, vph = 0;
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                // On the last tile the zeroing of stale V rows (done by the
-                // softmax of the query tile that reaches furthest) precedes every PV.
-                if (j == n_tiles - 1 && hasB && nA == n_tiles && !wait_bar(&sh.p_full[1], j & 1, sh, p.err_flag)) {
+            for (int j = 0; ok && j < nx; ++j) {
+                if (zero_tail && j == n_tiles - 1 && !wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
                     ok = false;
                     break;
                 }
-                if (!wait_bar(&sh.v_full[vst], vph, sh, p.err_flag)) { ok = false; break; }
+                if (!wait_bar(&sh.v_full[vst], vph, sh, p.err_flag) ||
+                    !wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) {
+                    ok = false;
+                    break;
+                }
+                umma::fence_after_sync();
                 const uint64_t vd = vd0 + static_cast<uint64_t>(vst) * kOpDesc;
-                bool deferred[2] = {false, false};
-                for (int xx = 0; ok && xx < 2; ++xx) {
-                    if (j >= nx[xx]) continue;
-                    if (!wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) { ok = false; break; }
-                    umma::fence_after_sync();
-                    const uint32_t tP = tmem + kColS + 64u * xx;
-                    const uint32_t tO = tmem + kColO + 128u * xx;
-                    const uint32_t acc0 = j > 0 ? 1u : 0u;
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+                for (int k = 0; k < kPVSteps; ++k)
+                    umma::mma_ts(tO, ts + 32u * (k >> 1) + 8u * (k & 1), vd + static_cast<uint32_t>((k * 2048) >> 4),
+                                 kIdescPV, k > 0 ? 1u : acc0);
+                if constexpr (BF16) {
 #pragma unroll
                     for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1), vd + static_cast<uint32_t>((k * 2048) >> 4),
-                                     kIdescPV, k > 0 ? 1u : acc0);
-                    if constexpr (BF16) {
-#pragma unroll
-                        for (int k = 0; k < kPVSteps; ++k)
-                            umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
-                                         vd + static_cast<uint32_t>((k * 2048) >> 4), kIdescPV, 1u);
-                    }
-                    // S_xx(j+1) right behind PV_xx(j) if its K tile is here;
-                    // otherwise after the other query tile's PV.
-                    if (j + 1 < nx[xx]) {
-                        if (k_landed(j + 1)) ok = qk(xx, j + 1);
-                        else deferred[xx] = true;
-                    }
+                        umma::mma_ts(tO, ts + 32u * (k >> 1) + 8u * (k & 1) + 16u,
+                                     vd + static_cast<uint32_t>((k * 2048) >> 4), kIdescPV, 1u);
                 }
-                if (!ok) break;
                 umma::commit(smem_addr(&sh.v_empty[vst]));
-                for (int xx = 0; ok && xx < 2; ++xx)
-                    if (deferred[xx]) ok = qk(xx, j + 1);
-                if (ok && j + 1 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 1) % NK]));
+                if (j + 1 < nx) ok = qk(j + 1);        // S_xx(j+1) right behind PV_xx(j)
                 if (++vst == NV) {
                     vst = 0;
                     vph ^= 1;
                 }
             }
-            umma::commit(smem_addr(&sh.done));
-            mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
+            umma::commit(smem_addr(&sh.done[xx]));
+            // Tiles only the other query tile uses: release their ring slots on
+            // this tile's behalf, each after the slot's previous phase completed.
+            for (int t = nx; ok && t < n_tiles; ++t) {
+                if (t >= NK && !wait_bar(&sh.k_empty[t % NK], ((t / NK) - 1) & 1, sh, p.err_flag)) { ok = false; break; }
+                mbar_arrive(&sh.k_empty[t % NK]);
+                if (t >= NV && !wait_bar(&sh.v_empty[t % NV], ((t / NV) - 1) & 1, sh, p.err_flag)) { ok = false; break; }
+                mbar_arrive(&sh.v_empty[t % NV]);
+            }
+            mbar_wait_bounded(&sh.done[xx], 0, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp < 16 && (x == 0 || hasB)) {
@@ -491,8 +487,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             umma::fence_before_sync();
             mbar_arrive(&sh.q_full[x]);
         }
-        // The query tile that reaches furthest zeroes the stale V rows of the last K/V tile.
-        const bool zeroer = x == (hasB ? 1 : 0) && n_tiles * kKV - 1 > qpos_max;
+        const bool zeroer = zero_tail && x == (hasB ? 1 : 0);
         const float sl = p.scale_log2;
         const uint64_t sl2 = f2(sl, sl);
         float m_run = -CUDART_INF_F;
@@ -572,8 +567,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const float2 acc = unf2(add2(acc0, acc1));
             l_run += acc.x + acc.y;
             if (zeroer && j == nx - 1) {
-                // V rows past the last attended position hold stale or unloaded
-                // data; zero them so that 0-weights cannot meet NaNs.
                 const int vst = j % NV;
                 if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
                 if (row < kKV && j * kKV + row > qpos_max && (R > 1 || h == 0)) {
@@ -582,13 +575,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
+                mbar_arrive(&sh.zeroed);
             }
             umma::wait_st();
             umma::fence_before_sync();
             mbar_arrive(&sh.p_full[x]);
         }
-        // `done` completes once every MMA of the CTA (the last PV included) has.
-        if (ok && warp_wait_bar(&sh.done, 0, sh, p.err_flag)) {
+        // done[x] completes once every MMA of this query tile (the last PV included) has.
+        if (ok && warp_wait_bar(&sh.done[x], 0, sh, p.err_flag)) {
             umma::fence_after_sync();
             float l_other = 0.f;
             const bool have = pair_exchange(sh, nx, x, q4, h, row, l_run, l_other, p.err_flag);

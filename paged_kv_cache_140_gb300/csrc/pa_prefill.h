@@ -11,7 +11,7 @@ namespace pa {
 
 constexpr int kPrefillTile = 128;       // rows of a query tile
 constexpr int kPrefillKV = 64;          // K/V tokens per pipeline stage
-constexpr int kPrefillThreads = 608;    // 16 softmax warps, K/Q loader, MMA issuer, V loader
+constexpr int kPrefillThreads = 640;    // 16 softmax warps, K loader, MMA issuer A, V loader, MMA issuer B
 
 struct PrefillParams {
     const void *q;                  // [num_tokens, num_heads, head_dim]
