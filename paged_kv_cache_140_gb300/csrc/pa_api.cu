@@ -498,10 +498,10 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     const size_t smem = pa::prefill_smem_bytes(head_dim);
     if (smem + 4096 > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
-    const int box_rows = std::min(block_size, pa::kPrefillKV);
-    CUtensorMap tk, tv;
-    if (!encode_map_16(&tk, k_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, box_rows) ||
-        !encode_map_16(&tv, v_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, box_rows))
+    CUtensorMap tq, tk, tv;
+    if (!encode_map_16(&tq, query, head_dim, num_heads, num_tokens, G, tokens_per_tile) ||
+        !encode_map_16(&tk, k_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
+        !encode_map_16(&tv, v_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size))
         return PA_ERR_CUDA;
 
     pa::PrefillParams p{};
@@ -523,7 +523,7 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     p.pairs_per_seq = static_cast<int>((tiles + 1) / 2);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err_flag = err_flag;
-    cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tk, tv, smem,
+    cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tq, tk, tv, smem,
                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

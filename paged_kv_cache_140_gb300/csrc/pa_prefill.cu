@@ -9,15 +9,13 @@
 //
 // A query tile is 128 rows of one (sequence, KV head): 128/G tokens times the
 // G query heads that share the KV head.  One CTA runs two consecutive query
-// tiles, X = A and B, against every 64-token K/V tile it loads, so each K/V
+// tiles, X = A and B, against every 128-token K/V tile it loads, so each K/V
 // byte brought into shared memory feeds 256 query rows (the SM's intake of
-// K/V, not the tensor cores, is what a single tile would be limited by).  Both
-// query tiles live in tensor memory, which leaves shared memory to deep K and
-// V rings that cover the long latency of the paged, block-by-block loads.
+// K/V, not the tensor cores, is what a single tile would be limited by).
 // Per K/V tile j and query tile X:
-//   S_X = Q_X K_j^T   tcgen05.mma, Q from tensor memory, K from shared memory
-//                     (TMA, 128-byte swizzle), S in tensor memory;
-//   softmax           eight warps per query tile, two threads per row (32
+//   S_X = Q_X K_j^T   tcgen05.mma, Q and K tiles in shared memory (TMA,
+//                     128-byte swizzle), S in tensor memory;
+//   softmax           eight warps per query tile, two threads per row (64
 //                     columns each, the row max traded through shared memory);
 //                     running max and sum in registers, the output rescaled
 //                     only when the max grows by more than 2^8; the weights P
@@ -32,12 +30,11 @@
 // significant bits, so for bf16 inputs P is split into P_hi + P_lo (both
 // bf16, P_lo = P - P_hi) and PV runs twice; binary16 weights are used as is.
 //
-// Warp roles: warps 0-15 load the query tiles into tensor memory and run the
-// softmax and the epilogue (warp w: query tile w / 8, column half (w / 4) % 2,
-// TMEM lanes 32 (w % 4)..); warp 16 loads the K tiles and warp 18 the V tiles
-// (both read the block table 32 entries at a time); one lane of warp 17 issues
-// query tile A's MMAs (warp 17 also owns the tensor memory) and one lane of
-// warp 19 query tile B's.  Every mbarrier wait is bounded (2 s); a timeout sets
+// Warp roles: warps 0-15 run the softmax and the epilogue (warp w: query tile
+// w / 8, column half (w / 4) % 2, TMEM lanes 32 (w % 4)..); warp 16 loads the
+// query tiles and the K tiles, warp 18 the V tiles (both read the block table
+// 32 entries at a time); one lane of warp 17 issues query tile A's MMAs (warp
+// 17 also owns the tensor memory) and one lane of warp 19 query tile B's.  Every mbarrier wait is bounded (2 s); a timeout sets
 // PA_FLAG_TIMEOUT and the CTA winds down without further MMAs.
 #include <math_constants.h>
 
@@ -49,25 +46,24 @@
 namespace pa {
 namespace {
 
-constexpr int kTile = kPrefillTile;      // query rows per query tile
-constexpr int kKV = kPrefillKV;          // keys per K/V tile
-constexpr int kRegion = kKV * 128;       // 64 rows x 128 bytes: one swizzled operand region
+constexpr int kTile = kPrefillTile;
+constexpr int kRegion = kTile * 128;     // 128 rows x 128 bytes: one swizzled operand region
 constexpr uint32_t kTmemCols = 512;
-// Tensor memory: Q of query tile X at columns 64 X (16-bit pairs), S/P of X
-// at 128 + 64 X, O of X at 256 + 128 X.  P of a 32-key chunk sits in that
-// chunk's own S columns: 16 columns of hi pairs, then (bf16) 16 of lo pairs.
-constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
+// Tensor memory: S/P of query tile X at columns 128 X, O of X at 256 + 128 X.
+// P of a 32-key chunk sits in that chunk's own S columns: 16 columns of hi
+// pairs, then (bf16) 16 columns of lo pairs.
+constexpr uint32_t kColS = 0, kColO = 256;
 constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18, kWarpMmaB = 19;
-constexpr int kMaxRing = 8;
+constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// K and V ring depths (tiles of 64 tokens).
+// K and V ring depths (tiles of 128 tokens).
 template <int D> struct Rings;
-template <> struct Rings<128> { static constexpr int K = 6, V = 6; };
-template <> struct Rings<64> { static constexpr int K = 8, V = 8; };
+template <> struct Rings<128> { static constexpr int K = 2, V = 2; };
+template <> struct Rings<64> { static constexpr int K = 4, V = 4; };
 
 struct Shared {
-    uint64_t q_full[2];                  // per query tile
+    uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
     uint64_t s_full[2], p_full[2];       // per query tile
     uint64_t done[2];                    // per query tile: all of its MMAs complete
@@ -196,8 +192,8 @@ __device__ __forceinline__ void store_chunk(void *out, int out_dtype, int64_t el
 }
 
 // A loader warp's view of the block table: 32 consecutive entries, one per
-// lane, with the next 32 already requested (a tile never straddles two groups:
-// 64 / bs divides 32 for bs <= 64, and a larger block holds whole tiles).
+// lane, with the next 32 already requested (tiles never straddle two groups:
+// 128 / bs divides 32).
 struct TableWindow {
     const int32_t *table;
     int needed;          // entries that may be read: blocks holding positions <= qpos_max
@@ -210,7 +206,11 @@ struct TableWindow {
     __device__ int32_t id_for(int entry, int i, int lane) {
         const int b = entry & ~31;
         if (b != base) {
-            cur = (b == base + 32) ? nxt : fetch(b, lane);
+            if (b == base + 32) {
+                cur = nxt;
+            } else {
+                cur = fetch(b, lane);
+            }
             nxt = fetch(b + 32, lane);
             base = b;
         }
@@ -218,56 +218,55 @@ struct TableWindow {
     }
 };
 
-// Issue one 64-token K or V tile: boxes of min(bs, 64) rows, one per block it
-// covers, times the 64-column halves of the head.
+// Issue one 128-token K or V tile (8 blocks of 16 tokens for bs = 16, two
+// 64-column boxes each); returns false on an abort.
 template <int R>
 __device__ __forceinline__ void load_tile(TableWindow &win, int t, int bs, int qpos_max, int kvh, int64_t num_blocks,
                                           uint8_t *dst, const CUtensorMap *map, uint64_t *full, int lane,
                                           Shared &sh, int *err_flag) {
-    const int rpb = min(bs, kKV);                    // rows per box
-    const int first = t * kKV;
-    const int last = min(qpos_max, first + kKV - 1);
-    const int nbox = (last - first) / rpb + 1;
-    const int i = lane < nbox ? lane : 0;
-    const int32_t bid = win.id_for(first / bs, (i * rpb) / bs, lane);
-    const bool ok = lane < nbox && bid >= 0 && static_cast<int64_t>(bid) < num_blocks;
+    const int bpt = kTile / bs;
+    const int last = min(qpos_max, t * kTile + kTile - 1);
+    const int nb = (last - t * kTile) / bs + 1;
+    const int32_t bid = win.id_for(t * bpt, lane < nb ? lane : 0, lane);
+    const bool ok = lane < nb && bid >= 0 && static_cast<int64_t>(bid) < num_blocks;
     const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-    const unsigned want = (nbox >= 32) ? 0xffffffffu : ((1u << nbox) - 1u);
+    const unsigned want = (nb >= 32) ? 0xffffffffu : ((1u << nb) - 1u);
     if (lane == 0) {
         if (okmask != want) {
             report(err_flag, PA_FLAG_BAD_BLOCK_ID);
             sh.bad = 1;
         }
-        mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(okmask)) * rpb * 128u * R);
+        mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(okmask)) * bs * 128u * R);
     }
     __syncwarp();
     if (ok) {
-        const int z = bid * bs + (first + i * rpb) % bs;
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            tma_load_3d_plain(dst + r * kRegion + i * rpb * 128, map, full, r * 64, kvh, z);
+            tma_load_3d_plain(dst + r * kRegion + lane * bs * 128, map, full, r * 64, kvh, bid * bs);
     }
 }
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     paged_prefill_kernel(const __grid_constant__ PrefillParams p,
+                         const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv) {
     constexpr int R = D / 64;               // 128-byte regions per row
-    constexpr int kOp = R * kRegion;        // one 64-row K or V tile
+    constexpr int kOp = R * kRegion;        // one 128-row operand tile
     constexpr int NK = Rings<D>::K, NV = Rings<D>::V;
     constexpr int kKSteps = D / 16;         // QK MMAs per tile (K = 16 each)
-    constexpr int kPVSteps = kKV / 16;      // PV MMAs per tile and weight part
-    constexpr int kHalfD = D / 2;           // O columns and query dims per softmax thread
-    constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kKV, false);
+    constexpr int kPVSteps = kTile / 16;    // PV MMAs per tile and weight part
+    constexpr int kHalfD = D / 2;           // O columns per softmax thread
+    constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kTile, false);
     constexpr uint32_t kIdescPV = umma::idesc_f16(BF16, kTile, D, true);
 
     __shared__ Shared sh;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sK = base;                     // K ring: NK tiles
+    uint8_t *sQ = base;                     // query tiles A, B
+    uint8_t *sK = sQ + 2 * kOp;             // K ring: NK tiles
     uint8_t *sV = sK + NK * kOp;            // V ring: NV tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int ctx = __ldg(p.context_lens + s);
 
     // Softmax threads: query tile x, row `row` (token rtok, head kvh * G + row % G),
-    // keys [32 h, 32 h + 32) of each K/V tile, O columns [D/2 h, D/2 h + D/2).
+    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O.
     const int x = (warp >> 3) & 1, q4 = warp & 3, h = (warp >> 2) & 1;
     const int row = 32 * q4 + lane;
     const int rtok = row >> lg;
@@ -318,16 +317,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         return;
     }
     const int qstartA = ctx - ql + t0A;     // position of tile A's first query token
-    const int nA = (qstartA + min(TT, ql - t0A) - 1) / kKV + 1;
+    const int nA = (qstartA + min(TT, ql - t0A) - 1) / kTile + 1;
     const int qpos_max = qstartA + (hasB ? TT + min(TT, ql - t0A - TT) : min(TT, ql - t0A)) - 1;
-    const int nB = hasB ? qpos_max / kKV + 1 : 0;
+    const int nB = hasB ? qpos_max / kTile + 1 : 0;
     const int n_tiles = hasB ? nB : nA;     // K/V tiles loaded (nB >= nA)
     // The last K/V tile reaches past the last attended position: its stale or
     // unloaded V rows are zeroed (by the query tile that reaches furthest)
     // before any PV reads it, so that 0-weights cannot meet NaNs.
-    const bool zero_tail = n_tiles * kKV - 1 > qpos_max;
+    const bool zero_tail = n_tiles * kTile - 1 > qpos_max;
 
     if (threadIdx.x == 0) {
+        mbar_init(&sh.q_full, 1);
         // A ring slot is free once every active query tile's issuer has
         // released it (its MMAs reading the slot completed).
         const uint32_t users = hasB ? 2u : 1u;
@@ -338,7 +338,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_init(&sh.v_empty[i], users);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.q_full[i], 256);
             mbar_init(&sh.s_full[i], 1);
             mbar_init(&sh.p_full[i], 256);
             for (int y = 0; y < 2; ++y)
@@ -368,7 +367,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         uint64_t *full = is_k ? sh.k_full : sh.v_full;
         uint64_t *empty = is_k ? sh.k_empty : sh.v_empty;
         uint8_t *ring = is_k ? sK : sV;
-        if (lane == 0) prefetch_tensormap(map);
+        if (lane == 0) {
+            prefetch_tensormap(map);
+            if (is_k) {
+                prefetch_tensormap(&tq);
+                mbar_arrive_expect_tx(&sh.q_full, kOp * (hasB ? 2 : 1));
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    tma_load_3d_plain(sQ + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A);
+                    if (hasB)
+                        tma_load_3d_plain(sQ + kOp + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A + TT);
+                }
+            }
+        }
         TableWindow win{p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq,
                         qpos_max / p.block_size + 1};
         int issued = 0;
@@ -383,6 +394,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (lane == 0 && sh.abort) {
             for (int t = max(0, issued - NR); t < issued; ++t)
                 mbar_wait_bounded(&full[t % NR], (t / NR) & 1, kWaitLimitNs);
+            if (is_k) mbar_wait_bounded(&sh.q_full, 0, kWaitLimitNs);
         }
     } else if (warp == kWarpMma || warp == kWarpMmaB) {
         // ------------------------------------------- MMA issuer of one query tile
@@ -391,12 +403,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             // Descriptors are built once; a stage or k-step only adds its byte
             // offset >> 4 to the 14-bit start-address field (shared addresses
             // stay below 256 KB, so the field never carries).
+            const uint64_t qd = umma::desc_sw128(smem_addr(sQ + xx * kOp), 16, 1024);
             const uint64_t kd0 = umma::desc_sw128(smem_addr(sK), 16, 1024);
             const uint64_t vd0 = umma::desc_sw128(smem_addr(sV), kRegion, 1024);
             constexpr uint32_t kOpDesc = kOp >> 4;
             const int nx = xx == 0 ? nA : nB;
-            const uint32_t tq = tmem + kColQ + 64u * xx;
-            const uint32_t ts = tmem + kColS + 64u * xx;
+            const uint32_t ts = tmem + kColS + 128u * xx;
             const uint32_t tO = tmem + kColO + 128u * xx;
             auto qk = [&](int t) -> bool {          // S_xx = Q_xx K_t^T, then release K_t
                 const int kst = t % NK;
@@ -404,14 +416,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 umma::fence_after_sync();
                 const uint64_t kd = kd0 + static_cast<uint64_t>(kst) * kOpDesc;
 #pragma unroll
-                for (int k = 0; k < kKSteps; ++k)
-                    umma::mma_ts(ts, tq + 8u * k, kd + static_cast<uint32_t>(((k >> 2) * kRegion + (k & 3) * 32) >> 4),
-                                 kIdescQK, k > 0 ? 1u : 0u);
+                for (int k = 0; k < kKSteps; ++k) {
+                    const uint32_t off = static_cast<uint32_t>(((k >> 2) * kRegion + (k & 3) * 32) >> 4);
+                    umma::mma_ss(ts, qd + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
+                }
                 umma::commit(smem_addr(&sh.s_full[xx]));
                 umma::commit(smem_addr(&sh.k_empty[kst]));
                 return true;
             };
-            bool ok = wait_bar(&sh.q_full[xx], 0, sh, p.err_flag) && qk(0);
+            bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag) && qk(0);
             int vst = 0, vph = 0;
             for (int j = 0; ok && j < nx; ++j) {
                 if (zero_tail && j == n_tiles - 1 && !wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
@@ -456,37 +469,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         __syncwarp();
     } else if (warp < 16 && (x == 0 || hasB)) {
-        // -------------------------------- query tile, softmax and epilogue
+        // ------------------------------------------- softmax and epilogue
         const int nx = x == 0 ? nA : nB;
         const int qpos = rtok < ntokx ? qstartA + x * TT + rtok : -1;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-        const uint32_t tS = tmem + kColS + 64u * x + lane_off + 32u * h;
+        const uint32_t tS = tmem + kColS + 128u * x + lane_off + 64u * h;
         const uint32_t tO = tmem + kColO + 128u * x + lane_off + kHalfD * h;
-        {
-            // This thread's half of its query row -> Q columns [D/4 h, D/4 h + D/4).
-            uint32_t qw[kHalfD / 2];
-            if (qpos >= 0) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
-                                                                   out_row * D + kHalfD * h);
-#pragma unroll
-                for (int i = 0; i < kHalfD / 8; ++i) {
-                    const uint4 v = __ldg(src + i);
-                    qw[4 * i] = v.x;
-                    qw[4 * i + 1] = v.y;
-                    qw[4 * i + 2] = v.z;
-                    qw[4 * i + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kHalfD / 2; ++i) qw[i] = 0u;
-            }
-#pragma unroll
-            for (int c = 0; c < kHalfD / 32; ++c)
-                umma::st_32x32b_x16(tmem + kColQ + 64u * x + lane_off + (kHalfD / 2) * h + 16 * c, qw + 16 * c);
-            umma::wait_st();
-            umma::fence_before_sync();
-            mbar_arrive(&sh.q_full[x]);
-        }
+        // The tile that reaches furthest zeroes the stale V rows of the last K/V tile.
         const bool zeroer = zero_tail && x == (hasB ? 1 : 0);
         const float sl = p.scale_log2;
         const uint64_t sl2 = f2(sl, sl);
@@ -496,24 +485,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int j = 0; j < nx; ++j) {
             if (!warp_wait_bar(&sh.s_full[x], j & 1, sh, p.err_flag)) { ok = false; break; }
             umma::fence_after_sync();
-            uint32_t v[32];
-            umma::ld_32x32b_x32(tS, v);
-            umma::wait_ld();
-            const int lim = qpos - j * kKV - 32 * h;    // keys c <= lim are attended
-            if (!__all_sync(0xffffffffu, lim >= 31)) {
+            const int lim = qpos - j * kTile - 64 * h;   // columns c <= lim are attended
+            const bool masked = !__all_sync(0xffffffffu, lim >= 63);
+            float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i > lim) v[i] = 0xff800000u;     // -inf
-            }
-            float a0 = -CUDART_INF_F, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                umma::ld_32x32b_x32(tS + 32 * c, v);
+                umma::wait_ld();
+                if (masked) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a0 = max3(a0, __uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
-                a1 = max3(a1, __uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
-                a2 = max3(a2, __uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
-                a3 = max3(a3, __uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i > lim) v[i] = 0xff800000u;     // -inf
+                }
+                float a0 = mx, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    a0 = max3(a0, __uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
+                    a1 = max3(a1, __uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+                    a2 = max3(a2, __uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+                    a3 = max3(a3, __uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+                }
+                mx = max3(a0, a1, fmaxf(a2, a3));
             }
-            float mx = max3(a0, a1, fmaxf(a2, a3));
             float mx_other;
             if (!pair_exchange(sh, j, x, q4, h, row, mx, mx_other, p.err_flag)) { ok = false; break; }
             mx = fmaxf(mx, mx_other);
@@ -531,9 +525,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                         umma::wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float2 ov = unf2(mul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2x));
-                            o[2 * i] = __float_as_uint(ov.x);
-                            o[2 * i + 1] = __float_as_uint(ov.y);
+                            const float2 v = unf2(mul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2x));
+                            o[2 * i] = __float_as_uint(v.x);
+                            o[2 * i + 1] = __float_as_uint(v.y);
                         }
                         st_32x32b_x32(tO + 32 * c, o);
                     }
@@ -543,33 +537,47 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     m_run = x_tile;
                 }
             }
-            // weights p = 2^(s * scale_log2 - m) as 16-bit pairs over this chunk's S columns
+            // weights p = 2^(s * scale_log2 - m) as 16-bit pairs, each 32-key
+            // chunk written over its own S columns
             const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
             const uint64_t nm2 = f2(-mref, -mref);
             uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
-            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float2 xv = unf2(fma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2, nm2));
-                const float p0 = fast_exp2(xv.x), p1 = fast_exp2(xv.y);
-                hi[i] = pack2<BF16>(p0, p1);
-                const float2 hv = Half2x<BF16>::to_float2(hi[i]);
-                if constexpr (BF16) {
-                    const float2 lv = unf2(sub2(f2(p0, p1), f2(hv.x, hv.y)));
-                    lo[i] = pack2<true>(lv.x, lv.y);
-                    if (i & 1) acc1 = add2(acc1, f2(p0, p1)); else acc0 = add2(acc0, f2(p0, p1));
-                } else {
-                    if (i & 1) acc1 = add2(acc1, f2(hv.x, hv.y)); else acc0 = add2(acc0, f2(hv.x, hv.y));
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                umma::ld_32x32b_x32(tS + 32 * c, v);
+                umma::wait_ld();
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i > lim) v[i] = 0xff800000u;
                 }
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float2 xv = unf2(fma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2, nm2));
+                    const float p0 = fast_exp2(xv.x), p1 = fast_exp2(xv.y);
+                    hi[i] = pack2<BF16>(p0, p1);
+                    const float2 hv = Half2x<BF16>::to_float2(hi[i]);
+                    if constexpr (BF16) {
+                        const float2 lv = unf2(sub2(f2(p0, p1), f2(hv.x, hv.y)));
+                        lo[i] = pack2<true>(lv.x, lv.y);
+                        if (i & 1) acc1 = add2(acc1, f2(p0, p1)); else acc0 = add2(acc0, f2(p0, p1));
+                    } else {
+                        if (i & 1) acc1 = add2(acc1, f2(hv.x, hv.y)); else acc0 = add2(acc0, f2(hv.x, hv.y));
+                    }
+                }
+                umma::st_32x32b_x16(tS + 32 * c, hi);
+                if constexpr (BF16) umma::st_32x32b_x16(tS + 32 * c + 16, lo);
             }
-            umma::st_32x32b_x16(tS, hi);
-            if constexpr (BF16) umma::st_32x32b_x16(tS + 16, lo);
             const float2 acc = unf2(add2(acc0, acc1));
             l_run += acc.x + acc.y;
             if (zeroer && j == nx - 1) {
+                // V rows past the last attended position hold stale or unloaded
+                // data; zero them so that 0-weights cannot meet NaNs.
                 const int vst = j % NV;
                 if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-                if (row < kKV && j * kKV + row > qpos_max && (R > 1 || h == 0)) {
+                if (j * kTile + row > qpos_max && (R > 1 || h == 0)) {
                     uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + (R > 1 ? h : 0) * kRegion + row * 128);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -594,10 +602,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 uint32_t o[32];
                 umma::ld_32x32b_x32(tO + 32 * c, o);
                 umma::wait_ld();
-                float ov[32];
+                float v[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] = zero ? 0.f : __uint_as_float(o[i]) * inv;
-                if (qpos >= 0) store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, ov);
+                for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : __uint_as_float(o[i]) * inv;
+                if (qpos >= 0) store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, v);
             }
         }
     }
@@ -611,14 +619,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 }
 
 template <int D, bool BF16>
-cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tk, const CUtensorMap &tv, size_t smem,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                     size_t smem, cudaStream_t stream) {
     auto kern = paged_prefill_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.pairs_per_seq;
-    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tk, tv);
+    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
@@ -627,15 +635,17 @@ cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tk, const CUtens
 size_t prefill_smem_bytes(int head_dim) {
     const size_t op = static_cast<size_t>(head_dim / 64) * kRegion;
     const int rings = head_dim == 128 ? Rings<128>::K + Rings<128>::V : Rings<64>::K + Rings<64>::V;
-    return 1024 + op * rings;
+    return 1024 + op * (2 + rings);
 }
 
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tk,
-                           const CUtensorMap &tv, size_t smem, cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
+                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem, cudaStream_t stream) {
     if (head_dim == 128)
-        return bf16 ? launch_t<128, true>(p, tk, tv, smem, stream) : launch_t<128, false>(p, tk, tv, smem, stream);
+        return bf16 ? launch_t<128, true>(p, tq, tk, tv, smem, stream)
+                    : launch_t<128, false>(p, tq, tk, tv, smem, stream);
     if (head_dim == 64)
-        return bf16 ? launch_t<64, true>(p, tk, tv, smem, stream) : launch_t<64, false>(p, tk, tv, smem, stream);
+        return bf16 ? launch_t<64, true>(p, tq, tk, tv, smem, stream)
+                    : launch_t<64, false>(p, tq, tk, tv, smem, stream);
     return cudaErrorInvalidValue;
 }
 

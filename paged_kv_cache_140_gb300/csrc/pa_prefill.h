@@ -9,9 +9,8 @@
 
 namespace pa {
 
-constexpr int kPrefillTile = 128;       // rows of a query tile
-constexpr int kPrefillKV = 64;          // K/V tokens per pipeline stage
-constexpr int kPrefillThreads = 640;    // 16 softmax warps, K loader, MMA issuer A, V loader, MMA issuer B
+constexpr int kPrefillTile = 128;       // rows of a query tile = KV tokens per stage
+constexpr int kPrefillThreads = 640;    // 16 softmax warps, K/Q loader, MMA issuer A, V loader, MMA issuer B
 
 struct PrefillParams {
     const void *q;                  // [num_tokens, num_heads, head_dim]
@@ -37,9 +36,9 @@ struct PrefillParams {
 // Dynamic shared memory of one prefill CTA.
 size_t prefill_smem_bytes(int head_dim);
 
-// Caches [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x min(bs, 64),
-// 128-byte swizzle).
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tk,
-                           const CUtensorMap &tv, size_t smem, cudaStream_t stream);
+// query [num_tokens, Hq, D] through `tq` (box 64 x G x 128/G); caches
+// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); 128-byte swizzle.
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
+                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem, cudaStream_t stream);
 
 }  // namespace pa
