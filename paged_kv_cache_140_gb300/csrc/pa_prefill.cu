@@ -22,19 +22,18 @@
 //                     written as 16-bit pairs over the S columns they came from;
 //   O_X += P_X V_j    tcgen05.mma with P read from tensor memory and V
 //                     (MN-major) from shared memory, O in tensor memory.
-// Each query tile has its own MMA-issuing thread, whose stream runs ...
-// PV_X(j), QK_X(j+1), PV_X(j+1) ...; tcgen05 operations of one thread execute
-// in issue order, so QK_X(j+1) overwrites S_X only after PV_X(j) has read P_X
-// from it, and when the softmax of tile j+1 starts, O_X already holds tile j.
-// Two issuers keep the tensor pipe fed while either one waits or commits.  bfloat16 weights carry only 8
+// The MMA stream runs ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...; tcgen05
+// operations of one thread execute in issue order, so QK_X(j+1) overwrites
+// S_X only after PV_X(j) has read P_X from it, and when the softmax of tile
+// j+1 starts, O_X already holds tile j.  bfloat16 weights carry only 8
 // significant bits, so for bf16 inputs P is split into P_hi + P_lo (both
 // bf16, P_lo = P - P_hi) and PV runs twice; binary16 weights are used as is.
 //
 // Warp roles: warps 0-15 run the softmax and the epilogue (warp w: query tile
 // w / 8, column half (w / 4) % 2, TMEM lanes 32 (w % 4)..); warp 16 loads the
 // query tiles and the K tiles, warp 18 the V tiles (both read the block table
-// 32 entries at a time); one lane of warp 17 issues query tile A's MMAs (warp
-// 17 also owns the tensor memory) and one lane of warp 19 query tile B's.  Every mbarrier wait is bounded (2 s); a timeout sets
+// 32 entries at a time); warp 17 owns the tensor memory and one of its lanes
+// issues every MMA.  Every mbarrier wait is bounded (2 s); a timeout sets
 // PA_FLAG_TIMEOUT and the CTA winds down without further MMAs.
 #include <math_constants.h>
 
@@ -53,7 +52,7 @@ constexpr uint32_t kTmemCols = 512;
 // P of a 32-key chunk sits in that chunk's own S columns: 16 columns of hi
 // pairs, then (bf16) 16 columns of lo pairs.
 constexpr uint32_t kColS = 0, kColO = 256;
-constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18, kWarpMmaB = 19;
+constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18;
 constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -66,8 +65,7 @@ struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
     uint64_t s_full[2], p_full[2];       // per query tile
-    uint64_t done[2];                    // per query tile: all of its MMAs complete
-    uint64_t zeroed;                     // once: stale V rows of the last K/V tile zeroed
+    uint64_t done;
     uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
     float red[2][2][2][kTile];           // [use parity][query tile][column half][row]
     uint32_t tmem_base;
@@ -321,21 +319,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int qpos_max = qstartA + (hasB ? TT + min(TT, ql - t0A - TT) : min(TT, ql - t0A)) - 1;
     const int nB = hasB ? qpos_max / kTile + 1 : 0;
     const int n_tiles = hasB ? nB : nA;     // K/V tiles loaded (nB >= nA)
-    // The last K/V tile reaches past the last attended position: its stale or
-    // unloaded V rows are zeroed (by the query tile that reaches furthest)
-    // before any PV reads it, so that 0-weights cannot meet NaNs.
-    const bool zero_tail = n_tiles * kTile - 1 > qpos_max;
 
     if (threadIdx.x == 0) {
         mbar_init(&sh.q_full, 1);
-        // A ring slot is free once every active query tile's issuer has
-        // released it (its MMAs reading the slot completed).
-        const uint32_t users = hasB ? 2u : 1u;
         for (int i = 0; i < kMaxRing; ++i) {
             mbar_init(&sh.k_full[i], 1);
-            mbar_init(&sh.k_empty[i], users);
+            mbar_init(&sh.k_empty[i], 1);
             mbar_init(&sh.v_full[i], 1);
-            mbar_init(&sh.v_empty[i], users);
+            mbar_init(&sh.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.s_full[i], 1);
@@ -343,9 +334,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int y = 0; y < 2; ++y)
                 for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][y][q], 64);
         }
-        mbar_init(&sh.done[0], 1);
-        mbar_init(&sh.done[1], 1);
-        mbar_init(&sh.zeroed, 256);
+        mbar_init(&sh.done, 1);
         sh.abort = 0;
         sh.bad = 0;
         fence_barrier_init();
@@ -396,76 +385,72 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 mbar_wait_bounded(&full[t % NR], (t / NR) & 1, kWaitLimitNs);
             if (is_k) mbar_wait_bounded(&sh.q_full, 0, kWaitLimitNs);
         }
-    } else if (warp == kWarpMma || warp == kWarpMmaB) {
-        // ------------------------------------------- MMA issuer of one query tile
-        const int xx = warp == kWarpMma ? 0 : 1;
-        if (lane == 0 && (xx == 0 || hasB)) {
-            // Descriptors are built once; a stage or k-step only adds its byte
-            // offset >> 4 to the 14-bit start-address field (shared addresses
-            // stay below 256 KB, so the field never carries).
-            const uint64_t qd = umma::desc_sw128(smem_addr(sQ + xx * kOp), 16, 1024);
-            const uint64_t kd0 = umma::desc_sw128(smem_addr(sK), 16, 1024);
-            const uint64_t vd0 = umma::desc_sw128(smem_addr(sV), kRegion, 1024);
-            constexpr uint32_t kOpDesc = kOp >> 4;
-            const int nx = xx == 0 ? nA : nB;
-            const uint32_t ts = tmem + kColS + 128u * xx;
-            const uint32_t tO = tmem + kColO + 128u * xx;
-            auto qk = [&](int t) -> bool {          // S_xx = Q_xx K_t^T, then release K_t
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t q_addr = smem_addr(sQ);
+            const uint32_t k_addr = smem_addr(sK);
+            const uint32_t v_addr = smem_addr(sV);
+            const int nx[2] = {nA, nB};
+            bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag);
+            int k_ready = -1;                  // last K tile known to have landed
+            auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
                 const int kst = t % NK;
-                if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                if (k_ready < t) {
+                    if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                    k_ready = t;
+                }
                 umma::fence_after_sync();
-                const uint64_t kd = kd0 + static_cast<uint64_t>(kst) * kOpDesc;
+                const uint32_t kt = k_addr + static_cast<uint32_t>(kst * kOp);
+                const uint32_t qx = q_addr + static_cast<uint32_t>(xx * kOp);
 #pragma unroll
                 for (int k = 0; k < kKSteps; ++k) {
-                    const uint32_t off = static_cast<uint32_t>(((k >> 2) * kRegion + (k & 3) * 32) >> 4);
-                    umma::mma_ss(ts, qd + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
+                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+                    umma::mma_ss(tmem + kColS + 128u * xx, umma::desc_sw128(qx + off, 16, 1024),
+                                 umma::desc_sw128(kt + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
                 }
                 umma::commit(smem_addr(&sh.s_full[xx]));
-                umma::commit(smem_addr(&sh.k_empty[kst]));
                 return true;
             };
-            bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag) && qk(0);
-            int vst = 0, vph = 0;
-            for (int j = 0; ok && j < nx; ++j) {
-                if (zero_tail && j == n_tiles - 1 && !wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
+            if (ok) ok = qk(0, 0);
+            if (ok && hasB) ok = qk(1, 0);
+            if (ok) umma::commit(smem_addr(&sh.k_empty[0]));
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int vst = j % NV;
+                const bool last = j == n_tiles - 1;
+                // On the last tile the zeroing of stale V rows (done by the
+                // softmax of the tile that reaches furthest) precedes every PV.
+                if (last && hasB && nA == n_tiles && !wait_bar(&sh.p_full[1], j & 1, sh, p.err_flag)) {
                     ok = false;
                     break;
                 }
-                if (!wait_bar(&sh.v_full[vst], vph, sh, p.err_flag) ||
-                    !wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) {
-                    ok = false;
-                    break;
-                }
-                umma::fence_after_sync();
-                const uint64_t vd = vd0 + static_cast<uint64_t>(vst) * kOpDesc;
-                const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-                for (int k = 0; k < kPVSteps; ++k)
-                    umma::mma_ts(tO, ts + 32u * (k >> 1) + 8u * (k & 1), vd + static_cast<uint32_t>((k * 2048) >> 4),
-                                 kIdescPV, k > 0 ? 1u : acc0);
-                if constexpr (BF16) {
+                if (!wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
+                for (int xx = 0; ok && xx < 2; ++xx) {
+                    if (j >= nx[xx]) continue;
+                    if (!wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) { ok = false; break; }
+                    umma::fence_after_sync();
+                    const uint32_t vt = v_addr + static_cast<uint32_t>(vst * kOp);
+                    const uint32_t tP = tmem + kColS + 128u * xx;
+                    const uint32_t tO = tmem + kColO + 128u * xx;
 #pragma unroll
                     for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tO, ts + 32u * (k >> 1) + 8u * (k & 1) + 16u,
-                                     vd + static_cast<uint32_t>((k * 2048) >> 4), kIdescPV, 1u);
+                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1),
+                                     umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV,
+                                     (j > 0 || k > 0) ? 1u : 0u);
+                    if constexpr (BF16) {
+#pragma unroll
+                        for (int k = 0; k < kPVSteps; ++k)
+                            umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
+                                         umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV, 1u);
+                    }
+                    if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
                 }
+                if (!ok) break;
                 umma::commit(smem_addr(&sh.v_empty[vst]));
-                if (j + 1 < nx) ok = qk(j + 1);        // S_xx(j+1) right behind PV_xx(j)
-                if (++vst == NV) {
-                    vst = 0;
-                    vph ^= 1;
-                }
+                if (j + 1 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 1) % NK]));
             }
-            umma::commit(smem_addr(&sh.done[xx]));
-            // Tiles only the other query tile uses: release their ring slots on
-            // this tile's behalf, each after the slot's previous phase completed.
-            for (int t = nx; ok && t < n_tiles; ++t) {
-                if (t >= NK && !wait_bar(&sh.k_empty[t % NK], ((t / NK) - 1) & 1, sh, p.err_flag)) { ok = false; break; }
-                mbar_arrive(&sh.k_empty[t % NK]);
-                if (t >= NV && !wait_bar(&sh.v_empty[t % NV], ((t / NV) - 1) & 1, sh, p.err_flag)) { ok = false; break; }
-                mbar_arrive(&sh.v_empty[t % NV]);
-            }
-            mbar_wait_bounded(&sh.done[xx], 0, kWaitLimitNs);
+            umma::commit(smem_addr(&sh.done));
+            mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp < 16 && (x == 0 || hasB)) {
@@ -476,7 +461,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const uint32_t tS = tmem + kColS + 128u * x + lane_off + 64u * h;
         const uint32_t tO = tmem + kColO + 128u * x + lane_off + kHalfD * h;
         // The tile that reaches furthest zeroes the stale V rows of the last K/V tile.
-        const bool zeroer = zero_tail && x == (hasB ? 1 : 0);
+        const bool zeroer = x == (hasB ? 1 : 0) && n_tiles * kTile - 1 > qpos_max;
         const float sl = p.scale_log2;
         const uint64_t sl2 = f2(sl, sl);
         float m_run = -CUDART_INF_F;
@@ -583,14 +568,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&sh.zeroed);
             }
             umma::wait_st();
             umma::fence_before_sync();
             mbar_arrive(&sh.p_full[x]);
         }
-        // done[x] completes once every MMA of this query tile (the last PV included) has.
-        if (ok && warp_wait_bar(&sh.done[x], 0, sh, p.err_flag)) {
+        // `done` completes once every MMA of the CTA (the last PV included) has.
+        if (ok && warp_wait_bar(&sh.done, 0, sh, p.err_flag)) {
             umma::fence_after_sync();
             float l_other = 0.f;
             const bool have = pair_exchange(sh, nx, x, q4, h, row, l_run, l_other, p.err_flag);

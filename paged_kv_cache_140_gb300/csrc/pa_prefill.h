@@ -10,7 +10,7 @@
 namespace pa {
 
 constexpr int kPrefillTile = 128;       // rows of a query tile = KV tokens per stage
-constexpr int kPrefillThreads = 640;    // 16 softmax warps, K/Q loader, MMA issuer A, V loader, MMA issuer B
+constexpr int kPrefillThreads = 608;    // 16 softmax warps, K/Q loader, MMA issuer, V loader
 
 struct PrefillParams {
     const void *q;                  // [num_tokens, num_heads, head_dim]
