@@ -589,7 +589,7 @@ def run_prefill(args, world, rank, local):
             "peak": peak,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
-            "traffic": None,
+            "traffic": load_traffic(args.workload, "prefill"),
             "algorithmic_flops_per_launch": flops,
             "launch_us": round(attn_ms * 1e3, 2),
             "peak_kind": peak_kind,
@@ -671,26 +671,36 @@ def run_prefill_reference(args, world, rank):
     }), flush=True)
 
 
-def decode_source_hash() -> str:
-    """Hash of the decode kernel's sources; a traffic figure taken from an
-    older kernel is not reported."""
+KERNEL_SOURCES = {
+    "decode": ("pa_decode.cu", "pa_device.cuh", "pa_internal.h"),
+    "prefill": ("pa_prefill.cu", "pa_prefill.h", "pa_umma.cuh", "pa_device.cuh"),
+}
+
+
+def source_hash(kind: str = "decode") -> str:
+    """Hash of a kernel's sources; a traffic figure taken from an older kernel
+    is not reported."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("pa_decode.cu", "pa_device.cuh", "pa_internal.h"):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "paged_kv_cache_140_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic(workload):
-    """DRAM bytes per decode launch (ncu dram__bytes_read.sum + write.sum),
-    scaled to this workload, from the committed profile summary - or None
-    when the summary was taken on a different kernel source."""
+def decode_source_hash() -> str:
+    return source_hash("decode")
+
+
+def load_traffic(workload, kind: str = "decode"):
+    """DRAM bytes per launch of the workload's main kernel (ncu
+    dram__bytes_read.sum + write.sum) from the committed profile summary, or
+    None when the summary was taken on a different kernel source."""
     path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("kernel_source_hash") != decode_source_hash():
+        if d.get("kernel_source_hash") != source_hash(kind):
             return None
         return d.get("dram_bytes_per_launch")
     except Exception:
