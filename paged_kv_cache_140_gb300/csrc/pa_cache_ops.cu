@@ -15,30 +15,48 @@ namespace pa {
 
 namespace {
 
-// grid.x: tokens (grid-stride), grid.y: slices of the row; each thread moves
-// one 16-byte chunk of K and one of V per token, so every chunk of a small
-// batch is in flight at once.  The kernel lets the next kernel in the stream
-// (normally the decode, launched with programmatic dependent launch) start
-// early; that kernel still waits for this one to complete before reading.
+// grid.x: tokens (grid-stride); a CTA moves a token's whole K and V row, each
+// thread up to 8 + 8 16-byte chunks at a time with all loads issued before
+// the stores, and with up to 16 CTAs per SM many tokens are in flight.  The
+// kernel lets the next kernel in the stream (normally the decode, launched
+// with programmatic dependent launch) start early; that kernel still waits
+// for this one to complete before reading.
 __global__ void __launch_bounds__(128)
     reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                              uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                              const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
                              int64_t num_slots, int64_t row16, int *err_flag) {
     pdl_launch_dependents();
-    const int64_t i = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
+    constexpr int kU = 8;
     for (int64_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
         const int64_t slot = slot_mapping[t];
         if (slot < 0) continue;
         if (slot >= num_slots) {
-            if (threadIdx.x == 0 && blockIdx.y == 0) report(err_flag, 0x1 /* PA_FLAG_BAD_SLOT */);
+            if (threadIdx.x == 0) report(err_flag, 0x1 /* PA_FLAG_BAD_SLOT */);
             continue;
         }
-        for (int64_t c = i; c < row16; c += static_cast<int64_t>(gridDim.y) * blockDim.x) {
-            const uint4 a = __ldg(key + t * row16 + c);
-            const uint4 b = __ldg(value + t * row16 + c);
-            k_cache[slot * row16 + c] = a;
-            v_cache[slot * row16 + c] = b;
+        const uint4 *ks = key + t * row16;
+        const uint4 *vs = value + t * row16;
+        uint4 *kd = k_cache + slot * row16;
+        uint4 *vd = v_cache + slot * row16;
+        for (int64_t c0 = threadIdx.x; c0 < row16; c0 += kU * blockDim.x) {
+            uint4 a[kU], b[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t c = c0 + u * blockDim.x;
+                if (c < row16) {
+                    a[u] = __ldg(ks + c);
+                    b[u] = __ldg(vs + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t c = c0 + u * blockDim.x;
+                if (c < row16) {
+                    kd[c] = a[u];
+                    vd[c] = b[u];
+                }
+            }
         }
     }
 }
@@ -135,12 +153,10 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
                                      int *err_flag, cudaStream_t stream) {
     const int64_t row16 = row_bytes / 16;
     const int threads = 128;
-    const int64_t slices = (row16 + threads - 1) / threads;
-    // About 32 CTAs per SM in total; long token lists grid-stride.
-    const int64_t cap = (static_cast<int64_t>(sm_count()) * 32 + slices - 1) / slices;
+    // Up to 16 CTAs (tokens) per SM at a time; long token lists grid-stride.
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
     const int64_t gx = num_tokens < cap ? num_tokens : cap;
-    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(slices < 65535 ? slices : 65535));
-    reshape_and_cache_kernel<<<grid, threads, 0, stream>>>(
+    reshape_and_cache_kernel<<<static_cast<unsigned>(gx), threads, 0, stream>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
         num_slots, row16, err_flag);
