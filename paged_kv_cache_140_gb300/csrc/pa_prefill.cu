@@ -97,6 +97,17 @@ __device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Sh
     return __all_sync(0xffffffffu, wait_bar(bar, parity, sh, err_flag));
 }
 
+// One lane of the (converged) warp, the same one on every call.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -387,68 +398,84 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t q_addr = smem_addr(sQ);
-            const uint32_t k_addr = smem_addr(sK);
-            const uint32_t v_addr = smem_addr(sV);
-            const int nx[2] = {nA, nB};
-            bool ok = wait_bar(&sh.q_full, 0, sh, p.err_flag);
-            int k_ready = -1;                  // last K tile known to have landed
-            auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
-                const int kst = t % NK;
-                if (k_ready < t) {
-                    if (!wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
-                    k_ready = t;
-                }
-                umma::fence_after_sync();
-                const uint32_t kt = k_addr + static_cast<uint32_t>(kst * kOp);
-                const uint32_t qx = q_addr + static_cast<uint32_t>(xx * kOp);
+        // The whole warp runs this loop in uniform control flow, so the
+        // descriptors (ring bases built once, k-step offsets as immediates)
+        // stay warp-uniform; one elected lane issues each MMA and commit.
+        const bool leader = elect_one();
+        const uint64_t qd0 = umma::desc_sw128(smem_addr(sQ), 16, 1024);
+        const uint64_t kd0 = umma::desc_sw128(smem_addr(sK), 16, 1024);
+        const uint64_t vd0 = umma::desc_sw128(smem_addr(sV), kRegion, 1024);
+        constexpr uint32_t kOpDesc = kOp >> 4;
+        const int nx[2] = {nA, nB};
+        bool ok = warp_wait_bar(&sh.q_full, 0, sh, p.err_flag);
+        int k_ready = -1;                      // last K tile known to have landed
+        auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
+            const int kst = t % NK;
+            if (k_ready < t) {
+                if (!warp_wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                k_ready = t;
+            }
+            umma::fence_after_sync();
+            const uint64_t qd = qd0 + static_cast<uint32_t>(xx) * kOpDesc;
+            const uint64_t kd = kd0 + static_cast<uint32_t>(kst) * kOpDesc;
+            const uint32_t ts = tmem + kColS + 128u * xx;
+            if (leader) {
 #pragma unroll
                 for (int k = 0; k < kKSteps; ++k) {
-                    const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-                    umma::mma_ss(tmem + kColS + 128u * xx, umma::desc_sw128(qx + off, 16, 1024),
-                                 umma::desc_sw128(kt + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+                    constexpr uint32_t kRegDesc = kRegion >> 4;
+                    const uint32_t off = (k >> 2) * kRegDesc + (k & 3) * 2;
+                    umma::mma_ss(ts, qd + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
                 }
                 umma::commit(smem_addr(&sh.s_full[xx]));
-                return true;
-            };
-            if (ok) ok = qk(0, 0);
-            if (ok && hasB) ok = qk(1, 0);
-            if (ok) umma::commit(smem_addr(&sh.k_empty[0]));
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int vst = j % NV;
-                const bool last = j == n_tiles - 1;
-                // On the last tile the zeroing of stale V rows (done by the
-                // softmax of the tile that reaches furthest) precedes every PV.
-                if (last && hasB && nA == n_tiles && !wait_bar(&sh.p_full[1], j & 1, sh, p.err_flag)) {
-                    ok = false;
-                    break;
-                }
-                if (!wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-                for (int xx = 0; ok && xx < 2; ++xx) {
-                    if (j >= nx[xx]) continue;
-                    if (!wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) { ok = false; break; }
-                    umma::fence_after_sync();
-                    const uint32_t vt = v_addr + static_cast<uint32_t>(vst * kOp);
-                    const uint32_t tP = tmem + kColS + 128u * xx;
-                    const uint32_t tO = tmem + kColO + 128u * xx;
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok) ok = qk(0, 0);
+        if (ok && hasB) ok = qk(1, 0);
+        if (ok && leader) umma::commit(smem_addr(&sh.k_empty[0]));
+        __syncwarp();
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            const int vst = j % NV;
+            const bool last = j == n_tiles - 1;
+            // On the last tile the zeroing of stale V rows (done by the
+            // softmax of the tile that reaches furthest) precedes every PV.
+            if (last && hasB && nA == n_tiles && !warp_wait_bar(&sh.p_full[1], j & 1, sh, p.err_flag)) {
+                ok = false;
+                break;
+            }
+            if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
+            const uint64_t vd = vd0 + static_cast<uint32_t>(vst) * kOpDesc;
+            for (int xx = 0; ok && xx < 2; ++xx) {
+                if (j >= nx[xx]) continue;
+                if (!warp_wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) { ok = false; break; }
+                umma::fence_after_sync();
+                const uint32_t tP = tmem + kColS + 128u * xx;
+                const uint32_t tO = tmem + kColO + 128u * xx;
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
+                if (leader) {
 #pragma unroll
                     for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1),
-                                     umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV,
-                                     (j > 0 || k > 0) ? 1u : 0u);
+                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1), vd + static_cast<uint32_t>(k * (2048 >> 4)),
+                                     kIdescPV, k > 0 ? 1u : acc0);
                     if constexpr (BF16) {
 #pragma unroll
                         for (int k = 0; k < kPVSteps; ++k)
                             umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
-                                         umma::desc_sw128(vt + k * 2048, kRegion, 1024), kIdescPV, 1u);
+                                         vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV, 1u);
                     }
-                    if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
                 }
-                if (!ok) break;
+                __syncwarp();
+                if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
+            }
+            if (!ok) break;
+            if (leader) {
                 umma::commit(smem_addr(&sh.v_empty[vst]));
                 if (j + 1 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 1) % NK]));
             }
+            __syncwarp();
+        }
+        if (leader) {
             umma::commit(smem_addr(&sh.done));
             mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
         }
