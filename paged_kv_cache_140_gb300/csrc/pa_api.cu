@@ -443,20 +443,22 @@ PA_EXPORT pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *
 
 namespace {
 
-// Tensor map over a dense 3-D array [d2][d1][d0] of 16-bit elements with a
-// (64, box1, box2) box and 128-byte swizzle.
-bool encode_map_16(CUtensorMap *map, const void *ptr, int64_t d0, int64_t d1, int64_t d2, int box1,
-                   int box2) {
+// Tensor map over a dense 3-D array [d2][d1][d0] of `es`-byte elements with
+// a (128 / es, box1, box2) box (128 bytes wide) and 128-byte swizzle.
+bool encode_map_128b(CUtensorMap *map, const void *ptr, int es, int64_t d0, int64_t d1, int64_t d2, int box1,
+                     int box2) {
     EncodeTiledFn fn = encode_tiled();
     if (fn == nullptr) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1),
                                 static_cast<cuuint64_t>(d2)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d0) * 2, static_cast<cuuint64_t>(d0 * d1) * 2};
-    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d0) * es, static_cast<cuuint64_t>(d0 * d1) * es};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box1),
+                               static_cast<cuuint32_t>(box2)};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(map, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+              const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -498,10 +500,12 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     const size_t smem = pa::prefill_smem_bytes(head_dim);
     if (smem + 4096 > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
-    CUtensorMap tq, tk, tv;
-    if (!encode_map_16(&tq, query, head_dim, num_heads, num_tokens, G, tokens_per_tile) ||
-        !encode_map_16(&tk, k_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
-        !encode_map_16(&tv, v_cache, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size))
+    CUtensorMap tq, tk, tv, to;
+    const int out_es = out_dtype == PA_F32 ? 4 : 2;
+    if (!encode_map_128b(&tq, query, 2, head_dim, num_heads, num_tokens, G, tokens_per_tile) ||
+        !encode_map_128b(&tk, k_cache, 2, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
+        !encode_map_128b(&tv, v_cache, 2, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
+        !encode_map_128b(&to, out, out_es, head_dim, num_heads, num_tokens, G, tokens_per_tile))
         return PA_ERR_CUDA;
 
     pa::PrefillParams p{};
@@ -523,7 +527,7 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     p.pairs_per_seq = static_cast<int>((tiles + 1) / 2);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err_flag = err_flag;
-    cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tq, tk, tv, smem,
+    cudaError_t e = pa::launch_prefill(p, head_dim, kv_dtype == PA_BF16, tq, tk, tv, to, smem,
                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -66,6 +66,7 @@ struct Shared {
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
     uint64_t s_full[2], p_full[2];       // per query tile
     uint64_t done;
+    uint64_t staged[2];                  // per query tile: its output rows staged for the TMA store
     uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
     float red[2][2][2][kTile];           // [use parity][query tile][column half][row]
     uint32_t tmem_base;
@@ -179,6 +180,43 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
+// 3-D tiled TMA store of one box from shared memory; completion is tracked
+// with the bulk-group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_wait_read() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// One 32-column chunk (columns col0 .. col0 + 31) of output row `row` into a
+// staging tile laid out as the output tensor map's boxes: 128-byte-wide
+// regions of 128 rows, 128-byte swizzle.
+__device__ __forceinline__ void stage_chunk(uint8_t *stage, int out_dtype, int row, int col0, const float (&v)[32]) {
+    if (out_dtype == PA_F32) {
+        uint8_t *rowp = stage + (col0 / 32) * kRegion + row * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4 *>(rowp + ((u ^ (row & 7)) << 4)) =
+                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    } else {
+        uint8_t *rowp = stage + (col0 / 64) * kRegion + row * 128;
+        const int k0 = (col0 % 64) / 8;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                w[k] = out_dtype == PA_BF16 ? pack2<true>(v[8 * u + 2 * k], v[8 * u + 2 * k + 1])
+                                            : pack2<false>(v[8 * u + 2 * k], v[8 * u + 2 * k + 1]);
+            *reinterpret_cast<uint4 *>(rowp + (((k0 + u) ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
 // One 32-column chunk of an output row -> global memory (out_dtype).
 __device__ __forceinline__ void store_chunk(void *out, int out_dtype, int64_t elem_off,
                                             const float (&v)[32]) {
@@ -260,7 +298,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     paged_prefill_kernel(const __grid_constant__ PrefillParams p,
                          const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
-                         const __grid_constant__ CUtensorMap tv) {
+                         const __grid_constant__ CUtensorMap tv,
+                         const __grid_constant__ CUtensorMap to) {
     constexpr int R = D / 64;               // 128-byte regions per row
     constexpr int kOp = R * kRegion;        // one 128-row operand tile
     constexpr int NK = Rings<D>::K, NV = Rings<D>::V;
@@ -346,6 +385,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][y][q], 64);
         }
         mbar_init(&sh.done, 1);
+        mbar_init(&sh.staged[0], 256);
+        mbar_init(&sh.staged[1], 256);
         sh.abort = 0;
         sh.bad = 0;
         fence_barrier_init();
@@ -608,15 +649,35 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const float l = l_run + l_other;
             const bool zero = *reinterpret_cast<volatile int *>(&sh.bad) != 0;
             const float inv = (l > 0.f && !zero && have) ? 1.f / l : 0.f;
+            // A full query tile (all its rows belong to this sequence) is staged in
+            // shared memory, idle now that every MMA is done (K ring for tile A,
+            // V ring for tile B), and written by TMA stores; a partial tile is
+            // written row by row so that no other sequence's rows are touched.
+            const bool full_tile = ntokx == TT;
+            uint8_t *stage = x == 0 ? sK : sV;
 #pragma unroll
             for (int c = 0; c < kHalfD / 32; ++c) {
                 uint32_t o[32];
                 umma::ld_32x32b_x32(tO + 32 * c, o);
                 umma::wait_ld();
-                float v[32];
+                float ov[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : __uint_as_float(o[i]) * inv;
-                if (qpos >= 0) store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, v);
+                for (int i = 0; i < 32; ++i) ov[i] = zero ? 0.f : __uint_as_float(o[i]) * inv;
+                if (full_tile)
+                    stage_chunk(stage, p.out_dtype, row, kHalfD * h + 32 * c, ov);
+                else if (qpos >= 0)
+                    store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, ov);
+            }
+            if (full_tile) {
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.staged[x]);
+                if (warp == 8 * x && lane == 0 && mbar_wait_bounded(&sh.staged[x], 0, kWaitLimitNs)) {
+                    const int es = p.out_dtype == PA_F32 ? 4 : 2;
+                    const int regions = D * es / 128;
+                    for (int r = 0; r < regions; ++r)
+                        tma_store_3d(&to, stage + r * kRegion, r * (128 / es), kvh * G, q0 + t0x);
+                    tma_store_commit_and_wait_read();
+                }
             }
         }
     }
@@ -631,13 +692,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
 template <int D, bool BF16>
 cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                     size_t smem, cudaStream_t stream) {
+                     const CUtensorMap &to, size_t smem, cudaStream_t stream) {
     auto kern = paged_prefill_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.pairs_per_seq;
-    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tq, tk, tv);
+    kern<<<static_cast<unsigned>(grid), kPrefillThreads, smem, stream>>>(p, tq, tk, tv, to);
     return cudaGetLastError();
 }
 
@@ -650,13 +711,14 @@ size_t prefill_smem_bytes(int head_dim) {
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
-                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem, cudaStream_t stream) {
+                           const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to, size_t smem,
+                           cudaStream_t stream) {
     if (head_dim == 128)
-        return bf16 ? launch_t<128, true>(p, tq, tk, tv, smem, stream)
-                    : launch_t<128, false>(p, tq, tk, tv, smem, stream);
+        return bf16 ? launch_t<128, true>(p, tq, tk, tv, to, smem, stream)
+                    : launch_t<128, false>(p, tq, tk, tv, to, smem, stream);
     if (head_dim == 64)
-        return bf16 ? launch_t<64, true>(p, tq, tk, tv, smem, stream)
-                    : launch_t<64, false>(p, tq, tk, tv, smem, stream);
+        return bf16 ? launch_t<64, true>(p, tq, tk, tv, to, smem, stream)
+                    : launch_t<64, false>(p, tq, tk, tv, to, smem, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -37,8 +37,11 @@ struct PrefillParams {
 size_t prefill_smem_bytes(int head_dim);
 
 // query [num_tokens, Hq, D] through `tq` (box 64 x G x 128/G); caches
-// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); 128-byte swizzle.
+// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); the output through
+// `to` (box 128 bytes x G x 128/G, written by full query tiles); all with
+// 128-byte swizzle.
 cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
-                           const CUtensorMap &tk, const CUtensorMap &tv, size_t smem, cudaStream_t stream);
+                           const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to, size_t smem,
+                           cudaStream_t stream);
 
 }  // namespace pa
