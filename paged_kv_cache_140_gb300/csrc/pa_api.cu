@@ -503,10 +503,8 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     CUtensorMap tq, tk, tv, to;
     const int out_es = out_dtype == PA_F32 ? 4 : 2;
     if (!encode_map_128b(&tq, query, 2, head_dim, num_heads, num_tokens, G, tokens_per_tile) ||
-        !encode_map_128b(&tk, k_cache, 2, head_dim, num_kv_heads, num_blocks * block_size, 1,
-                         std::min(block_size, pa::kPrefillKV)) ||
-        !encode_map_128b(&tv, v_cache, 2, head_dim, num_kv_heads, num_blocks * block_size, 1,
-                         std::min(block_size, pa::kPrefillKV)) ||
+        !encode_map_128b(&tk, k_cache, 2, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
+        !encode_map_128b(&tv, v_cache, 2, head_dim, num_kv_heads, num_blocks * block_size, 1, block_size) ||
         !encode_map_128b(&to, out, out_es, head_dim, num_heads, num_tokens, G, tokens_per_tile))
         return PA_ERR_CUDA;
 

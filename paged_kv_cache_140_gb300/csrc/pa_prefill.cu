@@ -9,35 +9,32 @@
 //
 // A query tile is 128 rows of one (sequence, KV head): 128/G tokens times the
 // G query heads that share the KV head.  One CTA runs two consecutive query
-// tiles, X = A and B, against every 64-token K/V tile it loads, so each K/V
-// byte brought into shared memory feeds 256 query rows.  Per K/V tile j and
-// query tile X:
-//   S_X(j) = Q_X K_j^T   tcgen05.mma, Q and K tiles in shared memory (TMA,
-//                        128-byte swizzle), S in tensor memory, two buffers
-//                        per query tile;
-//   softmax              eight warps per query tile, two threads per row (32
-//                        columns each, the row max traded through shared
-//                        memory); running max and sum in registers, the output
-//                        rescaled only when the max grows by more than 2^8; the
-//                        weights P written as 16-bit pairs over the S columns
-//                        they came from;
-//   O_X += P_X(j) V_j    tcgen05.mma with P read from tensor memory and V
-//                        (MN-major) from shared memory, O in tensor memory.
-// The MMA stream runs ... PV_A(j), QK_A(j+2), PV_B(j), QK_B(j+2) ...: tcgen05
-// operations of one thread execute in issue order, so QK_X(j+2) overwrites
-// the buffer of P_X(j) only after PV_X(j) has read it, and S_X(j+1) is
-// already computed when the softmax of tile j finishes - a query tile's
-// softmax never waits for its own PV.  bfloat16 weights carry only 8
+// tiles, X = A and B, against every 128-token K/V tile it loads, so each K/V
+// byte brought into shared memory feeds 256 query rows (the SM's intake of
+// K/V, not the tensor cores, is what a single tile would be limited by).
+// Per K/V tile j and query tile X:
+//   S_X = Q_X K_j^T   tcgen05.mma, Q and K tiles in shared memory (TMA,
+//                     128-byte swizzle), S in tensor memory;
+//   softmax           eight warps per query tile, two threads per row (64
+//                     columns each, the row max traded through shared memory);
+//                     running max and sum in registers, the output rescaled
+//                     only when the max grows by more than 2^8; the weights P
+//                     written as 16-bit pairs over the S columns they came from;
+//   O_X += P_X V_j    tcgen05.mma with P read from tensor memory and V
+//                     (MN-major) from shared memory, O in tensor memory.
+// The MMA stream runs ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...; tcgen05
+// operations of one thread execute in issue order, so QK_X(j+1) overwrites
+// S_X only after PV_X(j) has read P_X from it, and when the softmax of tile
+// j+1 starts, O_X already holds tile j.  bfloat16 weights carry only 8
 // significant bits, so for bf16 inputs P is split into P_hi + P_lo (both
 // bf16, P_lo = P - P_hi) and PV runs twice; binary16 weights are used as is.
 //
 // Warp roles: warps 0-15 run the softmax and the epilogue (warp w: query tile
 // w / 8, column half (w / 4) % 2, TMEM lanes 32 (w % 4)..); warp 16 loads the
 // query tiles and the K tiles, warp 18 the V tiles (both read the block table
-// 32 entries at a time); warp 17 owns the tensor memory and runs the MMA
-// issue loop, one elected lane issuing.  Every mbarrier wait is bounded
-// (2 s); a timeout sets PA_FLAG_TIMEOUT and the CTA winds down without
-// further MMAs.
+// 32 entries at a time); warp 17 owns the tensor memory and one of its lanes
+// issues every MMA.  Every mbarrier wait is bounded (2 s); a timeout sets
+// PA_FLAG_TIMEOUT and the CTA winds down without further MMAs.
 #include <math_constants.h>
 
 #include "pa.h"
@@ -48,31 +45,27 @@
 namespace pa {
 namespace {
 
-constexpr int kTile = kPrefillTile;      // query rows per query tile
-constexpr int kKV = kPrefillKV;          // keys per K/V tile
-constexpr int kRegionQ = kTile * 128;    // 128 rows x 128 bytes: one swizzled query (or staging) region
-constexpr int kRegion = kRegionQ;        // staging regions share the query-region shape
-constexpr int kRegionKV = kKV * 128;     // 64 rows x 128 bytes: one swizzled K or V region
+constexpr int kTile = kPrefillTile;
+constexpr int kRegion = kTile * 128;     // 128 rows x 128 bytes: one swizzled operand region
 constexpr uint32_t kTmemCols = 512;
-// Tensor memory: S/P buffer b of query tile X at columns 64 (2 X + b), O of X
-// at 256 + 128 X.  P of a 32-key chunk sits in that chunk's own S columns:
-// 16 columns of hi pairs, then (bf16) 16 columns of lo pairs.
+// Tensor memory: S/P of query tile X at columns 128 X, O of X at 256 + 128 X.
+// P of a 32-key chunk sits in that chunk's own S columns: 16 columns of hi
+// pairs, then (bf16) 16 columns of lo pairs.
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18;
-constexpr int kMaxRing = 8;
+constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// K and V ring depths (tiles of 64 tokens).
+// K and V ring depths (tiles of 128 tokens).
 template <int D> struct Rings;
-template <> struct Rings<128> { static constexpr int K = 4, V = 4; };
-template <> struct Rings<64> { static constexpr int K = 8, V = 8; };
+template <> struct Rings<128> { static constexpr int K = 2, V = 2; };
+template <> struct Rings<64> { static constexpr int K = 4, V = 4; };
 
 struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
-    uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];   // [query tile][S/P buffer]
+    uint64_t s_full[2], p_full[2];       // per query tile
     uint64_t done;
-    uint64_t zeroed;                     // once: stale V rows of the last K/V tile zeroed
     uint64_t staged[2];                  // per query tile: its output rows staged for the TMA store
     uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
     float red[2][2][2][kTile];           // [use parity][query tile][column half][row]
@@ -246,8 +239,8 @@ __device__ __forceinline__ void store_chunk(void *out, int out_dtype, int64_t el
 }
 
 // A loader warp's view of the block table: 32 consecutive entries, one per
-// lane, with the next 32 already requested (a tile never straddles two groups:
-// 64 / bs divides 32 for bs <= 64, and a larger block holds whole tiles).
+// lane, with the next 32 already requested (tiles never straddle two groups:
+// 128 / bs divides 32).
 struct TableWindow {
     const int32_t *table;
     int needed;          // entries that may be read: blocks holding positions <= qpos_max
@@ -260,7 +253,11 @@ struct TableWindow {
     __device__ int32_t id_for(int entry, int i, int lane) {
         const int b = entry & ~31;
         if (b != base) {
-            cur = (b == base + 32) ? nxt : fetch(b, lane);
+            if (b == base + 32) {
+                cur = nxt;
+            } else {
+                cur = fetch(b, lane);
+            }
             nxt = fetch(b + 32, lane);
             base = b;
         }
@@ -268,34 +265,31 @@ struct TableWindow {
     }
 };
 
-// Issue one 64-token K or V tile: boxes of min(bs, 64) rows, one per block it
-// covers, times the 64-column halves of the head.
+// Issue one 128-token K or V tile (8 blocks of 16 tokens for bs = 16, two
+// 64-column boxes each); returns false on an abort.
 template <int R>
 __device__ __forceinline__ void load_tile(TableWindow &win, int t, int bs, int qpos_max, int kvh, int64_t num_blocks,
                                           uint8_t *dst, const CUtensorMap *map, uint64_t *full, int lane,
                                           Shared &sh, int *err_flag) {
-    const int rpb = min(bs, kKV);                    // rows per box
-    const int first = t * kKV;
-    const int last = min(qpos_max, first + kKV - 1);
-    const int nbox = (last - first) / rpb + 1;
-    const int i = lane < nbox ? lane : 0;
-    const int32_t bid = win.id_for(first / bs, (i * rpb) / bs, lane);
-    const bool ok = lane < nbox && bid >= 0 && static_cast<int64_t>(bid) < num_blocks;
+    const int bpt = kTile / bs;
+    const int last = min(qpos_max, t * kTile + kTile - 1);
+    const int nb = (last - t * kTile) / bs + 1;
+    const int32_t bid = win.id_for(t * bpt, lane < nb ? lane : 0, lane);
+    const bool ok = lane < nb && bid >= 0 && static_cast<int64_t>(bid) < num_blocks;
     const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-    const unsigned want = (nbox >= 32) ? 0xffffffffu : ((1u << nbox) - 1u);
+    const unsigned want = (nb >= 32) ? 0xffffffffu : ((1u << nb) - 1u);
     if (lane == 0) {
         if (okmask != want) {
             report(err_flag, PA_FLAG_BAD_BLOCK_ID);
             sh.bad = 1;
         }
-        mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(okmask)) * rpb * 128u * R);
+        mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(okmask)) * bs * 128u * R);
     }
     __syncwarp();
     if (ok) {
-        const int z = bid * bs + (first + i * rpb) % bs;
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            tma_load_3d_plain(dst + r * kRegionKV + i * rpb * 128, map, full, r * 64, kvh, z);
+            tma_load_3d_plain(dst + r * kRegion + lane * bs * 128, map, full, r * 64, kvh, bid * bs);
     }
 }
 
@@ -307,13 +301,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                          const __grid_constant__ CUtensorMap tv,
                          const __grid_constant__ CUtensorMap to) {
     constexpr int R = D / 64;               // 128-byte regions per row
-    constexpr int kOpQ = R * kRegionQ;      // one 128-row query tile
-    constexpr int kOpKV = R * kRegionKV;    // one 64-row K or V tile
+    constexpr int kOp = R * kRegion;        // one 128-row operand tile
     constexpr int NK = Rings<D>::K, NV = Rings<D>::V;
     constexpr int kKSteps = D / 16;         // QK MMAs per tile (K = 16 each)
-    constexpr int kPVSteps = kKV / 16;      // PV MMAs per tile and weight part
+    constexpr int kPVSteps = kTile / 16;    // PV MMAs per tile and weight part
     constexpr int kHalfD = D / 2;           // O columns per softmax thread
-    constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kKV, false);
+    constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kTile, false);
     constexpr uint32_t kIdescPV = umma::idesc_f16(BF16, kTile, D, true);
 
     __shared__ Shared sh;
@@ -321,8 +314,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = base;                     // query tiles A, B
-    uint8_t *sK = sQ + 2 * kOpQ;            // K ring: NK tiles
-    uint8_t *sV = sK + NK * kOpKV;          // V ring: NV tiles
+    uint8_t *sK = sQ + 2 * kOp;             // K ring: NK tiles
+    uint8_t *sV = sK + NK * kOp;            // V ring: NV tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -350,7 +343,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int ctx = __ldg(p.context_lens + s);
 
     // Softmax threads: query tile x, row `row` (token rtok, head kvh * G + row % G),
-    // keys [32 h, 32 h + 32) of each K/V tile, O columns [D/2 h, D/2 h + D/2).
+    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O.
     const int x = (warp >> 3) & 1, q4 = warp & 3, h = (warp >> 2) & 1;
     const int row = 32 * q4 + lane;
     const int rtok = row >> lg;
@@ -372,14 +365,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         return;
     }
     const int qstartA = ctx - ql + t0A;     // position of tile A's first query token
-    const int nA = (qstartA + min(TT, ql - t0A) - 1) / kKV + 1;
+    const int nA = (qstartA + min(TT, ql - t0A) - 1) / kTile + 1;
     const int qpos_max = qstartA + (hasB ? TT + min(TT, ql - t0A - TT) : min(TT, ql - t0A)) - 1;
-    const int nB = hasB ? qpos_max / kKV + 1 : 0;
+    const int nB = hasB ? qpos_max / kTile + 1 : 0;
     const int n_tiles = hasB ? nB : nA;     // K/V tiles loaded (nB >= nA)
-    // The last K/V tile reaches past the last attended position: its stale or
-    // unloaded V rows are zeroed (by the query tile that reaches furthest)
-    // before any PV reads it, so that 0-weights cannot meet NaNs.
-    const bool zero_tail = n_tiles * kKV - 1 > qpos_max;
 
     if (threadIdx.x == 0) {
         mbar_init(&sh.q_full, 1);
@@ -390,17 +379,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_init(&sh.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(&sh.s_full[i][b], 1);
-                mbar_init(&sh.p_full[i][b], 256);
-                mbar_init(&sh.pv_done[i][b], 1);
-            }
+            mbar_init(&sh.s_full[i], 1);
+            mbar_init(&sh.p_full[i], 256);
             for (int y = 0; y < 2; ++y)
                 for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][y][q], 64);
-            mbar_init(&sh.staged[i], 256);
         }
         mbar_init(&sh.done, 1);
-        mbar_init(&sh.zeroed, 256);
+        mbar_init(&sh.staged[0], 256);
+        mbar_init(&sh.staged[1], 256);
         sh.abort = 0;
         sh.bad = 0;
         fence_barrier_init();
@@ -426,12 +412,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             prefetch_tensormap(map);
             if (is_k) {
                 prefetch_tensormap(&tq);
-                mbar_arrive_expect_tx(&sh.q_full, kOpQ * (hasB ? 2 : 1));
+                mbar_arrive_expect_tx(&sh.q_full, kOp * (hasB ? 2 : 1));
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    tma_load_3d_plain(sQ + r * kRegionQ, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A);
+                    tma_load_3d_plain(sQ + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A);
                     if (hasB)
-                        tma_load_3d_plain(sQ + kOpQ + r * kRegionQ, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A + TT);
+                        tma_load_3d_plain(sQ + kOp + r * kRegion, &tq, &sh.q_full, r * 64, kvh * G, q0 + t0A + TT);
                 }
             }
         }
@@ -441,7 +427,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t % NR;
             if (t >= NR && !warp_wait_bar(&empty[st], ((t / NR) - 1) & 1, sh, p.err_flag)) break;
-            load_tile<R>(win, t, p.block_size, qpos_max, kvh, p.num_blocks, ring + st * kOpKV, map, &full[st], lane,
+            load_tile<R>(win, t, p.block_size, qpos_max, kvh, p.num_blocks, ring + st * kOp, map, &full[st], lane,
                          sh, p.err_flag);
             ++issued;
         }
@@ -454,80 +440,79 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
         // The whole warp runs this loop in uniform control flow, so the
-        // descriptors (bases built once, k-step offsets as immediates) stay
-        // warp-uniform; one elected lane issues each MMA and commit.
+        // descriptors (ring bases built once, k-step offsets as immediates)
+        // stay warp-uniform; one elected lane issues each MMA and commit.
         const bool leader = elect_one();
         const uint64_t qd0 = umma::desc_sw128(smem_addr(sQ), 16, 1024);
         const uint64_t kd0 = umma::desc_sw128(smem_addr(sK), 16, 1024);
-        const uint64_t vd0 = umma::desc_sw128(smem_addr(sV), kRegionKV, 1024);
+        const uint64_t vd0 = umma::desc_sw128(smem_addr(sV), kRegion, 1024);
+        constexpr uint32_t kOpDesc = kOp >> 4;
         const int nx[2] = {nA, nB};
         bool ok = warp_wait_bar(&sh.q_full, 0, sh, p.err_flag);
         int k_ready = -1;                      // last K tile known to have landed
-        auto qk = [&](int xx, int t) -> bool {  // S_xx(t) = Q_xx K_t^T into buffer t % 2
+        auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
             const int kst = t % NK;
             if (k_ready < t) {
                 if (!warp_wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
                 k_ready = t;
             }
             umma::fence_after_sync();
-            const uint64_t qd = qd0 + static_cast<uint32_t>(xx) * static_cast<uint32_t>(kOpQ >> 4);
-            const uint64_t kd = kd0 + static_cast<uint32_t>(kst) * static_cast<uint32_t>(kOpKV >> 4);
-            const uint32_t ts = tmem + kColS + 64u * (2 * xx + (t & 1));
+            const uint64_t qd = qd0 + static_cast<uint32_t>(xx) * kOpDesc;
+            const uint64_t kd = kd0 + static_cast<uint32_t>(kst) * kOpDesc;
+            const uint32_t ts = tmem + kColS + 128u * xx;
             if (leader) {
 #pragma unroll
-                for (int k = 0; k < kKSteps; ++k)
-                    umma::mma_ss(ts, qd + static_cast<uint32_t>((k >> 2) * (kRegionQ >> 4) + (k & 3) * 2),
-                                 kd + static_cast<uint32_t>((k >> 2) * (kRegionKV >> 4) + (k & 3) * 2), kIdescQK,
-                                 k > 0 ? 1u : 0u);
-                umma::commit(smem_addr(&sh.s_full[xx][t & 1]));
+                for (int k = 0; k < kKSteps; ++k) {
+                    constexpr uint32_t kRegDesc = kRegion >> 4;
+                    const uint32_t off = (k >> 2) * kRegDesc + (k & 3) * 2;
+                    umma::mma_ss(ts, qd + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
+                }
+                umma::commit(smem_addr(&sh.s_full[xx]));
             }
             __syncwarp();
             return true;
         };
-        // S for the first two K/V tiles of both query tiles.
-        for (int t = 0; ok && t < 2 && t < n_tiles; ++t) {
-            for (int xx = 0; ok && xx < 2; ++xx)
-                if (t < nx[xx]) ok = qk(xx, t);
-            if (ok && leader) umma::commit(smem_addr(&sh.k_empty[t % NK]));
-            __syncwarp();
-        }
+        if (ok) ok = qk(0, 0);
+        if (ok && hasB) ok = qk(1, 0);
+        if (ok && leader) umma::commit(smem_addr(&sh.k_empty[0]));
+        __syncwarp();
         for (int j = 0; ok && j < n_tiles; ++j) {
             const int vst = j % NV;
-            if (zero_tail && j == n_tiles - 1 && !warp_wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
+            const bool last = j == n_tiles - 1;
+            // On the last tile the zeroing of stale V rows (done by the
+            // softmax of the tile that reaches furthest) precedes every PV.
+            if (last && hasB && nA == n_tiles && !warp_wait_bar(&sh.p_full[1], j & 1, sh, p.err_flag)) {
                 ok = false;
                 break;
             }
             if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-            const uint64_t vd = vd0 + static_cast<uint32_t>(vst) * static_cast<uint32_t>(kOpKV >> 4);
+            const uint64_t vd = vd0 + static_cast<uint32_t>(vst) * kOpDesc;
             for (int xx = 0; ok && xx < 2; ++xx) {
                 if (j >= nx[xx]) continue;
-                const int b = j & 1;
-                if (!warp_wait_bar(&sh.p_full[xx][b], (j >> 1) & 1, sh, p.err_flag)) { ok = false; break; }
+                if (!warp_wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) { ok = false; break; }
                 umma::fence_after_sync();
-                const uint32_t tP = tmem + kColS + 64u * (2 * xx + b);
+                const uint32_t tP = tmem + kColS + 128u * xx;
                 const uint32_t tO = tmem + kColO + 128u * xx;
                 const uint32_t acc0 = j > 0 ? 1u : 0u;
                 if (leader) {
 #pragma unroll
                     for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1),
-                                     vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV, k > 0 ? 1u : acc0);
+                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1), vd + static_cast<uint32_t>(k * (2048 >> 4)),
+                                     kIdescPV, k > 0 ? 1u : acc0);
                     if constexpr (BF16) {
 #pragma unroll
                         for (int k = 0; k < kPVSteps; ++k)
                             umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
                                          vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV, 1u);
                     }
-                    umma::commit(smem_addr(&sh.pv_done[xx][b]));
                 }
                 __syncwarp();
-                // S_xx(j+2) into the buffer P_xx(j) just left, right behind PV_xx(j)
-                if (j + 2 < nx[xx]) ok = qk(xx, j + 2);
+                if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
             }
             if (!ok) break;
             if (leader) {
                 umma::commit(smem_addr(&sh.v_empty[vst]));
-                if (j + 2 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 2) % NK]));
+                if (j + 1 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 1) % NK]));
             }
             __syncwarp();
         }
@@ -541,51 +526,50 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int nx = x == 0 ? nA : nB;
         const int qpos = rtok < ntokx ? qstartA + x * TT + rtok : -1;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const uint32_t tS = tmem + kColS + 128u * x + lane_off + 64u * h;
         const uint32_t tO = tmem + kColO + 128u * x + lane_off + kHalfD * h;
-        const bool zeroer = zero_tail && x == (hasB ? 1 : 0);
+        // The tile that reaches furthest zeroes the stale V rows of the last K/V tile.
+        const bool zeroer = x == (hasB ? 1 : 0) && n_tiles * kTile - 1 > qpos_max;
         const float sl = p.scale_log2;
         const uint64_t sl2 = f2(sl, sl);
         float m_run = -CUDART_INF_F;
         float l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < nx; ++j) {
-            const int b = j & 1;
-            if (!warp_wait_bar(&sh.s_full[x][b], (j >> 1) & 1, sh, p.err_flag)) { ok = false; break; }
+            if (!warp_wait_bar(&sh.s_full[x], j & 1, sh, p.err_flag)) { ok = false; break; }
             umma::fence_after_sync();
-            const uint32_t tS = tmem + kColS + 64u * (2 * x + b) + lane_off + 32u * h;
-            uint32_t v[32];
-            umma::ld_32x32b_x32(tS, v);
-            umma::wait_ld();
-            const int lim = qpos - j * kKV - 32 * h;    // keys c <= lim are attended
-            if (!__all_sync(0xffffffffu, lim >= 31)) {
+            const int lim = qpos - j * kTile - 64 * h;   // columns c <= lim are attended
+            const bool masked = !__all_sync(0xffffffffu, lim >= 63);
+            float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i > lim) v[i] = 0xff800000u;     // -inf
-            }
-            float a0 = -CUDART_INF_F, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                umma::ld_32x32b_x32(tS + 32 * c, v);
+                umma::wait_ld();
+                if (masked) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a0 = max3(a0, __uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
-                a1 = max3(a1, __uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
-                a2 = max3(a2, __uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
-                a3 = max3(a3, __uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i > lim) v[i] = 0xff800000u;     // -inf
+                }
+                float a0 = mx, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    a0 = max3(a0, __uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
+                    a1 = max3(a1, __uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+                    a2 = max3(a2, __uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+                    a3 = max3(a3, __uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+                }
+                mx = max3(a0, a1, fmaxf(a2, a3));
             }
-            float mx = max3(a0, a1, fmaxf(a2, a3));
             float mx_other;
             if (!pair_exchange(sh, j, x, q4, h, row, mx, mx_other, p.err_flag)) { ok = false; break; }
             mx = fmaxf(mx, mx_other);
             const float x_tile = mx * sl;
             const bool need = x_tile > m_run + 8.f;
             if (__any_sync(0xffffffffu, need)) {
+                // O_x already holds tile j-1: PV(j-1) preceded QK(j) in the MMA stream.
                 const float f = need ? fast_exp2(m_run - x_tile) : 1.f;
                 if (j > 0) {
-                    // O_x must hold tile j-1 before it is rescaled: wait for PV(j-1)
-                    // (PV(j-2) completed before S(j) was issued).
-                    if (!warp_wait_bar(&sh.pv_done[x][(j - 1) & 1], ((j - 1) >> 1) & 1, sh, p.err_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    umma::fence_after_sync();
                     const uint64_t f2x = f2(f, f);
 #pragma unroll
                     for (int c = 0; c < kHalfD / 32; ++c) {
@@ -594,9 +578,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                         umma::wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float2 ov = unf2(mul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2x));
-                            o[2 * i] = __float_as_uint(ov.x);
-                            o[2 * i + 1] = __float_as_uint(ov.y);
+                            const float2 v = unf2(mul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2x));
+                            o[2 * i] = __float_as_uint(v.x);
+                            o[2 * i + 1] = __float_as_uint(v.y);
                         }
                         st_32x32b_x32(tO + 32 * c, o);
                     }
@@ -606,43 +590,56 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     m_run = x_tile;
                 }
             }
-            // weights p = 2^(s * scale_log2 - m) as 16-bit pairs over this chunk's S columns
+            // weights p = 2^(s * scale_log2 - m) as 16-bit pairs, each 32-key
+            // chunk written over its own S columns
             const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
             const uint64_t nm2 = f2(-mref, -mref);
             uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
-            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float2 xv = unf2(fma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2, nm2));
-                const float p0 = fast_exp2(xv.x), p1 = fast_exp2(xv.y);
-                hi[i] = pack2<BF16>(p0, p1);
-                const float2 hv = Half2x<BF16>::to_float2(hi[i]);
-                if constexpr (BF16) {
-                    const float2 lv = unf2(sub2(f2(p0, p1), f2(hv.x, hv.y)));
-                    lo[i] = pack2<true>(lv.x, lv.y);
-                    if (i & 1) acc1 = add2(acc1, f2(p0, p1)); else acc0 = add2(acc0, f2(p0, p1));
-                } else {
-                    if (i & 1) acc1 = add2(acc1, f2(hv.x, hv.y)); else acc0 = add2(acc0, f2(hv.x, hv.y));
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                umma::ld_32x32b_x32(tS + 32 * c, v);
+                umma::wait_ld();
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i > lim) v[i] = 0xff800000u;
                 }
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float2 xv = unf2(fma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2, nm2));
+                    const float p0 = fast_exp2(xv.x), p1 = fast_exp2(xv.y);
+                    hi[i] = pack2<BF16>(p0, p1);
+                    const float2 hv = Half2x<BF16>::to_float2(hi[i]);
+                    if constexpr (BF16) {
+                        const float2 lv = unf2(sub2(f2(p0, p1), f2(hv.x, hv.y)));
+                        lo[i] = pack2<true>(lv.x, lv.y);
+                        if (i & 1) acc1 = add2(acc1, f2(p0, p1)); else acc0 = add2(acc0, f2(p0, p1));
+                    } else {
+                        if (i & 1) acc1 = add2(acc1, f2(hv.x, hv.y)); else acc0 = add2(acc0, f2(hv.x, hv.y));
+                    }
+                }
+                umma::st_32x32b_x16(tS + 32 * c, hi);
+                if constexpr (BF16) umma::st_32x32b_x16(tS + 32 * c + 16, lo);
             }
-            umma::st_32x32b_x16(tS, hi);
-            if constexpr (BF16) umma::st_32x32b_x16(tS + 16, lo);
             const float2 acc = unf2(add2(acc0, acc1));
             l_run += acc.x + acc.y;
             if (zeroer && j == nx - 1) {
+                // V rows past the last attended position hold stale or unloaded
+                // data; zero them so that 0-weights cannot meet NaNs.
                 const int vst = j % NV;
                 if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-                if (row < kKV && j * kKV + row > qpos_max && (R > 1 || h == 0)) {
-                    uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOpKV + (R > 1 ? h : 0) * kRegionKV + row * 128);
+                if (j * kTile + row > qpos_max && (R > 1 || h == 0)) {
+                    uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + (R > 1 ? h : 0) * kRegion + row * 128);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&sh.zeroed);
             }
             umma::wait_st();
             umma::fence_before_sync();
-            mbar_arrive(&sh.p_full[x][b]);
+            mbar_arrive(&sh.p_full[x]);
         }
         // `done` completes once every MMA of the CTA (the last PV included) has.
         if (ok && warp_wait_bar(&sh.done, 0, sh, p.err_flag)) {
@@ -653,12 +650,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const bool zero = *reinterpret_cast<volatile int *>(&sh.bad) != 0;
             const float inv = (l > 0.f && !zero && have) ? 1.f / l : 0.f;
             // A full query tile (all its rows belong to this sequence) is staged in
-            // shared memory, idle now that every MMA is done (query tile A's
-            // region for A, query tile B's and then the K ring for B), and written
-            // by TMA stores; a partial tile is written row by row so that no
-            // other sequence's rows are touched.
+            // shared memory, idle now that every MMA is done (K ring for tile A,
+            // V ring for tile B), and written by TMA stores; a partial tile is
+            // written row by row so that no other sequence's rows are touched.
             const bool full_tile = ntokx == TT;
-            uint8_t *stage = x == 0 ? sQ : sQ + kOpQ;
+            uint8_t *stage = x == 0 ? sK : sV;
 #pragma unroll
             for (int c = 0; c < kHalfD / 32; ++c) {
                 uint32_t o[32];
@@ -668,8 +664,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ov[i] = zero ? 0.f : __uint_as_float(o[i]) * inv;
                 if (full_tile)
-                    stage_chunk(x == 0 || p.out_dtype != PA_F32 ? stage : sK, p.out_dtype, row,
-                                kHalfD * h + 32 * c, ov);
+                    stage_chunk(stage, p.out_dtype, row, kHalfD * h + 32 * c, ov);
                 else if (qpos >= 0)
                     store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, ov);
             }
@@ -679,9 +674,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 if (warp == 8 * x && lane == 0 && mbar_wait_bounded(&sh.staged[x], 0, kWaitLimitNs)) {
                     const int es = p.out_dtype == PA_F32 ? 4 : 2;
                     const int regions = D * es / 128;
-                    uint8_t *src = x == 0 || es == 2 ? stage : sK;
                     for (int r = 0; r < regions; ++r)
-                        tma_store_3d(&to, src + r * kRegion, r * (128 / es), kvh * G, q0 + t0x);
+                        tma_store_3d(&to, stage + r * kRegion, r * (128 / es), kvh * G, q0 + t0x);
                     tma_store_commit_and_wait_read();
                 }
             }
@@ -711,9 +705,9 @@ cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtens
 }  // namespace
 
 size_t prefill_smem_bytes(int head_dim) {
-    const size_t r = static_cast<size_t>(head_dim / 64);
+    const size_t op = static_cast<size_t>(head_dim / 64) * kRegion;
     const int rings = head_dim == 128 ? Rings<128>::K + Rings<128>::V : Rings<64>::K + Rings<64>::V;
-    return 1024 + 2 * r * kRegionQ + static_cast<size_t>(rings) * r * kRegionKV;
+    return 1024 + op * (2 + rings);
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,

@@ -9,8 +9,7 @@
 
 namespace pa {
 
-constexpr int kPrefillTile = 128;       // rows of a query tile
-constexpr int kPrefillKV = 64;          // K/V tokens per pipeline stage
+constexpr int kPrefillTile = 128;       // rows of a query tile = KV tokens per stage
 constexpr int kPrefillThreads = 608;    // 16 softmax warps, K/Q loader, MMA issuer, V loader
 
 struct PrefillParams {
@@ -38,7 +37,7 @@ struct PrefillParams {
 size_t prefill_smem_bytes(int head_dim);
 
 // query [num_tokens, Hq, D] through `tq` (box 64 x G x 128/G); caches
-// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x min(bs, 64)); the output through
+// [NB * bs, Hkv, D] through `tk` / `tv` (box 64 x 1 x bs); the output through
 // `to` (box 128 bytes x G x 128/G, written by full query tiles); all with
 // 128-byte swizzle.
 cudaError_t launch_prefill(const PrefillParams &p, int head_dim, bool bf16, const CUtensorMap &tq,
