@@ -327,6 +327,28 @@ pa_status pa_copy_blocks(void *k_cache, void *v_cache,
                          int head_dim, pa_dtype dtype, int *err_flag, void *stream);
 
 /*
+ * pa_copy_blocks_layers -- pa_copy_blocks for every layer of a model's cache
+ * in one launch.
+ *
+ * The per-model cache is one tensor [layers, 2, blocks, block_size, heads,
+ * head_dim] (Page C §2.2): layer l's K cache is kv_cache[l][0] and its V cache
+ * kv_cache[l][1].  A sequence's physical blocks are the same in every layer,
+ * so one (src, dst) pair list copies the block in all of them:
+ *     kv_cache[l][0][dst_p] = kv_cache[l][0][src_p],
+ *     kv_cache[l][1][dst_p] = kv_cache[l][1][src_p]   for every layer l,
+ * bit-exact; rules and device-side checks as for pa_copy_blocks.
+ *
+ *   kv_cache      : [num_layers, 2, num_blocks, block_size, num_kv_heads,
+ *                   head_dim] of `dtype` (F16, BF16 or FP8_E4M3), contiguous
+ *   block_mapping : [num_pairs, 2] int64 (src, dst), device memory
+ * num_layers == 0 or num_pairs == 0 is a no-op; at most 65535 layers.
+ */
+pa_status pa_copy_blocks_layers(void *kv_cache, int num_layers,
+                                const int64_t *block_mapping, int64_t num_pairs,
+                                int64_t num_blocks, int block_size, int num_kv_heads,
+                                int head_dim, pa_dtype dtype, int *err_flag, void *stream);
+
+/*
  * pa_swap_blocks -- copy whole blocks between two caches.
  *
  * Swap-mode preemption moves a preempted request's KV blocks from GPU memory

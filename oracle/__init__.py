@@ -116,6 +116,22 @@ def copy_blocks(k_cache, v_cache, block_mapping):
     return kc, vc, int(bad)
 
 
+def copy_blocks_layers(kv_cache, block_mapping):
+    """copy_blocks applied to every layer of a per-model cache
+    [layers, 2, NB, bs, Hkv, D] (layer l's K is [l][0], its V [l][1];
+    nano-vllm walkthrough §2.2), on a copy.  Elements of any size are moved
+    as 16-bit words."""
+    kv = np.array(kv_cache, copy=True, order="C")
+    L = kv.shape[0]
+    words = kv.view(np.uint16).reshape(L, 2, kv.shape[2], kv.shape[3], kv.shape[4], -1)
+    bad = 0
+    for layer in range(L):
+        k, v, b = copy_blocks(words[layer, 0], words[layer, 1], block_mapping)
+        words[layer, 0], words[layer, 1] = k, v
+        bad += b
+    return kv, bad
+
+
 def paged_attention(q, k_cache, v_cache, dtype: str, block_tables, context_lens, scale,
                     num_kv_heads: int | None = None) -> np.ndarray:
     """softmax(q K^T * scale) V over each sequence's paged context, in fp64.

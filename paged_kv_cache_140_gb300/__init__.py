@@ -23,7 +23,7 @@ from . import _lib
 from ._lib import (FLAG_BAD_BLOCK_ID, FLAG_BAD_CONTEXT_LEN, FLAG_BAD_COPY_PAIR, FLAG_BAD_SLOT,
                    FLAG_TIMEOUT, PA_BF16, PA_F16, PA_F32, PA_FP8_E4M3, PagedAttentionError)
 
-__all__ = ["reshape_and_cache", "decode", "decode_append", "prefill", "copy_blocks", "swap_blocks", "decode_workspace_size",
+__all__ = ["reshape_and_cache", "decode", "decode_append", "prefill", "copy_blocks", "copy_blocks_layers", "swap_blocks", "decode_workspace_size",
            "decode_partition_size", "DecodeWorkspace", "new_err_flag", "read_err_flag",
            "PagedAttentionError", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK_ID", "FLAG_BAD_CONTEXT_LEN",
            "FLAG_BAD_COPY_PAIR", "FLAG_TIMEOUT", "library_path"]
@@ -126,6 +126,22 @@ def copy_blocks(k_cache, v_cache, block_mapping, err_flag=None) -> None:
                                     block_mapping.shape[0], nb, bs, hkv, d, _cache_code(k_cache),
                                     _ptr(err_flag), _stream(k_cache.device))
     _lib.check(st, "pa_copy_blocks")
+
+
+def copy_blocks_layers(kv_cache, block_mapping, err_flag=None) -> None:
+    """copy_blocks for every layer of a model's cache
+    ``kv_cache`` [layers, 2, NB, bs, Hkv, D] (K at [l][0], V at [l][1]), one launch."""
+    for n, t in (("kv_cache", kv_cache), ("block_mapping", block_mapping)):
+        _cuda_contig(n, t)
+    torch = _torch()
+    _need(kv_cache.dim() == 6 and kv_cache.shape[1] == 2, "kv_cache must be [layers, 2, NB, bs, Hkv, D]")
+    _need(block_mapping.dtype == torch.int64 and block_mapping.dim() == 2 and block_mapping.shape[1] == 2,
+          "block_mapping must be int64 [P, 2]")
+    layers, _, nb, bs, hkv, d = kv_cache.shape
+    st = _lib.load().pa_copy_blocks_layers(_ptr(kv_cache), layers, _ptr(block_mapping), block_mapping.shape[0],
+                                           nb, bs, hkv, d, _cache_code(kv_cache), _ptr(err_flag),
+                                           _stream(kv_cache.device))
+    _lib.check(st, "pa_copy_blocks_layers")
 
 
 def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, err_flag=None) -> None:

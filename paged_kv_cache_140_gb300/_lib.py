@@ -35,6 +35,7 @@ SIGNATURES = {
     "pa_prefill": (_I, [_P, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I64, _I, _I, _I, _I, _I, _I64, _F, _P,
                         _P]),
     "pa_copy_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _I, _I, _I, _P, _P]),
+    "pa_copy_blocks_layers": (_I, [_P, _I, _P, _I64, _I64, _I, _I, _I, _I, _P, _P]),
     "pa_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P, _P]),
     "pa_check_err_flag": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int), _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "pa.h"
+#include "pa_cache_ops.h"
 #include "pa_internal.h"
 #include "pa_prefill.h"
 
@@ -240,6 +241,28 @@ PA_EXPORT pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *
     cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, k_cache, v_cache, block_mapping, num_pairs,
                                            num_blocks, num_blocks, block_bytes, err_flag,
                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT pa_status pa_copy_blocks_layers(void *kv_cache, int num_layers, const int64_t *block_mapping,
+                                          int64_t num_pairs, int64_t num_blocks, int block_size,
+                                          int num_kv_heads, int head_dim, pa_dtype dtype, int *err_flag,
+                                          void *stream) {
+    if (num_layers < 0 || num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || !cache_dtype_ok(dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_layers > 65535) return PA_ERR_UNSUPPORTED;
+    const int64_t block_bytes =
+        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * elem_bytes(dtype);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0 || num_layers == 0) return PA_OK;
+    if (!kv_cache || !block_mapping || !aligned16(kv_cache)) return PA_ERR_INVALID_ARG;
+    // [layers, 2, num_blocks, ...]: layer l's K at l * 2 * NB blocks, its V right after.
+    uint8_t *base = static_cast<uint8_t *>(kv_cache);
+    const int64_t cache_bytes = num_blocks * block_bytes;
+    cudaError_t e = pa::launch_copy_blocks(base, base + cache_bytes, base, base + cache_bytes, block_mapping,
+                                           num_pairs, num_blocks, num_blocks, block_bytes, err_flag,
+                                           static_cast<cudaStream_t>(stream), num_layers, 2 * cache_bytes);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

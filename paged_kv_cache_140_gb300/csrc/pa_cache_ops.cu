@@ -8,8 +8,8 @@
 // ("优化大模型推理：PagedAttention 如何实现 GPU 显存高效管理", copy-on-write
 // section).  Both are pure data movement bound by HBM bandwidth; grids are
 // sized in multiples of the SM count by the host.
+#include "pa_cache_ops.h"
 #include "pa_device.cuh"
-#include "pa_internal.h"
 
 namespace pa {
 
@@ -100,14 +100,21 @@ __global__ void __launch_bounds__(128)
     }
 }
 
-// grid.x: copy pairs (grid-stride), grid.y: slices of the block; each thread
-// moves 4 chunks of 16 bytes of K and of V per iteration.  Source and
-// destination are separate caches (swap_blocks: e.g. GPU and pinned host
-// memory) or the same one (copy_blocks; its pairs never overlap).
+// grid.x: copy pairs (grid-stride), grid.y: slices of the block, grid.z:
+// layers (caches `layer16` 16-byte units apart); each thread moves 4 chunks
+// of 16 bytes of K and of V per iteration.  Source and destination are
+// separate caches (swap_blocks: e.g. GPU and pinned host memory) or the same
+// one (copy_blocks; its pairs never overlap).
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(const uint4 *src_k, const uint4 *src_v, uint4 *dst_k, uint4 *dst_v,
                        const int64_t *__restrict__ block_mapping, int64_t num_pairs,
-                       int64_t src_blocks, int64_t dst_blocks, int64_t block16, int *err_flag) {
+                       int64_t src_blocks, int64_t dst_blocks, int64_t block16, int64_t layer16,
+                       int *err_flag) {
+    const int64_t lo = static_cast<int64_t>(blockIdx.z) * layer16;
+    src_k += lo;
+    src_v += lo;
+    dst_k += lo;
+    dst_v += lo;
     const int64_t slice = (block16 + gridDim.y - 1) / gridDim.y;
     const int64_t beg = blockIdx.y * slice;
     const int64_t end = min(block16, beg + slice);
@@ -115,7 +122,7 @@ __global__ void __launch_bounds__(256)
         const int64_t src = block_mapping[2 * pr];
         const int64_t dst = block_mapping[2 * pr + 1];
         if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
-            if (threadIdx.x == 0 && blockIdx.y == 0) report(err_flag, 0x8 /* PA_FLAG_BAD_COPY_PAIR */);
+            if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) report(err_flag, 0x8 /* PA_FLAG_BAD_COPY_PAIR */);
             continue;
         }
         const uint4 *ks = src_k + src * block16;
@@ -185,25 +192,28 @@ cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, voi
 cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
                                const int64_t *block_mapping, int64_t num_pairs, int64_t src_blocks,
                                int64_t dst_blocks, int64_t block_bytes, int *err_flag,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int layers, int64_t layer_bytes) {
     const int64_t block16 = block_bytes / 16;
     const int threads = 256;
     const int sms = sm_count();
+    if (layers < 1 || layers > 65535) return cudaErrorInvalidValue;
     // Enough CTAs to cover the SMs a few times over, each slice >= 4 chunks/thread.
     int64_t slices = (block16 + 4 * threads - 1) / (4 * threads);
     const int64_t want = 4LL * sms;
-    if (num_pairs * slices < want) {
-        const int64_t more = (want + num_pairs - 1) / num_pairs;
+    const int64_t units = num_pairs * layers;
+    if (units * slices < want) {
+        const int64_t more = (want + units - 1) / units;
         const int64_t maxs = (block16 + threads - 1) / threads;
         slices = more < maxs ? more : maxs;
     }
     if (slices < 1) slices = 1;
     if (slices > 65535) slices = 65535;
     const int64_t gx = num_pairs < 65535LL * 16 ? num_pairs : 65535LL * 16;
-    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(slices));
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(slices), static_cast<unsigned>(layers));
     copy_blocks_kernel<<<grid, threads, 0, stream>>>(
         static_cast<const uint4 *>(src_k), static_cast<const uint4 *>(src_v), static_cast<uint4 *>(dst_k),
-        static_cast<uint4 *>(dst_v), block_mapping, num_pairs, src_blocks, dst_blocks, block16, err_flag);
+        static_cast<uint4 *>(dst_v), block_mapping, num_pairs, src_blocks, dst_blocks, block16, layer_bytes / 16,
+        err_flag);
     return cudaGetLastError();
 }
 

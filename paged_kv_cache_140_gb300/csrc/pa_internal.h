@@ -1,4 +1,4 @@
-// Host-side interface between the C ABI (pa_api.cu) and the kernel files.
+// Host-side interface between the C ABI (pa_api.cu) and the decode kernel file.
 #pragma once
 
 #include <cuda.h>
@@ -61,24 +61,5 @@ size_t decode_smem_bytes(int head_dim, int group, int elem_bytes, int warps, int
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, int kv,
                           const CUtensorMap &tmap_k, const CUtensorMap &tmap_v, int grid,
                           int warps, size_t smem, cudaStream_t stream);
-
-cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
-                                     void *v_cache, const int64_t *slot_mapping,
-                                     int64_t num_tokens, int64_t num_slots, int64_t row_bytes,
-                                     int *err_flag, cudaStream_t stream);
-
-// Quantising variant: 16-bit rows (bf16 if `bf16`) -> e4m3 codes of
-// x / scale; `row_elems` elements per token row (a multiple of 8).
-cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, void *k_cache,
-                                         void *v_cache, const int64_t *slot_mapping,
-                                         int64_t num_tokens, int64_t num_slots, int64_t row_elems,
-                                         bool bf16, float k_scale, float v_scale, int *err_flag,
-                                         cudaStream_t stream);
-
-// Whole-block copies src -> dst (the same cache for copy_blocks).
-cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
-                               const int64_t *block_mapping, int64_t num_pairs, int64_t src_blocks,
-                               int64_t dst_blocks, int64_t block_bytes, int *err_flag,
-                               cudaStream_t stream);
 
 }  // namespace pa

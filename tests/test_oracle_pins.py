@@ -415,3 +415,26 @@ def test_prefill_is_causal_attention_over_the_paged_context(oracle_lib):
     last = cu[1:] - 1
     dec = oracle_lib.paged_attention(q[last], kc, vc, "f16", tables, np.array(ctx, np.int32), 0.4)
     assert np.array_equal(got[last], dec)
+
+
+def test_copy_blocks_layers_is_per_layer_copy_blocks(oracle_lib):
+    """[layers, 2, NB, bs, Hkv, D]: every layer's K and V get the same block copies;
+    checked against NumPy assignment layer by layer, bad pairs counted per layer."""
+    rng = np.random.default_rng(23)
+    L, NB, bs, Hkv, D = 3, 10, 4, 2, 8
+    kv = rng.integers(0, 2**16, size=(L, 2, NB, bs, Hkv, D), dtype=np.uint16)
+    pairs = np.array([[1, 7], [3, 2], [9, 4], [12, 5], [0, -1]], dtype=np.int64)
+    got, bad = oracle_lib.copy_blocks_layers(kv, pairs)
+    want = kv.copy()
+    for layer in range(L):
+        for src, dst in pairs:
+            if 0 <= src < NB and 0 <= dst < NB:
+                want[layer, :, dst] = kv[layer, :, src]
+    assert np.array_equal(got, want) and bad == 2 * L
+    bytes_kv = rng.integers(0, 256, size=(2, 2, NB, bs, Hkv, 16), dtype=np.uint8)
+    got8, _ = oracle_lib.copy_blocks_layers(bytes_kv, pairs[:3])
+    want8 = bytes_kv.copy()
+    for layer in range(2):
+        for src, dst in pairs[:3]:
+            want8[layer, :, dst] = bytes_kv[layer, :, src]
+    assert np.array_equal(got8, want8)
