@@ -287,9 +287,10 @@ pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype,
  * num_heads / num_kv_heads a power of two up to 128.  Products run on the
  * tensor cores with fp32 accumulation; the softmax weights are rounded to
  * binary16, or for bfloat16 inputs split into two bfloat16 parts.
- * Device-side problems: an invalid cu_seqlens_q entry, or a q_len above
- * max_q_len, sets PA_FLAG_BAD_CONTEXT_LEN and leaves the affected rows
- * unwritten; a context length outside [q_len, max_blocks_per_seq * bs] gives
+ * Device-side problems: an invalid cu_seqlens_q entry sets
+ * PA_FLAG_BAD_CONTEXT_LEN and leaves that sequence's rows unwritten; a q_len
+ * above max_q_len sets it too, and rows beyond the 128/G-token query tiles
+ * the bound implies are left unwritten; a context length outside [q_len, max_blocks_per_seq * bs] gives
  * zero rows and PA_FLAG_BAD_CONTEXT_LEN; a block id outside [0, num_blocks)
  * is not read, sets PA_FLAG_BAD_BLOCK_ID and gives zero rows for the query
  * tiles that needed it.  No workspace; nothing is allocated.

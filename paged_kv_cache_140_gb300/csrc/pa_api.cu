@@ -546,6 +546,7 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     p.log2_group = lg;
     p.block_size = block_size;
     p.num_blocks = num_blocks;
+    p.max_q_len = max_q_len;
     p.tiles_per_seq = static_cast<int>(tiles);
     p.pairs_per_seq = static_cast<int>((tiles + 1) / 2);
     p.scale_log2 = scale * 1.4426950408889634f;

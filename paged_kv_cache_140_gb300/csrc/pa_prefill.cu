@@ -335,8 +335,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         return;
     }
     const int ql = q1 - q0;
-    if (ql > p.tiles_per_seq * TT && pi == 0 && kvh == 0 && threadIdx.x == 0)
-        report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
+    if (ql > p.max_q_len && pi == 0 && kvh == 0 && threadIdx.x == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
     const int t0A = 2 * pi * TT;            // first token of query tile A (B follows)
     if (t0A >= ql) return;
     const bool hasB = t0A + TT < ql;

@@ -27,6 +27,7 @@ struct PrefillParams {
     int log2_group;                 // log2(num_heads / num_kv_heads)
     int block_size;
     int64_t num_blocks;
+    int max_q_len;                  // host bound on every sequence's new-token count
     int tiles_per_seq;              // query tiles per sequence: ceil(max_q_len * group / 128)
     int pairs_per_seq;              // CTAs per (sequence, KV head): ceil(tiles_per_seq / 2)
     float scale_log2;               // softmax scale * log2(e)

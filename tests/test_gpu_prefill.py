@@ -205,3 +205,35 @@ def test_prefill_rejects_bad_arguments(torch):
     with pytest.raises(pa.PagedAttentionError):
         pa.prefill(torch.empty(q3.shape, device="cuda"), q3, T["k_cache"], T["v_cache"], T["block_tables"],
                    T["context_lens"], cu, 0.1, max_q_len=5)
+
+
+def test_prefill_bad_lengths_are_flagged(torch):
+    """q_len > ctx gives zero rows and PA_FLAG_BAD_CONTEXT_LEN; a decreasing
+    cu_seqlens_q or a q_len above max_q_len is flagged too; good sequences
+    are unaffected."""
+    import paged_kv_cache_140_gb300 as pa
+    b = make("prefill", num_seqs=3, prefix_lens=[40, 60, 20], q_lens=[30, 50, 10], num_heads=4, num_kv_heads=4)
+    ref, _, _ = oracle.prefill_step(b)
+    # context shorter than the tail of sequence 1
+    T = to_device(b)
+    T["context_lens"][1] = 20
+    out, _, err = run_prefill(torch, b, dev=T)
+    assert err & pa.FLAG_BAD_CONTEXT_LEN
+    assert float(out[30:80].abs().max()) == 0.0
+    assert_attention_close(out[:30], ref[:30], "f32", "sequence 0")
+    assert_attention_close(out[80:], ref[80:], "f32", "sequence 2")
+    # q_len above the host's max_q_len bound
+    out2, _, err2 = run_prefill(torch, b.__class__(**{**b.__dict__, "max_q_len": 16}))
+    assert err2 & pa.FLAG_BAD_CONTEXT_LEN
+    # cu_seqlens_q running backwards for sequence 2
+    T3 = to_device(b)
+    cu = torch.from_numpy(b.cu_seqlens_q).cuda()
+    cu[3] = 70
+    out3 = torch.zeros(T3["q"].shape, dtype=torch.float32, device="cuda")
+    err3 = pa.new_err_flag()
+    pa.reshape_and_cache(T3["key"], T3["value"], T3["k_cache"], T3["v_cache"], T3["slot_mapping"])
+    pa.prefill(out3, T3["q"], T3["k_cache"], T3["v_cache"], T3["block_tables"], T3["context_lens"], cu,
+               float(b.scale), max_q_len=b.max_q_len, err_flag=err3)
+    torch.cuda.synchronize()
+    assert pa.read_err_flag(err3) & pa.FLAG_BAD_CONTEXT_LEN
+    assert_attention_close(out3[:80], ref[:80], "f32", "sequences 0-1")
