@@ -64,7 +64,9 @@ template <> struct Rings<64> { static constexpr int K = 4, V = 4; };
 struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
-    uint64_t s_full[2], p_full[2];       // per query tile
+    uint64_t s_full[2];                  // per query tile
+    uint64_t p_full[2][2];               // [query tile][32-key chunk of each thread's 64 keys]
+    uint64_t zeroed;                     // once: stale V rows of the last K/V tile zeroed
     uint64_t done;
     uint64_t staged[2];                  // per query tile: its output rows staged for the TMA store
     uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
@@ -368,6 +370,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int qpos_max = qstartA + (hasB ? TT + min(TT, ql - t0A - TT) : min(TT, ql - t0A)) - 1;
     const int nB = hasB ? qpos_max / kTile + 1 : 0;
     const int n_tiles = hasB ? nB : nA;     // K/V tiles loaded (nB >= nA)
+    // The last K/V tile reaches past the last attended position: its stale or
+    // unloaded V rows are zeroed (by the query tile that reaches furthest)
+    // before any PV reads it, so that 0-weights cannot meet NaNs.
+    const bool zero_tail = n_tiles * kTile - 1 > qpos_max;
 
     if (threadIdx.x == 0) {
         mbar_init(&sh.q_full, 1);
@@ -379,11 +385,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i], 256);
+            mbar_init(&sh.p_full[i][0], 256);
+            mbar_init(&sh.p_full[i][1], 256);
             for (int y = 0; y < 2; ++y)
                 for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][y][q], 64);
         }
         mbar_init(&sh.done, 1);
+        mbar_init(&sh.zeroed, 256);
         mbar_init(&sh.staged[0], 256);
         mbar_init(&sh.staged[1], 256);
         sh.abort = 0;
@@ -477,10 +485,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         __syncwarp();
         for (int j = 0; ok && j < n_tiles; ++j) {
             const int vst = j % NV;
-            const bool last = j == n_tiles - 1;
-            // On the last tile the zeroing of stale V rows (done by the
-            // softmax of the tile that reaches furthest) precedes every PV.
-            if (last && hasB && nA == n_tiles && !warp_wait_bar(&sh.p_full[1], j & 1, sh, p.err_flag)) {
+            if (zero_tail && j == n_tiles - 1 && !warp_wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
                 ok = false;
                 break;
             }
@@ -488,24 +493,31 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const uint64_t vd = vd0 + static_cast<uint32_t>(vst) * kOpDesc;
             for (int xx = 0; ok && xx < 2; ++xx) {
                 if (j >= nx[xx]) continue;
-                if (!warp_wait_bar(&sh.p_full[xx], j & 1, sh, p.err_flag)) { ok = false; break; }
-                umma::fence_after_sync();
                 const uint32_t tP = tmem + kColS + 128u * xx;
                 const uint32_t tO = tmem + kColO + 128u * xx;
                 const uint32_t acc0 = j > 0 ? 1u : 0u;
-                if (leader) {
+                // Each softmax thread writes its 64 keys' weights in two 32-key
+                // chunks; chunk c of both row halves feeds k-steps {2c, 2c+1,
+                // 4+2c, 5+2c}, so half of PV runs while the second chunk is made.
 #pragma unroll
-                    for (int k = 0; k < kPVSteps; ++k)
-                        umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1), vd + static_cast<uint32_t>(k * (2048 >> 4)),
-                                     kIdescPV, k > 0 ? 1u : acc0);
-                    if constexpr (BF16) {
+                for (int c = 0; c < 2; ++c) {
+                    if (!warp_wait_bar(&sh.p_full[xx][c], j & 1, sh, p.err_flag)) { ok = false; break; }
+                    umma::fence_after_sync();
+                    if (leader) {
 #pragma unroll
-                        for (int k = 0; k < kPVSteps; ++k)
-                            umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
-                                         vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV, 1u);
+                        for (int kk = 0; kk < kPVSteps / 2; ++kk) {
+                            const int k = 2 * c + (kk & 1) + 4 * (kk >> 1);
+                            umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1),
+                                         vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV,
+                                         (c > 0 || kk > 0) ? 1u : acc0);
+                            if constexpr (BF16)
+                                umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
+                                             vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV, 1u);
+                        }
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
+                if (!ok) break;
                 if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
             }
             if (!ok) break;
@@ -528,7 +540,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const uint32_t tS = tmem + kColS + 128u * x + lane_off + 64u * h;
         const uint32_t tO = tmem + kColO + 128u * x + lane_off + kHalfD * h;
         // The tile that reaches furthest zeroes the stale V rows of the last K/V tile.
-        const bool zeroer = x == (hasB ? 1 : 0) && n_tiles * kTile - 1 > qpos_max;
+        const bool zeroer = zero_tail && x == (hasB ? 1 : 0);
         const float sl = p.scale_log2;
         const uint64_t sl2 = f2(sl, sl);
         float m_run = -CUDART_INF_F;
@@ -589,8 +601,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     m_run = x_tile;
                 }
             }
+            if (zeroer && j == nx - 1) {
+                const int vst = j % NV;
+                if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
+                if (j * kTile + row > qpos_max && (R > 1 || h == 0)) {
+                    uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + (R > 1 ? h : 0) * kRegion + row * 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.zeroed);
+            }
             // weights p = 2^(s * scale_log2 - m) as 16-bit pairs, each 32-key
-            // chunk written over its own S columns
+            // chunk written over its own S columns and released on its own
             const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
             const uint64_t nm2 = f2(-mref, -mref);
             uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
@@ -621,24 +644,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 }
                 umma::st_32x32b_x16(tS + 32 * c, hi);
                 if constexpr (BF16) umma::st_32x32b_x16(tS + 32 * c + 16, lo);
+                umma::wait_st();
+                umma::fence_before_sync();
+                mbar_arrive(&sh.p_full[x][c]);
             }
             const float2 acc = unf2(add2(acc0, acc1));
             l_run += acc.x + acc.y;
-            if (zeroer && j == nx - 1) {
-                // V rows past the last attended position hold stale or unloaded
-                // data; zero them so that 0-weights cannot meet NaNs.
-                const int vst = j % NV;
-                if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-                if (j * kTile + row > qpos_max && (R > 1 || h == 0)) {
-                    uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + (R > 1 ? h : 0) * kRegion + row * 128);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-            }
-            umma::wait_st();
-            umma::fence_before_sync();
-            mbar_arrive(&sh.p_full[x]);
         }
         // `done` completes once every MMA of the CTA (the last PV included) has.
         if (ok && warp_wait_bar(&sh.done, 0, sh, p.err_flag)) {
