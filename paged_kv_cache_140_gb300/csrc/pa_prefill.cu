@@ -2,24 +2,25 @@
 //
 // After a prefix-cache hit only a sequence's tail is computed: its new query
 // tokens attend, causally, to the cached prefix blocks and to themselves
-// ("SGLang / nano-vllm ... PagedAttention" walkthrough, §3.4; the block table
-// and [block, offset] cache layout of §2.2).  Query token i of a sequence
-// with q_len new tokens and ctx total tokens sits at position
-// ctx - q_len + i and attends positions 0 .. that position.
+// (nano-vllm walkthrough, lqnn.cn/news/170268, §3.4; the block table and
+// [block, offset] cache layout of §2.2).  Query token i of a sequence with
+// q_len new tokens and ctx total tokens sits at position ctx - q_len + i and
+// attends positions 0 .. that position.
 //
 // A query tile is 128 rows of one (sequence, KV head): 128/G tokens times the
 // G query heads that share the KV head.  One CTA runs two consecutive query
 // tiles, X = A and B, against every 128-token K/V tile it loads, so each K/V
-// byte brought into shared memory feeds 256 query rows (the SM's intake of
-// K/V, not the tensor cores, is what a single tile would be limited by).
-// Per K/V tile j and query tile X:
+// byte brought into shared memory feeds 256 query rows and the two tiles'
+// MMAs interleave in the tensor pipe.  Per K/V tile j and query tile X:
 //   S_X = Q_X K_j^T   tcgen05.mma, Q and K tiles in shared memory (TMA,
 //                     128-byte swizzle), S in tensor memory;
 //   softmax           eight warps per query tile, two threads per row (64
 //                     columns each, the row max traded through shared memory);
 //                     running max and sum in registers, the output rescaled
 //                     only when the max grows by more than 2^8; the weights P
-//                     written as 16-bit pairs over the S columns they came from;
+//                     written as 16-bit pairs over the S columns they came
+//                     from, released to the MMA in two 32-key chunks so that
+//                     half of PV runs while the second chunk is made;
 //   O_X += P_X V_j    tcgen05.mma with P read from tensor memory and V
 //                     (MN-major) from shared memory, O in tensor memory.
 // The MMA stream runs ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...; tcgen05
@@ -28,12 +29,15 @@
 // j+1 starts, O_X already holds tile j.  bfloat16 weights carry only 8
 // significant bits, so for bf16 inputs P is split into P_hi + P_lo (both
 // bf16, P_lo = P - P_hi) and PV runs twice; binary16 weights are used as is.
+// Full query tiles leave through shared-memory staging and TMA stores.
 //
 // Warp roles: warps 0-15 run the softmax and the epilogue (warp w: query tile
 // w / 8, column half (w / 4) % 2, TMEM lanes 32 (w % 4)..); warp 16 loads the
 // query tiles and the K tiles, warp 18 the V tiles (both read the block table
-// 32 entries at a time); warp 17 owns the tensor memory and one of its lanes
-// issues every MMA.  Every mbarrier wait is bounded (2 s); a timeout sets
+// 32 entries at a time); warp 17 owns the tensor memory and runs the MMA
+// issue loop in uniform control flow, one elected lane issuing (tcgen05
+// operands computed per lane inside a one-lane branch cost ~40 % of the MMA
+// rate).  Every mbarrier wait is bounded (2 s); a timeout sets
 // PA_FLAG_TIMEOUT and the CTA winds down without further MMAs.
 #include <math_constants.h>
 
