@@ -55,6 +55,9 @@ CASES = [
     ("gqa", dict(num_seqs=2, ctx_cap=12000), None),
     ("13b", dict(num_seqs=8, block_size=8), 64),
     ("7b", dict(context_lens=[0, 1, 16, 17, 255, 256, 257]), 64),
+    ("tiny", dict(num_heads=8, num_kv_heads=2), None),
+    ("7b", dict(num_seqs=6, block_size=32), None),
+    ("gqa", dict(num_seqs=3, ctx_cap=3000, block_size=8), 128),
 ]
 
 
