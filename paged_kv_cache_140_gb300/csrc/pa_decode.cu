@@ -163,16 +163,17 @@ __device__ __forceinline__ void store_row(void *base, int dtype, int64_t off, co
     }
 }
 
-// 128-dim heads run at most 12 warps per CTA (the slot ring fills shared
-// memory); 64-dim heads run up to 16.
-template <int D>
-constexpr int kMaxThreads = D == 128 ? 384 : 512;
+// 128-dim heads with 16-bit caches run at most 12 warps per CTA (their slot
+// ring fills shared memory); e4m3 caches (half the slot) and 64-dim heads run
+// up to 16, in 128 registers per thread.
+template <int D, int KV>
+constexpr int kMaxThreads = (D == 128 && KV < 2) ? 384 : 512;
 
 // KV: 0 = f16 cache and query, 1 = bf16 cache and query, 2 / 3 = e4m3 cache
 // with an f16 / bf16 query (run as f16 MMAs; e4m3 values are exact in f16,
 // bf16 queries are rounded to f16).
 template <int D, int G, int KV>
-__global__ void __launch_bounds__(kMaxThreads<D>, 1)
+__global__ void __launch_bounds__((kMaxThreads<D, KV>), 1)
     paged_decode_kernel(const __grid_constant__ DecodeParams p,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v) {
