@@ -378,7 +378,7 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
     // the defaults for tuning); fewer warps are used if shared memory is short.
     const Tuning &tune = tuning();
     const int stages = tune.stages > 0 ? tune.stages : pa::kDefaultStages;
-    const int max_warps = (head_dim == 128 && !fp8) ? 12 : 16;
+    const int max_warps = head_dim == 128 ? 12 : 16;
     const int def_warps = head_dim == 128 ? (fp8 ? pa::kDefaultWarpsFp8 : pa::kDefaultWarps128) : 16;
     int warps = tune.warps > 0 ? std::min(tune.warps, max_warps) : def_warps;
     const int es = elem_bytes(kv_dtype);

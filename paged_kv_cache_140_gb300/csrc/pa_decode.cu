@@ -15,12 +15,15 @@
 //    into contiguous ranges of equal token weight, one per warp, so a
 //    long-tailed length mix cannot leave SMs idle at the end.
 //  * Each warp owns a ring of shared-memory slots.  A slot holds one 16-token
-//    stage: the K and V rows of one KV head, brought in by TMA (3-D tensor map
-//    over [blocks*block_size, Hkv, D], 64-element boxes with 128-byte swizzle)
+//    stage (two for an e4m3 cache, 8 KB of K and V either way): the K and V
+//    rows of one KV head, brought in by TMA (3-D tensor map over
+//    [blocks*block_size, Hkv, D], 128-byte boxes with 128-byte swizzle)
 //    straight from the physical block the table names, plus the item's query
-//    rows (bulk copy) on its first stage.  Loads for the next stages - across
-//    item boundaries - are in flight while the warp computes on the current
-//    one; the block-table slice of the next item is prefetched into registers.
+//    rows (bulk copy) on its first stage.  The stages of a slot are processed
+//    jointly: QK of each, one softmax update over all their tokens, PV of
+//    each.  Loads for the next slots - across item boundaries - are in flight
+//    while the warp computes on the current one; the block-table slice of the
+//    next item is prefetched into registers.
 //  * QK and PV run on warp-level tensor-core MMA (m16n8k16, fp32 accumulate):
 //    the query heads of one KV group are the N = 8 columns (a dense tile for
 //    G = 8, padded for smaller groups).  Decode is bound by reading K/V; the
@@ -49,12 +52,20 @@ constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kRowBytes = 128;                          // one swizzled 64-element half row
 constexpr int kRegionBytes = kStageTokens * kRowBytes;  // 16 rows x 128 B = 2 KB
 
-// ES = bytes per cache element (2: f16/bf16, 1: e4m3).
-template <int D, int G, int ES>
+// Slots of an e4m3 cache carry two consecutive 16-token stages (8 KB of K
+// and V, like one 16-bit stage), so that the per-slot work (barrier wait,
+// loads, bookkeeping) is paid once per 8 KB; 16-bit caches one stage.
+template <int ES>
+constexpr int kSub = ES == 1 ? 2 : 1;
+
+// ES = bytes per cache element (2: f16/bf16, 1: e4m3).  A slot holds SUB
+// stages: K of stage h at h * kHalfBytes, V of stage h at kVOffset + the same.
+template <int D, int G, int ES, int SUB = kSub<ES>>
 struct Layout {
     static constexpr int kBoxes = D * ES / 128;            // 128-byte TMA boxes per K (or V) row
     static constexpr int kBoxElems = 128 / ES;             // elements per box row
-    static constexpr int kTileBytes = kBoxes * kRegionBytes;
+    static constexpr int kHalfBytes = kBoxes * kRegionBytes;   // one stage's K (or V) rows
+    static constexpr int kTileBytes = SUB * kHalfBytes;
     static constexpr int kVOffset = kTileBytes;
     static constexpr int kQOffset = 2 * kTileBytes;
     static constexpr int kQBytes = G * D * 2;              // the query stays 16-bit
@@ -163,11 +174,10 @@ __device__ __forceinline__ void store_row(void *base, int dtype, int64_t off, co
     }
 }
 
-// 128-dim heads with 16-bit caches run at most 12 warps per CTA (their slot
-// ring fills shared memory); e4m3 caches (half the slot) and 64-dim heads run
-// up to 16, in 128 registers per thread.
+// 128-dim heads run at most 12 warps per CTA (the slot ring fills shared
+// memory); 64-dim heads run up to 16.
 template <int D, int KV>
-constexpr int kMaxThreads = (D == 128 && KV < 2) ? 384 : 512;
+constexpr int kMaxThreads = D == 128 ? 384 : 512;
 
 // KV: 0 = f16 cache and query, 1 = bf16 cache and query, 2 / 3 = e4m3 cache
 // with an f16 / bf16 query (run as f16 MMAs; e4m3 values are exact in f16,
@@ -182,6 +192,7 @@ __global__ void __launch_bounds__((kMaxThreads<D, KV>), 1)
     constexpr bool BF16 = KV == 1;     // MMA operand type
     static_assert(!kFp8 || D == 128, "the e4m3 cache path is built for head_dim 128");
     using L = Layout<D, G, kFp8 ? 1 : 2>;
+    constexpr int SUB = kSub<kFp8 ? 1 : 2>;    // stages per slot
     using Cvt = Half2x<BF16>;
     constexpr int KS = L::kSteps;   // QK steps over the head dim
     constexpr int MT = L::kSteps;   // PV tiles over the head dim
@@ -341,46 +352,56 @@ __global__ void __launch_bounds__((kMaxThreads<D, KV>), 1)
                 next_ready = true;
             }
         }
-        const int tok0 = ic.part * P + ij * kStageTokens;
-        const int n = ic.ntok > 0 ? min(kStageTokens, ic.ntok - ij * kStageTokens) : 0;
-        int mask = n > 0 ? static_cast<int>((1u << n) - 1u) : 0;
-        int ids[2] = {-1, -1};
-        uint32_t bytes = 0;
+        int tok0[SUB], ids[SUB][2];
+        uint32_t mask_all = 0, bytes = 0;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            if (b < nsub) {
-                const bool used = n > b * bs;
-                const int idx = used ? (tok0 + b * bs) / bs - fb : 0;
-                const int id = __shfl_sync(kFull, bid, idx & 31);
-                if (used) {
-                    if (id < 0 || static_cast<int64_t>(id) >= p.num_blocks) {
-                        mask &= ~(((1 << rows) - 1) << (b * bs));
-                        if (lane == 0) report(p.err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
-                    } else {
-                        ids[b] = id;
-                        bytes += 2u * L::kBoxes * rows * kRowBytes;
+        for (int hs = 0; hs < SUB; ++hs) {
+            const int js = ij + hs;   // stage of the item
+            tok0[hs] = ic.part * P + js * kStageTokens;
+            const int n = (ic.ntok > 0 && js < ic.nst) ? min(kStageTokens, ic.ntok - js * kStageTokens) : 0;
+            int mask = n > 0 ? static_cast<int>((1u << n) - 1u) : 0;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                ids[hs][b] = -1;
+                if (b < nsub) {
+                    const bool used = n > b * bs;
+                    const int idx = used ? (tok0[hs] + b * bs) / bs - fb : 0;
+                    const int id = __shfl_sync(kFull, bid, idx & 31);
+                    if (used) {
+                        if (id < 0 || static_cast<int64_t>(id) >= p.num_blocks) {
+                            mask &= ~(((1 << rows) - 1) << (b * bs));
+                            if (lane == 0) report(p.err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
+                        } else {
+                            ids[hs][b] = id;
+                            bytes += 2u * L::kBoxes * rows * kRowBytes;
+                        }
                     }
                 }
             }
+            mask_all |= static_cast<uint32_t>(mask) << (kStageTokens * hs);
         }
         const bool with_q = (ij == 0 && ic.ntok > 0);
         if (with_q) bytes += L::kQBytes;
         if (lane == 0) {
             StageMeta m;
             m.s = ic.s; m.kvh = ic.kvh; m.part = ic.part; m.j = ij;
-            m.nst = ic.nst; m.nparts = ic.nparts; m.mask = mask; m.pad = 0;
+            m.nst = ic.nst; m.nparts = ic.nparts; m.mask = static_cast<int>(mask_all); m.pad = 0;
             meta[slot] = m;
             mbar_arrive_expect_tx(&bars[slot], bytes);
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                if (ids[b] >= 0) {
-                    const int z = ids[b] * bs + ((tok0 + b * bs) % bs);
+            for (int hs = 0; hs < SUB; ++hs) {
 #pragma unroll
-                    for (int h = 0; h < L::kBoxes; ++h) {
-                        tma_load_3d(sp + h * kRegionBytes + b * rows * kRowBytes, &tmap_k,
-                                    &bars[slot], h * L::kBoxElems, ic.kvh, z, policy);
-                        tma_load_3d(sp + L::kVOffset + h * kRegionBytes + b * rows * kRowBytes,
-                                    &tmap_v, &bars[slot], h * L::kBoxElems, ic.kvh, z, policy);
+                for (int b = 0; b < 2; ++b) {
+                    if (ids[hs][b] >= 0) {
+                        const int z = ids[hs][b] * bs + ((tok0[hs] + b * bs) % bs);
+                        uint8_t *kd = sp + hs * L::kHalfBytes + b * rows * kRowBytes;
+#pragma unroll
+                        for (int h = 0; h < L::kBoxes; ++h) {
+                            tma_load_3d(kd + h * kRegionBytes, &tmap_k, &bars[slot], h * L::kBoxElems, ic.kvh, z,
+                                        policy);
+                            tma_load_3d(kd + L::kVOffset + h * kRegionBytes, &tmap_v, &bars[slot],
+                                        h * L::kBoxElems, ic.kvh, z, policy);
+                        }
                     }
                 }
             }
@@ -390,7 +411,8 @@ __global__ void __launch_bounds__((kMaxThreads<D, KV>), 1)
                 bulk_load(sp + L::kQOffset, qsrc, L::kQBytes, &bars[slot]);
             }
         }
-        if (++ij == ic.nst) {
+        ij += SUB;
+        if (ij >= ic.nst) {
             ij = 0;
             for (int k = 0; k < step; ++k) ic.advance(ctx_s, prefix, Hkv, P, B);
             more = ic.start < hi;
@@ -491,79 +513,105 @@ __global__ void __launch_bounds__((kMaxThreads<D, KV>), 1)
             for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
         }
 
-        if (m.j == nj && ((m.mask >> nrow) & 1) && nid >= 0 && nid < p.num_blocks) {
-            // This stage holds the step's new token: put its K/V row into the
-            // tile (in place of whatever the cache slot held) and into the cache.
-            const int64_t nslot = static_cast<int64_t>(nid) * bs + npos % bs;
-            const int64_t row_off = (nslot * Hkv + m.kvh) * D;
-            if constexpr (kFp8) {
-                const float2 a = Half2x<kQBf16>::to_float2(nk.x), b = Half2x<kQBf16>::to_float2(nk.y);
-                const float2 c2 = Half2x<kQBf16>::to_float2(nv.x), d2 = Half2x<kQBf16>::to_float2(nv.y);
-                const uint32_t ck = f32x2_to_e4m3x2(__fdiv_rn(a.x, p.k_scale_w), __fdiv_rn(a.y, p.k_scale_w)) |
-                                    (f32x2_to_e4m3x2(__fdiv_rn(b.x, p.k_scale_w), __fdiv_rn(b.y, p.k_scale_w)) << 16);
-                const uint32_t cv = f32x2_to_e4m3x2(__fdiv_rn(c2.x, p.v_scale_w), __fdiv_rn(c2.y, p.v_scale_w)) |
-                                    (f32x2_to_e4m3x2(__fdiv_rn(d2.x, p.v_scale_w), __fdiv_rn(d2.y, p.v_scale_w)) << 16);
-                const int off = nrow * kRowBytes + (((lane >> 2) ^ (nrow & 7)) << 4) + (lane & 3) * 4;
-                *reinterpret_cast<uint32_t *>(sp + off) = ck;
-                *reinterpret_cast<uint32_t *>(sp + L::kVOffset + off) = cv;
-                reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.k_cache_w) + row_off)[lane] = ck;
-                reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.v_cache_w) + row_off)[lane] = cv;
-            } else {
-                if (D == 128 || lane < 16) {
-                    const int hr = D == 128 ? (lane >> 4) : 0, cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
-                    const int off = hr * kRegionBytes + nrow * kRowBytes + ((cc ^ (nrow & 7)) << 4) + sub;
-                    *reinterpret_cast<uint2 *>(sp + off) = nk;
-                    *reinterpret_cast<uint2 *>(sp + L::kVOffset + off) = nv;
-                    uint2 *kd = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.k_cache_w) + row_off);
-                    uint2 *vd = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.v_cache_w) + row_off);
-                    kd[lane] = nk;
-                    vd[lane] = nv;
+        // The slot's SUB stages (m.j, m.j + 1, ...) are processed jointly: QK of
+        // each, one softmax update over all their tokens, PV of each.  A second
+        // stage past the item's end (odd stage count) is skipped.
+        const bool second = SUB > 1 && m.j + 1 < m.nst;
+        int smask[SUB];
+#pragma unroll
+        for (int hs = 0; hs < SUB; ++hs)
+            smask[hs] = static_cast<int>((static_cast<uint32_t>(m.mask) >> (kStageTokens * hs)) & 0xffffu);
+
+#pragma unroll
+        for (int hs = 0; hs < SUB; ++hs) {
+            uint8_t *sp_h = sp + hs * L::kHalfBytes;   // stage m.j + hs: K rows here, V at + kVOffset
+            if (m.j + hs == nj && ((smask[hs] >> nrow) & 1) && nid >= 0 && nid < p.num_blocks) {
+                // This stage holds the step's new token: put its K/V row into the
+                // tile (in place of whatever the cache slot held) and into the cache.
+                const int64_t nslot = static_cast<int64_t>(nid) * bs + npos % bs;
+                const int64_t row_off = (nslot * Hkv + m.kvh) * D;
+                if constexpr (kFp8) {
+                    const float2 a = Half2x<kQBf16>::to_float2(nk.x), b = Half2x<kQBf16>::to_float2(nk.y);
+                    const float2 c2 = Half2x<kQBf16>::to_float2(nv.x), d2 = Half2x<kQBf16>::to_float2(nv.y);
+                    const uint32_t ck = f32x2_to_e4m3x2(__fdiv_rn(a.x, p.k_scale_w), __fdiv_rn(a.y, p.k_scale_w)) |
+                                        (f32x2_to_e4m3x2(__fdiv_rn(b.x, p.k_scale_w), __fdiv_rn(b.y, p.k_scale_w)) << 16);
+                    const uint32_t cv = f32x2_to_e4m3x2(__fdiv_rn(c2.x, p.v_scale_w), __fdiv_rn(c2.y, p.v_scale_w)) |
+                                        (f32x2_to_e4m3x2(__fdiv_rn(d2.x, p.v_scale_w), __fdiv_rn(d2.y, p.v_scale_w)) << 16);
+                    const int off = nrow * kRowBytes + (((lane >> 2) ^ (nrow & 7)) << 4) + (lane & 3) * 4;
+                    *reinterpret_cast<uint32_t *>(sp_h + off) = ck;
+                    *reinterpret_cast<uint32_t *>(sp_h + L::kVOffset + off) = cv;
+                    reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.k_cache_w) + row_off)[lane] = ck;
+                    reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.v_cache_w) + row_off)[lane] = cv;
+                } else {
+                    if (D == 128 || lane < 16) {
+                        const int hr = D == 128 ? (lane >> 4) : 0, cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
+                        const int off = hr * kRegionBytes + nrow * kRowBytes + ((cc ^ (nrow & 7)) << 4) + sub;
+                        *reinterpret_cast<uint2 *>(sp_h + off) = nk;
+                        *reinterpret_cast<uint2 *>(sp_h + L::kVOffset + off) = nv;
+                        uint2 *kd = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.k_cache_w) + row_off);
+                        uint2 *vd = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.v_cache_w) + row_off);
+                        kd[lane] = nk;
+                        vd[lane] = nv;
+                    }
                 }
+                __syncwarp();
             }
-            __syncwarp();
         }
 
-        // ---- QK^T: 16 tokens x 8 heads, two accumulators over the dim steps ----
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-            const int j = lane >> 3, r = lane & 7;
-            const int tok = r + 8 * (j & 1);
-            if constexpr (!kFp8) {
+        // ---- QK^T per stage: 16 tokens x 8 heads, two accumulators over the dim steps ----
+        // x[hs][i]: i = 0 (token g, head 2t), 1 (g, 2t+1), 2 (g+8, 2t), 3 (g+8, 2t+1)
+        float x[SUB][4];
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int ch = 2 * ks + (j >> 1);
-                    uint32_t a[4];
-                    ldsm_x4(a, sa + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
-                    mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
-                }
-            } else {
-                // ldmatrix on the byte tile viewed as 16-bit: each register holds
-                // four consecutive dims of one token; split into two f16 pairs,
-                // each 32-dim chunk feeds two MMAs (dims permuted alike in q).
+        for (int hs = 0; hs < SUB; ++hs) {
+            if (hs > 0 && !second) {
+                x[hs][0] = x[hs][1] = x[hs][2] = x[hs][3] = -INFINITY;
+                continue;
+            }
+            const uint32_t sa_h = sa + hs * L::kHalfBytes;
+            float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int j = lane >> 3, r = lane & 7;
+                const int tok = r + 8 * (j & 1);
+                if constexpr (!kFp8) {
 #pragma unroll
-                for (int kc = 0; kc < D / 32; ++kc) {
-                    const int ch = 2 * kc + (j >> 1);
-                    uint32_t a[4], lo[4], hi[4];
-                    ldsm_x4(a, sa + tok * kRowBytes + ((ch ^ r) << 4));
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int ch = 2 * ks + (j >> 1);
+                        uint32_t a[4];
+                        ldsm_x4(a, sa_h + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
+                        mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
+                    }
+                } else {
+                    // ldmatrix on the byte tile viewed as 16-bit: each register holds
+                    // four consecutive dims of one token; split into two f16 pairs,
+                    // each 32-dim chunk feeds two MMAs (dims permuted alike in q).
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(a[i], lo[i], hi[i]);
-                    mma_16816<false>(c[0], lo, qf[2 * kc][0], qf[2 * kc][1]);
-                    mma_16816<false>(c[1], hi, qf[2 * kc + 1][0], qf[2 * kc + 1][1]);
+                    for (int kc = 0; kc < D / 32; ++kc) {
+                        const int ch = 2 * kc + (j >> 1);
+                        uint32_t a[4], lo[4], hi[4];
+                        ldsm_x4(a, sa_h + tok * kRowBytes + ((ch ^ r) << 4));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(a[i], lo[i], hi[i]);
+                        mma_16816<false>(c[0], lo, qf[2 * kc][0], qf[2 * kc][1]);
+                        mma_16816<false>(c[1], hi, qf[2 * kc + 1][0], qf[2 * kc + 1][1]);
+                    }
                 }
             }
-        }
-        // x[i]: i = 0 (token g, head 2t), 1 (g, 2t+1), 2 (g+8, 2t), 3 (g+8, 2t+1)
-        float x[4];
-        {
-            const bool v_lo = (m.mask >> g) & 1, v_hi = (m.mask >> (g + 8)) & 1;
+            const bool v_lo = (smask[hs] >> g) & 1, v_hi = (smask[hs] >> (g + 8)) & 1;
             const bool h0 = 2 * t < G, h1 = 2 * t + 1 < G;
             const float sc = p.scale_log2;
-            x[0] = (v_lo && h0) ? (c[0][0] + c[1][0]) * sc : -INFINITY;
-            x[1] = (v_lo && h1) ? (c[0][1] + c[1][1]) * sc : -INFINITY;
-            x[2] = (v_hi && h0) ? (c[0][2] + c[1][2]) * sc : -INFINITY;
-            x[3] = (v_hi && h1) ? (c[0][3] + c[1][3]) * sc : -INFINITY;
+            x[hs][0] = (v_lo && h0) ? (c[0][0] + c[1][0]) * sc : -INFINITY;
+            x[hs][1] = (v_lo && h1) ? (c[0][1] + c[1][1]) * sc : -INFINITY;
+            x[hs][2] = (v_hi && h0) ? (c[0][2] + c[1][2]) * sc : -INFINITY;
+            x[hs][3] = (v_hi && h1) ? (c[0][3] + c[1][3]) * sc : -INFINITY;
         }
-        float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+
+        // ---- one online-softmax update over the slot's tokens ----
+        float mx[2] = {fmaxf(x[0][0], x[0][2]), fmaxf(x[0][1], x[0][3])};
+#pragma unroll
+        for (int hs = 1; hs < SUB; ++hs) {
+            mx[0] = fmaxf(mx[0], fmaxf(x[hs][0], x[hs][2]));
+            mx[1] = fmaxf(mx[1], fmaxf(x[hs][1], x[hs][3]));
+        }
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             mx[0] = fmaxf(mx[0], __shfl_xor_sync(kFull, mx[0], o));
@@ -591,80 +639,87 @@ __global__ void __launch_bounds__((kMaxThreads<D, KV>), 1)
         }
         const float mu0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
         const float mu1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
-        const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
-        const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
-        l_run[0] += p0 + p2;
-        l_run[1] += p1 + p3;
 
-        // ---- P as the PV B fragment: lane needs p(token 2t|2t+1|2t+8|2t+9, head g) ----
-        uint32_t bhi[2], blo[2];
-        {
-            const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
-            const bool odd = g & 1;
-            const float a0 = __shfl_sync(kFull, p0, srcA), a1 = __shfl_sync(kFull, p1, srcA);
-            const float a2 = __shfl_sync(kFull, p2, srcA), a3 = __shfl_sync(kFull, p3, srcA);
-            const float b0 = __shfl_sync(kFull, p0, srcB), b1 = __shfl_sync(kFull, p1, srcB);
-            const float b2 = __shfl_sync(kFull, p2, srcB), b3 = __shfl_sync(kFull, p3, srcB);
-            const float w[4] = {odd ? a1 : a0, odd ? b1 : b0, odd ? a3 : a2, odd ? b3 : b2};
-            // Split each weight into a 16-bit high part and a 16-bit residual,
-            // so the tensor-core product keeps ~16 significant bits of p.
+        // ---- per stage: weights, P as the PV B fragment, PV ----
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                bhi[k] = pack2<BF16>(w[2 * k], w[2 * k + 1]);
-                const float2 h = Cvt::to_float2(bhi[k]);
-                blo[k] = pack2<BF16>(w[2 * k] - h.x, w[2 * k + 1] - h.y);
-            }
-        }
+        for (int hs = 0; hs < SUB; ++hs) {
+            if (hs > 0 && !second) continue;
+            const float p0 = fast_exp2(x[hs][0] - mu0), p1 = fast_exp2(x[hs][1] - mu1);
+            const float p2 = fast_exp2(x[hs][2] - mu0), p3 = fast_exp2(x[hs][3] - mu1);
+            l_run[0] += p0 + p2;
+            l_run[1] += p1 + p3;
 
-        // ---- PV over the stage; rows past the context are zeroed first ----
-        const uint32_t va = sa + L::kVOffset;
-        if (m.mask != 0xffff) {
-            // Stale rows (past the context, or of a skipped block) may hold
-            // NaN; 0 * NaN would poison the tensor-core sums, so clear them.
-            uint8_t *vt = sp + L::kVOffset;
+            // lane needs p(token 2t|2t+1|2t+8|2t+9, head g)
+            uint32_t bhi[2], blo[2];
+            {
+                const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
+                const bool odd = g & 1;
+                const float a0 = __shfl_sync(kFull, p0, srcA), a1 = __shfl_sync(kFull, p1, srcA);
+                const float a2 = __shfl_sync(kFull, p2, srcA), a3 = __shfl_sync(kFull, p3, srcA);
+                const float b0 = __shfl_sync(kFull, p0, srcB), b1 = __shfl_sync(kFull, p1, srcB);
+                const float b2 = __shfl_sync(kFull, p2, srcB), b3 = __shfl_sync(kFull, p3, srcB);
+                const float w[4] = {odd ? a1 : a0, odd ? b1 : b0, odd ? a3 : a2, odd ? b3 : b2};
+                // Split each weight into a 16-bit high part and a 16-bit residual,
+                // so the tensor-core product keeps ~16 significant bits of p.
 #pragma unroll
-            for (int k = 0; k < kStageTokens * L::kBoxes * 8 / 32; ++k) {
-                const int q16 = lane + 32 * k;                // 16-byte chunk index
-                const int row = (q16 >> 3) % kStageTokens;    // 8 chunks per 128-byte row
-                if (!((m.mask >> row) & 1))
-                    *reinterpret_cast<uint4 *>(vt + q16 * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncwarp();
-        }
-        {
-            const int j = lane >> 3, r = lane & 7;
-            const int tok = r + 8 * (j >> 1);
-            if constexpr (!kFp8) {
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int ch = 2 * mt + (j & 1);
-                    uint32_t a[4];
-                    ldsm_x4_trans(a, va + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
-                    mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
-                    mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                for (int k = 0; k < 2; ++k) {
+                    bhi[k] = pack2<BF16>(w[2 * k], w[2 * k + 1]);
+                    const float2 h = Cvt::to_float2(bhi[k]);
+                    blo[k] = pack2<BF16>(w[2 * k] - h.x, w[2 * k + 1] - h.y);
                 }
-            } else {
-                // Transposed ldmatrix of the byte tile viewed as 16-bit gives
-                // (tokens 2t, 2t+1) x (dims 2g, 2g+1); regroup the bytes so
-                // each f16 pair is one dim over two tokens: even dims feed
-                // acc[2vc], odd dims acc[2vc+1].
+            }
+
+            // rows past the context are zeroed first
+            uint8_t *sp_h = sp + hs * L::kHalfBytes;
+            const uint32_t va = sa + hs * L::kHalfBytes + L::kVOffset;
+            if (smask[hs] != 0xffff) {
+                // Stale rows (past the context, or of a skipped block) may hold
+                // NaN; 0 * NaN would poison the tensor-core sums, so clear them.
+                uint8_t *vt = sp_h + L::kVOffset;
 #pragma unroll
-                for (int vc = 0; vc < D / 32; ++vc) {
-                    const int ch = 2 * vc + (j & 1);
-                    uint32_t a[4], ev[4], od[4];
-                    ldsm_x4_trans(a, va + tok * kRowBytes + ((ch ^ r) << 4));
+                for (int k = 0; k < kStageTokens * L::kBoxes * 8 / 32; ++k) {
+                    const int q16 = lane + 32 * k;                // 16-byte chunk index
+                    const int row = (q16 >> 3) % kStageTokens;    // 8 chunks per 128-byte row
+                    if (!((smask[hs] >> row) & 1))
+                        *reinterpret_cast<uint4 *>(vt + q16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            {
+                const int j = lane >> 3, r = lane & 7;
+                const int tok = r + 8 * (j >> 1);
+                if constexpr (!kFp8) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(prmt(a[i], 0x3120u), ev[i], od[i]);
-                    mma_16816<false>(acc[2 * vc], ev, bhi[0], bhi[1]);
-                    mma_16816<false>(acc[2 * vc], ev, blo[0], blo[1]);
-                    mma_16816<false>(acc[2 * vc + 1], od, bhi[0], bhi[1]);
-                    mma_16816<false>(acc[2 * vc + 1], od, blo[0], blo[1]);
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const int ch = 2 * mt + (j & 1);
+                        uint32_t a[4];
+                        ldsm_x4_trans(a, va + (ch >> 3) * kRegionBytes + tok * kRowBytes + (((ch & 7) ^ r) << 4));
+                        mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
+                        mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                    }
+                } else {
+                    // Transposed ldmatrix of the byte tile viewed as 16-bit gives
+                    // (tokens 2t, 2t+1) x (dims 2g, 2g+1); regroup the bytes so
+                    // each f16 pair is one dim over two tokens: even dims feed
+                    // acc[2vc], odd dims acc[2vc+1].
+#pragma unroll
+                    for (int vc = 0; vc < D / 32; ++vc) {
+                        const int ch = 2 * vc + (j & 1);
+                        uint32_t a[4], ev[4], od[4];
+                        ldsm_x4_trans(a, va + tok * kRowBytes + ((ch ^ r) << 4));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(prmt(a[i], 0x3120u), ev[i], od[i]);
+                        mma_16816<false>(acc[2 * vc], ev, bhi[0], bhi[1]);
+                        mma_16816<false>(acc[2 * vc], ev, blo[0], blo[1]);
+                        mma_16816<false>(acc[2 * vc + 1], od, bhi[0], bhi[1]);
+                        mma_16816<false>(acc[2 * vc + 1], od, blo[0], blo[1]);
+                    }
                 }
             }
         }
 
         // ---- item end: output (or partial state) staged through shared memory ----
-        if (m.j == m.nst - 1) {
+        if (m.j + SUB >= m.nst) {
             float lt[2] = {l_run[0], l_run[1]};
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {

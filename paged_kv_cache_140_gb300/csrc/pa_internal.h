@@ -15,10 +15,10 @@ constexpr int kStageTokens = 16;
 // 7B, GQA, prefix sharing); deeper rings or more warps only add L2/HBM queueing.
 constexpr int kDefaultStages = 2;
 constexpr int kDefaultWarps128 = 8;
-// e4m3 caches: a stage carries half the bytes and more per-byte work, so
-// more warps per SM keep HBM busy (16 x 2 in 128 registers measured best,
-// 1.4 % ahead of 12 warps in 168 registers).
-constexpr int kDefaultWarpsFp8 = 16;
+// e4m3 caches: a slot carries two 16-token stages (8 KB of K and V); 12
+// warps fill shared memory (measured best: 8 warps 341 us, 11 293.5, 12 268.4
+// on the 13B-shaped step).
+constexpr int kDefaultWarpsFp8 = 12;
 
 struct DecodeParams {
     void *out;
