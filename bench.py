@@ -244,6 +244,26 @@ def device_tensors(b, device):
     return host, dev
 
 
+def stage_inputs(tensors, device):
+    """One pinned host buffer holding every tensor of ``tensors`` (256-byte
+    aligned) and its device twin, with device views shaped like the inputs:
+    a step's inputs then cross to the GPU in one copy, as a serving engine
+    stages them."""
+    import torch
+    offs, n = {}, 0
+    for k, v in tensors.items():
+        offs[k] = n
+        n += (v.numel() * v.element_size() + 255) // 256 * 256
+    flat_h = torch.empty(max(n, 256), dtype=torch.uint8).pin_memory()
+    flat_d = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    views = {}
+    for k, v in tensors.items():
+        nb = v.numel() * v.element_size()
+        flat_h[offs[k]:offs[k] + nb].copy_(v.contiguous().view(-1).view(torch.uint8))
+        views[k] = flat_d[offs[k]:offs[k] + nb].view(v.dtype).view(v.shape)
+    return flat_h, flat_d, views
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -348,18 +368,16 @@ def run_ours(args, world, rank, local):
     ms_step = ms_total / K
     decode_ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
 
-    # End to end: pinned host inputs -> device, the step, result -> pinned host.
-    pinned = {k: v.pin_memory() for k, v in host.items()}
+    # End to end: the step's inputs staged in one pinned host buffer and
+    # copied in one transfer, the step's launches replayed as one CUDA graph
+    # (pa.StepGraph), the result copied back to pinned host memory.
+    used = {k: v for k, v in host.items() if k != "block_mapping" or has_pairs}
+    flat_h, flat_d, e2e_in = stage_inputs(used, device)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    e2e_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    h2d = sum(v.numel() * v.element_size() for k, v in pinned.items() if k != "block_mapping" or has_pairs)
+    h2d = sum(v.numel() * v.element_size() for v in used.values())
     d2h = out_h.numel() * out_h.element_size()
 
-    def e2e_step():
-        for k, v in pinned.items():
-            if k == "block_mapping" and not has_pairs:
-                continue
-            e2e_in[k].copy_(v, non_blocking=True)
+    def e2e_kernels():
         if has_pairs:
             pa.copy_blocks(T["k_cache"], T["v_cache"], e2e_in["block_mapping"])
         pa.reshape_and_cache(e2e_in["key"], e2e_in["value"], T["k_cache"], T["v_cache"], e2e_in["slot_mapping"],
@@ -367,6 +385,13 @@ def run_ours(args, world, rank, local):
         pa.decode(out, e2e_in["q"], T["k_cache"], T["v_cache"], e2e_in["block_tables"], e2e_in["context_lens"],
                   float(b.scale), max_context_len=b.max_context_len, partition_size=b.partition_size,
                   workspace=ws, k_scale=b.k_scale, v_scale=b.v_scale)
+
+    flat_d.copy_(flat_h, non_blocking=True)
+    step_graph = pa.StepGraph(e2e_kernels)
+
+    def e2e_step():
+        flat_d.copy_(flat_h, non_blocking=True)
+        step_graph.replay()
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -432,8 +457,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(kv_all / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens -> device, "
-                        "the step, output -> pinned host, stream sync; the KV cache stays resident"},
+                "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens (staged in one "
+                        "pinned buffer) -> device in one copy, the step's launches replayed as one CUDA graph "
+                        "(pa.StepGraph), output -> pinned host, stream sync; the KV cache stays resident"},
         "gpu_launches": K * ((1 if fused else 2) + (1 if has_pairs else 0) + (1 if split else 0)),
         "fused_append": bool(fused),
         "clocks": clocks,
@@ -527,17 +553,19 @@ def run_prefill(args, world, rank, local):
     ms_step = t0.elapsed_time(t1) / K
     attn_ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
 
-    pinned = {k: v.pin_memory() for k, v in host.items()}
+    # End to end as for decode: one staged copy in, the step as one graph
+    # launch, the result back to pinned host memory.
+    used = {k: v for k, v in host.items() if k != "block_mapping" or has_pairs}
+    flat_h, flat_d, e2e_in = stage_inputs(used, device)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    e2e_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    used = [k for k in pinned if k != "block_mapping" or has_pairs]
-    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in used)
+    h2d = sum(v.numel() * v.element_size() for v in used.values())
     d2h = out_h.numel() * out_h.element_size()
+    flat_d.copy_(flat_h, non_blocking=True)
+    step_graph = pa.StepGraph(lambda: step(src=e2e_in))
 
     def e2e_step():
-        for k in used:
-            e2e_in[k].copy_(pinned[k], non_blocking=True)
-        step(src=e2e_in)
+        flat_d.copy_(flat_h, non_blocking=True)
+        step_graph.replay()
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -596,8 +624,9 @@ def run_prefill(args, world, rank, local):
         },
         "e2e": {"value": round(fl_all / (e2e_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens/cu_seqlens_q -> "
-                        "device, the step, output -> pinned host, stream sync; the KV cache stays resident"},
+                "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens/cu_seqlens_q "
+                        "(staged in one pinned buffer) -> device in one copy, the step's launches replayed as one "
+                        "CUDA graph (pa.StepGraph), output -> pinned host, stream sync; the KV cache stays resident"},
         "gpu_launches": K * (2 + (1 if has_pairs else 0)),
         "clocks": clocks,
     }

@@ -26,7 +26,7 @@ from ._lib import (FLAG_BAD_BLOCK_ID, FLAG_BAD_CONTEXT_LEN, FLAG_BAD_COPY_PAIR, 
 __all__ = ["reshape_and_cache", "decode", "decode_append", "prefill", "copy_blocks", "copy_blocks_layers", "swap_blocks", "decode_workspace_size",
            "decode_partition_size", "DecodeWorkspace", "new_err_flag", "read_err_flag",
            "PagedAttentionError", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK_ID", "FLAG_BAD_CONTEXT_LEN",
-           "FLAG_BAD_COPY_PAIR", "FLAG_TIMEOUT", "library_path"]
+           "FLAG_BAD_COPY_PAIR", "FLAG_TIMEOUT", "library_path", "StepGraph"]
 
 
 def library_path() -> str:
@@ -313,3 +313,38 @@ def prefill(out, query, k_cache, v_cache, block_tables, context_lens, cu_seqlens
                                 _ptr(context_lens), _ptr(cu_seqlens_q), B, T, int(max_q_len), Hq, hkv, D, bs,
                                 nb, float(scale), _ptr(err_flag), _stream(query.device))
     _lib.check(st, "pa_prefill")
+
+
+class StepGraph:
+    """A step of this library's calls captured once as a CUDA graph and then
+    replayed with one launch, as a serving loop does for its decode step.
+
+    ``fn()`` enqueues the step (e.g. :func:`reshape_and_cache` then
+    :func:`decode`) on the current stream, on device buffers that stay
+    allocated at the same addresses for the graph's lifetime; refill those
+    buffers in place between replays.  Everything ``fn`` needs is allocated
+    before capture: it is run ``warmup`` times first (so default workspaces
+    exist), and workspaces passed to it must already be large enough.  The
+    argument checks of each call run at capture; a replay launches the
+    captured kernels (with their programmatic dependent launch edges) as they
+    were.
+    """
+
+    def __init__(self, fn, warmup: int = 1):
+        torch = _torch()
+        self._fn = fn
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(max(1, warmup)):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+        torch.cuda.synchronize()
+
+    def replay(self) -> None:
+        """Launch the captured step on the current stream."""
+        self.graph.replay()
