@@ -244,6 +244,15 @@ def device_tensors(b, device):
     return host, dev
 
 
+def step_percentiles(marks):
+    """p10 / p50 / p90 of the per-step times (us) between consecutive events."""
+    ts = sorted(a.elapsed_time(z) * 1e3 for a, z in zip(marks[:-1], marks[1:]))
+    if not ts:
+        return None
+    q = lambda f: round(ts[min(len(ts) - 1, int(f * (len(ts) - 1) + 0.5))], 2)
+    return {"p10": q(0.1), "p50": q(0.5), "p90": q(0.9)}
+
+
 def stage_inputs(tensors, device):
     """One pinned host buffer holding every tensor of ``tensors`` (256-byte
     aligned) and its device twin, with device views shaped like the inputs:
@@ -357,9 +366,12 @@ def run_ours(args, world, rank, local):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     t0.record(stream)
+    marks[0].record(stream)
     for k in range(K):
         step(evs[k])
+        marks[k + 1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -367,6 +379,7 @@ def run_ours(args, world, rank, local):
     ms_total = t0.elapsed_time(t1)
     ms_step = ms_total / K
     decode_ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
+    pct = step_percentiles(marks)
 
     # End to end: the step's inputs staged in one pinned host buffer and
     # copied in one transfer, the step's launches replayed as one CUDA graph
@@ -423,6 +436,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup,
         "ms_per_step": round(ms_max, 5),
         "us_per_step": round(ms_max * 1e3, 2),
+        "us_per_step_pct": pct,
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 1),
         "peak_kind": peak_kind,
@@ -543,15 +557,19 @@ def run_prefill(args, world, rank, local):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     t0.record(stream)
+    marks[0].record(stream)
     for k in range(K):
         step(evs[k])
+        marks[k + 1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
     ms_step = t0.elapsed_time(t1) / K
     attn_ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
+    pct = step_percentiles(marks)
 
     # End to end as for decode: one staged copy in, the step as one graph
     # launch, the result back to pinned host memory.
@@ -594,6 +612,7 @@ def run_prefill(args, world, rank, local):
         "warmup": args.warmup,
         "ms_per_step": round(ms_max, 5),
         "us_per_step": round(ms_max * 1e3, 2),
+        "us_per_step_pct": pct,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -701,7 +720,7 @@ def run_prefill_reference(args, world, rank):
 
 
 KERNEL_SOURCES = {
-    "decode": ("pa_decode.cu", "pa_device.cuh", "pa_internal.h"),
+    "decode": ("pa_decode.cu", "pa_decode_coop.cu", "pa_device.cuh", "pa_internal.h"),
     "prefill": ("pa_prefill.cu", "pa_prefill.h", "pa_umma.cuh", "pa_device.cuh"),
 }
 

@@ -70,6 +70,8 @@ struct Tuning {
     int stages = 0;  // 0: default
     int warps = 0;
     int interleave = 1;
+    int coop = 1;            // 0: never use the CTA-cooperative decode kernel
+    int coop_stages = 0;     // 0: default
 };
 
 int env_int(const char *name, int lo, int hi) {
@@ -86,6 +88,9 @@ const Tuning &tuning() {
         r.warps = env_int("PA_DECODE_WARPS", 1, 16);
         const char *il = getenv("PA_DECODE_INTERLEAVE");
         r.interleave = (il != nullptr && il[0] == '0') ? 0 : 1;
+        const char *co = getenv("PA_DECODE_COOP");
+        r.coop = (co != nullptr && co[0] == '0') ? 0 : 1;
+        r.coop_stages = env_int("PA_DECODE_COOP_STAGES", 2, 4);
         return r;
     }();
     return t;
@@ -154,6 +159,26 @@ bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, i
               const_cast<void *>(cache), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map over a 16-bit cache [NB * bs, Hkv, D] with its dimensions taken
+// in the order (dim, token, head): a box {64, 16, 8} is one 64-column half of
+// 16 token rows for 8 consecutive KV heads, landing as 8 per-head tiles of 16
+// rows x 128 bytes, 128-byte swizzle (the cooperative decode kernel).
+bool encode_cache_map_heads8(CUtensorMap *map, const void *cache, int64_t num_blocks, int block_size,
+                             int num_kv_heads, int head_dim) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
+                                static_cast<cuuint64_t>(num_blocks) * block_size,
+                                static_cast<cuuint64_t>(num_kv_heads)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2,
+                                   static_cast<cuuint64_t>(head_dim) * 2};
+    const cuuint32_t box[3] = {64u, 16u, 8u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(cache), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -423,6 +448,24 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
     p.v_scale_w = v_scale;
     p.interleave = tune.interleave;
 
+    // 16-bit caches whose KV heads come in groups of 8 run the CTA-cooperative
+    // kernel (8-head TMA boxes); everything else the per-warp kernel.
+    if (tune.coop && !fp8 && new_k == nullptr && head_dim == 128 && num_kv_heads % 8 == 0 &&
+        block_size % 16 == 0) {
+        int cst = tune.coop_stages > 0 ? tune.coop_stages : 3;
+        while (cst > 2 && pa::decode_coop_smem_bytes(G, cst, num_seqs) > static_cast<size_t>(dev.smem_optin))
+            --cst;
+        const size_t csmem = pa::decode_coop_smem_bytes(G, cst, num_seqs);
+        CUtensorMap ck, cv;
+        if (csmem > 0 && csmem <= static_cast<size_t>(dev.smem_optin) &&
+            encode_cache_map_heads8(&ck, k_cache, num_blocks, block_size, num_kv_heads, head_dim) &&
+            encode_cache_map_heads8(&cv, v_cache, num_blocks, block_size, num_kv_heads, head_dim)) {
+            p.stages = cst;
+            const cudaError_t e = pa::launch_decode_coop(p, G, kv_dtype == PA_BF16, ck, cv, dev.sms, csmem,
+                                                         static_cast<cudaStream_t>(stream));
+            return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+        }
+    }
     const int kv = fp8 ? (q_dtype == PA_F16 ? 2 : 3) : (kv_dtype == PA_BF16 ? 1 : 0);
     cudaError_t e = pa::launch_decode(p, head_dim, G, kv, tk, tv, dev.sms, warps,
                                       smem_used, static_cast<cudaStream_t>(stream));

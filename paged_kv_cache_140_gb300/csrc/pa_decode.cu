@@ -927,9 +927,14 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtenso
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(grid), dim3(warps * 32), smem, stream, p, tk, tv);
-    if (e != cudaSuccess || p.max_partitions <= 1) return e;
-    // Merge of split sequences: 1-8 warps per (sequence, KV head, query head),
-    // about 16 partitions per warp.
+    if (e != cudaSuccess) return e;
+    return launch_decode_merge(p, D, G, stream);
+}
+
+// Merge of split sequences: 1-8 warps per (sequence, KV head, query head),
+// about 16 partitions per warp.
+template <int D, int G>
+cudaError_t launch_merge_t(const DecodeParams &p, cudaStream_t stream) {
     int wt = 1;
     while (wt < 8 && wt * 16 < p.max_partitions) wt *= 2;
     const int64_t tasks = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * G;
@@ -937,6 +942,17 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tk, const CUtenso
     return launch_pdl(paged_decode_merge_kernel<D, G>,
                       dim3(static_cast<unsigned>((tasks + per_cta - 1) / per_cta)), dim3(256), 0,
                       stream, p, wt);
+}
+
+template <int D>
+cudaError_t launch_merge_g(const DecodeParams &p, int group, cudaStream_t stream) {
+    switch (group) {
+        case 1: return launch_merge_t<D, 1>(p, stream);
+        case 2: return launch_merge_t<D, 2>(p, stream);
+        case 4: return launch_merge_t<D, 4>(p, stream);
+        case 8: return launch_merge_t<D, 8>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int D, int G>
@@ -985,6 +1001,13 @@ size_t decode_smem_bytes(int head_dim, int group, int elem_bytes, int warps, int
     if (head_dim == 64) return smem_g<64, 2>(group, warps, stages, num_seqs);
     return elem_bytes == 1 ? smem_g<128, 1>(group, warps, stages, num_seqs)
                            : smem_g<128, 2>(group, warps, stages, num_seqs);
+}
+
+cudaError_t launch_decode_merge(const DecodeParams &p, int head_dim, int group, cudaStream_t stream) {
+    if (p.max_partitions <= 1) return cudaSuccess;
+    if (head_dim == 64) return launch_merge_g<64>(p, group, stream);
+    if (head_dim == 128) return launch_merge_g<128>(p, group, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, int kv,

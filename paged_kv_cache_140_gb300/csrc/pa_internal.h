@@ -58,6 +58,19 @@ struct DecodeParams {
 size_t decode_smem_bytes(int head_dim, int group, int elem_bytes, int warps, int stages,
                          int num_seqs);
 
+// The CTA-cooperative decode kernel (pa_decode_coop.cu): 16-bit caches, head
+// dim 128, KV heads a multiple of 8, block size a multiple of 16; `tk`/`tv`
+// map each cache as (dim, token, head) with {64, 16, 8} boxes.  Launches the
+// merge kernel after it when sequences are split.
+size_t decode_coop_smem_bytes(int group, int stages, int num_seqs);
+cudaError_t launch_decode_coop(const DecodeParams &p, int group, bool bf16, const CUtensorMap &tk,
+                               const CUtensorMap &tv, int grid, size_t smem, cudaStream_t stream);
+
+// The merge of split sequences' partial states (pa_decode.cu), chained with
+// programmatic dependent launch; nothing is launched when no sequence splits.
+cudaError_t launch_decode_merge(const DecodeParams &p, int head_dim, int group, cudaStream_t stream);
+
+
 // kv: 0 = f16 cache/query, 1 = bf16, 2 = e4m3 cache + f16 query, 3 = e4m3 + bf16.
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, int kv,
                           const CUtensorMap &tmap_k, const CUtensorMap &tmap_v, int grid,
