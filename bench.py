@@ -244,6 +244,16 @@ def device_tensors(b, device):
     return host, dev
 
 
+def decode_kernel_name(b, fused=False):
+    """The decode kernel pa_decode runs for this batch: the CTA-cooperative one
+    for 16-bit caches whose KV heads come in groups of 8 (head_dim 128, block
+    size a multiple of 16; PA_DECODE_COOP=0 turns it off), else the per-warp
+    one."""
+    coop = (os.environ.get("PA_DECODE_COOP", "1")[:1] != "0" and not fused and b.cache_dtype != "fp8"
+            and b.head_dim == 128 and b.num_kv_heads % 8 == 0 and b.block_size % 16 == 0)
+    return "paged_decode_coop_kernel" if coop else "paged_decode_kernel"
+
+
 def step_percentiles(marks):
     """p10 / p50 / p90 of the per-step times (us) between consecutive events."""
     ts = sorted(a.elapsed_time(z) * 1e3 for a, z in zip(marks[:-1], marks[1:]))
@@ -458,7 +468,7 @@ def run_ours(args, world, rank, local):
             "parallelism": f"replicas x{world} (independent batches per GPU)",
         },
         "roofline": {
-            "kernel": "paged_decode_kernel",
+            "kernel": decode_kernel_name(b, fused),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
