@@ -730,7 +730,7 @@ def run_prefill_reference(args, world, rank):
 
 
 KERNEL_SOURCES = {
-    "decode": ("pa_decode.cu", "pa_decode_coop.cu", "pa_device.cuh", "pa_internal.h"),
+    "decode": ("pa_decode.cu", "pa_decode_coop.cu", "pa_decode_common.cuh", "pa_device.cuh", "pa_internal.h"),
     "prefill": ("pa_prefill.cu", "pa_prefill.h", "pa_umma.cuh", "pa_device.cuh"),
 }
 

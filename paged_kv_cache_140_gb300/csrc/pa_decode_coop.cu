@@ -23,6 +23,7 @@
 //    when all eight consumers are done with it; every wait is bounded and a
 //    timeout sets PA_FLAG_TIMEOUT.  The producer also owns the work cursor and
 //    the block-table reads, so the consumers' loop holds only the math.
+#include "pa_decode_common.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -30,7 +31,8 @@ namespace pa {
 
 namespace {
 
-constexpr uint32_t kFull = 0xffffffffu;
+using namespace decode_common;
+
 constexpr int kGroupHeads = 8;                    // KV heads per box and consumer warps
 constexpr int kCoopThreads = (kGroupHeads + 1) * 32;
 constexpr int kRow = 128;                         // bytes of one swizzled 64-element row half
@@ -58,12 +60,6 @@ struct CoopMeta {
 
 __device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Stages of a sequence summed over its KV heads (the per-warp kernel's weight).
-__device__ __forceinline__ uint32_t seq_weight(int ctx, int hkv) {
-    const int st = ctx > 0 ? (ctx + kStageTokens - 1) / kStageTokens : 1;
-    return static_cast<uint32_t>(st) * static_cast<uint32_t>(hkv);
 }
 
 // Items (s, part, group) in that order; an item weighs 8 x its stages.
@@ -96,39 +92,6 @@ struct CoopCursor {
         }
     }
 };
-
-// Maximum over the warp of a float, via an order-preserving integer image.
-__device__ __forceinline__ float warp_max(float x) {
-    int k = __float_as_int(x);
-    k = k >= 0 ? k : k ^ 0x7fffffff;
-    k = __reduce_max_sync(kFull, k);
-    return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
-}
-
-// D/32 consecutive floats of a row as f32, bf16 or f16 (pa_dtype 2, 1, 0), RNE.
-template <int D>
-__device__ __forceinline__ void store_row(void *base, int dtype, int64_t off, const float *o) {
-    constexpr int DPL = D / 32;
-    if (dtype == 2) {
-        float *dst = static_cast<float *>(base) + off;
-        if constexpr (DPL == 4)
-            *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-        else
-            *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
-    } else {
-        uint16_t h[DPL];
-#pragma unroll
-        for (int i = 0; i < DPL; ++i)
-            h[i] = dtype == 1 ? __bfloat16_as_ushort(__float2bfloat16_rn(o[i]))
-                              : __half_as_ushort(__float2half_rn(o[i]));
-        uint16_t *dst = static_cast<uint16_t *>(base) + off;
-        if constexpr (DPL == 4)
-            *reinterpret_cast<uint2 *>(dst) =
-                make_uint2(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16));
-        else
-            *reinterpret_cast<uint32_t *>(dst) = h[0] | (uint32_t(h[1]) << 16);
-    }
-}
 
 template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(kCoopThreads, 1)
@@ -531,21 +494,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
             __syncwarp();
         }
     }
-}
-
-template <typename Kern, typename... Args>
-cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <int G, bool BF16>
