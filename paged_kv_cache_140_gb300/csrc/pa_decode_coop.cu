@@ -21,8 +21,11 @@
 //    plus residual.
 //  * Slots are CTA-wide: `full` completes when a stage's copies land, `empty`
 //    when all eight consumers are done with it; every wait is bounded and a
-//    timeout sets PA_FLAG_TIMEOUT.  The producer also owns the work cursor and
-//    the block-table reads, so the consumers' loop holds only the math.
+//    timeout sets PA_FLAG_TIMEOUT.  An item's query rows go to a 2-entry ring
+//    of their own (read once, at the item's first stage), so slots hold only
+//    K and V and a 3-deep ring fits for groups of up to 4 query heads per KV
+//    head.  The producer also owns the work cursor and the block-table reads,
+//    so the consumers' loop holds only the math.
 #include "pa_decode_common.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -44,9 +47,8 @@ struct CoopLayout {
     static constexpr int kBoxBytes = kGroupHeads * kHeadTile;      // 16 KB
     static constexpr int kKBytes = kHalves * kBoxBytes;
     static constexpr int kVOffset = kKBytes;
-    static constexpr int kQOffset = 2 * kKBytes;
     static constexpr int kQBytes = kGroupHeads * G * D * 2;         // the group's query rows
-    static constexpr int kSlotBytes = ((kQOffset + kQBytes + 1023) / 1024) * 1024;
+    static constexpr int kSlotBytes = 2 * kKBytes;                  // K and V of one stage
     static constexpr int kOStride = D + 4;
     static constexpr int kOBytes = G * kOStride * 4;                // per consumer warp
     static constexpr int kSteps = D / 16;
@@ -57,6 +59,10 @@ struct CoopMeta {
     int s, kvh0, part, j;        // s < 0: no more work
     int nst, nparts, mask, pad;
 };
+
+// The items' query rows sit in a ring of their own (kQRing entries, one per
+// item), so that stage slots hold only K and V.
+constexpr int kQRing = 2;
 
 __device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -119,12 +125,15 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
     const int ngroups = Hkv / kGroupHeads;
 
     uint8_t *slots = smem;
-    uint8_t *misc = smem + static_cast<size_t>(S) * L::kSlotBytes;
+    uint8_t *qbuf = smem + static_cast<size_t>(S) * L::kSlotBytes;   // kQRing x kQBytes
+    uint8_t *misc = qbuf + kQRing * L::kQBytes;
     CoopMeta *meta = reinterpret_cast<CoopMeta *>(misc);
     misc += S * sizeof(CoopMeta);
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + S;
-    misc += 2 * S * 8;
+    uint64_t *qfull = empty + S;
+    uint64_t *qempty = qfull + kQRing;
+    misc += (2 * S + 2 * kQRing) * 8;
     float *obuf_all = reinterpret_cast<float *>(misc);
     misc += kGroupHeads * L::kOBytes;
     uint32_t *warp_tot = reinterpret_cast<uint32_t *>(misc);
@@ -136,6 +145,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kGroupHeads);
+        }
+        for (int i = 0; i < kQRing; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], kGroupHeads);
         }
         fence_barrier_init();
         prefetch_tensormap(&tmap_k);
@@ -218,6 +231,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         }
         int islot = 0;
         uint32_t uses = 0;   // slots filled so far (the empty barrier's phase follows it)
+        uint32_t items = 0;  // items started (the query ring's position and phase)
         bool ok = true;
         auto take_slot = [&]() -> int {
             const int slot = islot;
@@ -242,6 +256,29 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                     bid = __ldg(p.block_tables + static_cast<int64_t>(ic.s) * p.max_blocks_per_seq + fb + lane);
             }
             const int kvh0 = ic.grp * kGroupHeads;
+            {
+                // the item's query rows into the next entry of the query ring
+                const int qi = static_cast<int>(items % kQRing);
+                if (items >= static_cast<uint32_t>(kQRing)) {
+                    const uint32_t par = ((items / kQRing) - 1) & 1u;
+                    if (!mbar_try_wait(&qempty[qi], par) && !mbar_wait_bounded(&qempty[qi], par)) {
+                        if (lane == 0) report(p.err_flag, 0x10 /* PA_FLAG_TIMEOUT */);
+                        ok = false;
+                        break;
+                    }
+                }
+                if (lane == 0) {
+                    const bool with_q = ic.ntok > 0;
+                    mbar_arrive_expect_tx(&qfull[qi], with_q ? static_cast<uint32_t>(L::kQBytes) : 0u);
+                    if (with_q) {
+                        const uint16_t *qsrc = static_cast<const uint16_t *>(p.q) +
+                                               (static_cast<int64_t>(ic.s) * Hq + kvh0 * G) * D;
+                        bulk_load(qbuf + qi * L::kQBytes, qsrc, L::kQBytes, &qfull[qi]);
+                    }
+                }
+                ++items;
+                __syncwarp();
+            }
             for (int j = 0; ok && j < ic.nst; ++j) {
                 const int slot = take_slot();
                 if (!ok) break;
@@ -255,14 +292,12 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                     mask = 0;
                     if (lane == 0) report(p.err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
                 }
-                const bool with_q = j == 0 && ic.ntok > 0;
                 if (lane == 0) {
                     CoopMeta m;
                     m.s = ic.s; m.kvh0 = kvh0; m.part = ic.part; m.j = j;
                     m.nst = ic.nst; m.nparts = ic.nparts; m.mask = mask; m.pad = 0;
                     meta[slot] = m;
-                    const uint32_t bytes = (load ? 2u * L::kKBytes : 0u) + (with_q ? L::kQBytes : 0u);
-                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    mbar_arrive_expect_tx(&full[slot], load ? 2u * L::kKBytes : 0u);
                     if (load) {
                         const int z = id * bs + (tok0 % bs);
 #pragma unroll
@@ -271,11 +306,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                             tma_load_3d(sp + L::kVOffset + h * L::kBoxBytes, &tmap_v, &full[slot], h * 64, z,
                                         kvh0, policy);
                         }
-                    }
-                    if (with_q) {
-                        const uint16_t *qsrc = static_cast<const uint16_t *>(p.q) +
-                                               (static_cast<int64_t>(ic.s) * Hq + kvh0 * G) * D;
-                        bulk_load(sp + L::kQOffset, qsrc, L::kQBytes, &full[slot]);
                     }
                 }
                 __syncwarp();
@@ -307,6 +337,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
     float m_run[2], l_run[2];
     int cslot = 0;
     uint32_t cphase = 0;
+    uint32_t citems = 0;   // items started (the query ring's position and phase)
     for (;;) {
         const int slot = cslot;
         uint8_t *sp = slots + static_cast<size_t>(slot) * L::kSlotBytes;
@@ -326,13 +357,24 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         const uint32_t va = sa + L::kVOffset + warp * kHeadTile; // my V rows, half 0
 
         if (m.j == 0) {
-            // new item: my query heads' B fragments from the slot
-            const uint32_t *qw = reinterpret_cast<const uint32_t *>(sp + L::kQOffset) + warp * (G * D / 2);
+            // new item: my query heads' B fragments from the query ring
+            const int qi = static_cast<int>(citems % kQRing);
+            const uint32_t qpar = (citems / kQRing) & 1u;
+            ++citems;
+            if (!mbar_try_wait(&qfull[qi], qpar) && !mbar_wait_bounded(&qfull[qi], qpar)) {
+                if (lane == 0) report(p.err_flag, 0x10 /* PA_FLAG_TIMEOUT */);
+                return;
+            }
+            const uint32_t *qw =
+                reinterpret_cast<const uint32_t *>(qbuf + qi * L::kQBytes) + warp * (G * D / 2);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 qf[ks][0] = g < G ? qw[(g * D + ks * 16 + 2 * t) >> 1] : 0u;
                 qf[ks][1] = g < G ? qw[(g * D + ks * 16 + 2 * t + 8) >> 1] : 0u;
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(&qempty[qi]);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 m_run[e] = -INFINITY;
@@ -511,6 +553,7 @@ template <int G>
 size_t coop_smem_for(int stages, int num_seqs) {
     using L = CoopLayout<128, G>;
     return 1024 + static_cast<size_t>(stages) * (L::kSlotBytes + sizeof(CoopMeta) + 16) +
+           static_cast<size_t>(kQRing) * (L::kQBytes + 16) +
            kGroupHeads * L::kOBytes + 32 * 4 + 4 * static_cast<size_t>(num_seqs) +
            4 * (static_cast<size_t>(num_seqs) + 1);
 }
