@@ -1,0 +1,63 @@
+"""GPU checks of the CTA-cooperative decode kernel (16-bit caches whose KV
+heads come in groups of 8, head_dim 128, block size a multiple of 16): parity
+with the oracle for every group size, including G = 8 (two-deep ring), and bit
+equality with the per-warp kernel, which a child process selects with
+PA_DECODE_COOP=0."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_140_gb300 import workloads as W
+
+from pa_harness import assert_attention_close, run_step
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_140_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+CASES = [   # (workload, Hq, Hkv, dtype, block size)
+    ("7b", 8, 8, "f16", 16),
+    ("7b", 16, 8, "bf16", 16),
+    ("7b", 32, 8, "bf16", 32),
+    ("7b", 64, 8, "f16", 16),
+    ("7b", 32, 16, "bf16", 64),
+    ("7b", 48, 24, "f16", 16),
+]
+
+
+@pytest.mark.parametrize("name,hq,hkv,dtype,bs", CASES, ids=[f"{c[1]}x{c[2]}-{c[3]}-bs{c[4]}" for c in CASES])
+def test_cooperative_kernel_matches_oracle(name, hq, hkv, dtype, bs):
+    b = W.make_batch(name, num_seqs=6, ctx_cap=1500, num_heads=hq, num_kv_heads=hkv, dtype=dtype,
+                     block_size=bs)
+    ref, kc, vc = oracle.decode_step(b)
+    out, T, flag = run_step(b)
+    assert flag == 0
+    assert_attention_close(out, ref, "f32", f"coop {hq}/{hkv} {dtype} bs {bs}")
+
+
+@pytest.mark.parametrize("hq,hkv,dtype", [(40, 40, "bf16"), (32, 8, "bf16"), (64, 8, "f16")])
+def test_cooperative_and_per_warp_kernels_agree_bit_for_bit(tmp_path, hq, hkv, dtype):
+    outs = {}
+    for coop in ("1", "0"):
+        path = str(tmp_path / f"out_{coop}.npy")
+        env = dict(os.environ, PA_DECODE_COOP=coop)
+        r = subprocess.run([sys.executable, os.path.join(HERE, "coop_child.py"), "7b", str(hq), str(hkv), dtype,
+                            path], env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs[coop] = np.load(path)
+    assert np.array_equal(outs["1"], outs["0"])
