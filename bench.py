@@ -244,12 +244,12 @@ def device_tensors(b, device):
     return host, dev
 
 
-def decode_kernel_name(b, fused=False):
-    """The decode kernel pa_decode runs for this batch: the CTA-cooperative one
-    for 16-bit caches whose KV heads come in groups of 8 (head_dim 128, block
-    size a multiple of 16; PA_DECODE_COOP=0 turns it off), else the per-warp
-    one."""
-    coop = (os.environ.get("PA_DECODE_COOP", "1")[:1] != "0" and not fused and b.cache_dtype != "fp8"
+def decode_kernel_name(b):
+    """The decode kernel pa_decode / pa_decode_append run for this batch: the
+    CTA-cooperative one for 16-bit caches whose KV heads come in groups of 8
+    (head_dim 128, block size a multiple of 16; PA_DECODE_COOP=0 turns it off),
+    else the per-warp one."""
+    coop = (os.environ.get("PA_DECODE_COOP", "1")[:1] != "0" and b.cache_dtype != "fp8"
             and b.head_dim == 128 and b.num_kv_heads % 8 == 0 and b.block_size % 16 == 0)
     return "paged_decode_coop_kernel" if coop else "paged_decode_kernel"
 
@@ -312,7 +312,15 @@ def run_ours(args, world, rank, local):
                                      b.max_context_len, b.partition_size) > 0
     stream = torch.cuda.current_stream(device)
 
-    fused = args.fused and not has_pairs and len(b.slot_mapping) == int((b.context_lens > 0).sum())
+    # The step as one pa_decode_append call where it applies (one new token
+    # per sequence at position ctx - 1, no copy-on-write pairs first) and runs
+    # on the cooperative kernel (append kernel + decode chained, measured
+    # faster than the separate calls); --fused forces it on the per-warp kernel
+    # too (in-kernel append, measured slower); else, or with --separate,
+    # reshape_and_cache followed by decode.
+    applicable = not has_pairs and len(b.slot_mapping) == int((b.context_lens > 0).sum())
+    fused = applicable and not args.separate and (
+        args.fused or decode_kernel_name(b) == "paged_decode_coop_kernel")
     if fused:
         has = torch.from_numpy(np.nonzero(b.context_lens > 0)[0]).to(device)
         T["key_rows"] = torch.zeros((b.num_seqs, b.num_kv_heads, b.head_dim), dtype=T["key"].dtype,
@@ -395,12 +403,23 @@ def run_ours(args, world, rank, local):
     # copied in one transfer, the step's launches replayed as one CUDA graph
     # (pa.StepGraph), the result copied back to pinned host memory.
     used = {k: v for k, v in host.items() if k != "block_mapping" or has_pairs}
+    if fused:
+        # pa_decode_append takes one new row per sequence; no slot mapping
+        used = {k: v for k, v in used.items() if k not in ("key", "value", "slot_mapping")}
+        used["key_rows"] = T["key_rows"].cpu()
+        used["value_rows"] = T["value_rows"].cpu()
     flat_h, flat_d, e2e_in = stage_inputs(used, device)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in used.values())
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_kernels():
+        if fused:
+            pa.decode_append(out, e2e_in["q"], e2e_in["key_rows"], e2e_in["value_rows"], T["k_cache"],
+                             T["v_cache"], e2e_in["block_tables"], e2e_in["context_lens"], float(b.scale),
+                             max_context_len=b.max_context_len, partition_size=b.partition_size,
+                             workspace=ws, k_scale=b.k_scale, v_scale=b.v_scale)
+            return
         if has_pairs:
             pa.copy_blocks(T["k_cache"], T["v_cache"], e2e_in["block_mapping"])
         pa.reshape_and_cache(e2e_in["key"], e2e_in["value"], T["k_cache"], T["v_cache"], e2e_in["slot_mapping"],
@@ -468,7 +487,7 @@ def run_ours(args, world, rank, local):
             "parallelism": f"replicas x{world} (independent batches per GPU)",
         },
         "roofline": {
-            "kernel": decode_kernel_name(b, fused),
+            "kernel": decode_kernel_name(b),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -481,11 +500,16 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(kv_all / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens (staged in one "
-                        "pinned buffer) -> device in one copy, the step's launches replayed as one CUDA graph "
-                        "(pa.StepGraph), output -> pinned host, stream sync; the KV cache stays resident"},
-        "gpu_launches": K * ((1 if fused else 2) + (1 if has_pairs else 0) + (1 if split else 0)),
+                "note": "per step: pinned host inputs (q, the new K/V rows, block_tables, context_lens; "
+                        "slot_mapping too for the separate calls) staged in one pinned buffer -> device in one "
+                        "copy, the step's launches replayed as one CUDA graph (pa.StepGraph), output -> pinned "
+                        "host, stream sync; the KV cache stays resident"},
+        # fused on the cooperative kernel: an append kernel, then the decode
+        "gpu_launches": K * ((2 if (not fused or decode_kernel_name(b) == "paged_decode_coop_kernel") else 1) +
+                             (1 if has_pairs else 0) + (1 if split else 0)),
         "fused_append": bool(fused),
+        "step": ("pa_decode_append (the new rows appended, then attended)" if fused else
+                 ("pa_copy_blocks + " if has_pairs else "") + "pa_reshape_and_cache + pa_decode"),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -952,7 +976,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--swap", action="store_true", help="measure swap_blocks bandwidth instead")
     ap.add_argument("--fused", action="store_true",
-                    help="run the step's reshape_and_cache inside the decode launch (pa_decode_append)")
+                    help="(the default where it applies) run the step as pa_decode_append: the new rows "
+                         "appended and attended in one call")
+    ap.add_argument("--separate", action="store_true",
+                    help="run the step as pa_reshape_and_cache followed by pa_decode")
     ap.add_argument("--clock-probe-s", type=float, default=2.0,
                     help="seconds of steps run under the clock sampler before the timed region")
     args = ap.parse_args(argv)

@@ -449,9 +449,11 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
     p.interleave = tune.interleave;
 
     // 16-bit caches whose KV heads come in groups of 8 run the CTA-cooperative
-    // kernel (8-head TMA boxes); everything else the per-warp kernel.
-    if (tune.coop && !fp8 && new_k == nullptr && head_dim == 128 && num_kv_heads % 8 == 0 &&
-        block_size % 16 == 0) {
+    // kernel (8-head TMA boxes); everything else the per-warp kernel.  With new
+    // rows to append, an append kernel writes them first and the cooperative
+    // kernel, chained by programmatic dependent launch, waits for it only
+    // before the stages that hold those rows.
+    if (tune.coop && !fp8 && head_dim == 128 && num_kv_heads % 8 == 0 && block_size % 16 == 0) {
         int cst = tune.coop_stages > 0 ? tune.coop_stages : 3;
         while (cst > 2 && pa::decode_coop_smem_bytes(G, cst, num_seqs) > static_cast<size_t>(dev.smem_optin))
             --cst;
@@ -461,6 +463,15 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
             encode_cache_map_heads8(&ck, k_cache, num_blocks, block_size, num_kv_heads, head_dim) &&
             encode_cache_map_heads8(&cv, v_cache, num_blocks, block_size, num_kv_heads, head_dim)) {
             p.stages = cst;
+            if (new_k != nullptr) {
+                const cudaError_t ea = pa::launch_append_rows(
+                    new_k, new_v, const_cast<void *>(k_cache), const_cast<void *>(v_cache), block_tables,
+                    context_lens, max_blocks_per_seq, max_context_len, block_size, num_blocks, num_seqs,
+                    static_cast<int64_t>(num_kv_heads) * head_dim * 2, err_flag, static_cast<cudaStream_t>(stream));
+                if (ea != cudaSuccess) return PA_ERR_CUDA;
+                p.new_k = p.new_v = nullptr;
+                p.defer_wait = 1;
+            }
             const cudaError_t e = pa::launch_decode_coop(p, G, kv_dtype == PA_BF16, ck, cv, dev.sms, csmem,
                                                          static_cast<cudaStream_t>(stream));
             return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

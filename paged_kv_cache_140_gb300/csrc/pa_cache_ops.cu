@@ -61,6 +61,56 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// One new token per sequence, written where the sequence's block table puts
+// position context_lens[s] - 1 (the decode step's append): the same bytes
+// reshape_and_cache writes for that slot.  Sequences with no valid token
+// (length <= 0 or above the bound) write nothing; a block id outside the pool
+// is flagged and skipped.  Like reshape_and_cache it lets the next kernel (the
+// decode, launched with programmatic dependent launch) start early.
+__global__ void __launch_bounds__(128)
+    append_rows_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                       uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                       const int32_t *__restrict__ block_tables, const int32_t *__restrict__ context_lens,
+                       int max_blocks_per_seq, int max_context_len, int block_size, int64_t num_blocks,
+                       int num_seqs, int64_t row16, int *err_flag) {
+    pdl_launch_dependents();
+    constexpr int kU = 8;
+    for (int s = blockIdx.x; s < num_seqs; s += gridDim.x) {
+        const int c = context_lens[s];
+        if (c <= 0 || c > max_context_len) continue;
+        const int pos = c - 1;
+        const int blk = block_tables[static_cast<int64_t>(s) * max_blocks_per_seq + pos / block_size];
+        if (blk < 0 || static_cast<int64_t>(blk) >= num_blocks) {
+            if (threadIdx.x == 0) report(err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
+            continue;
+        }
+        const int64_t slot = static_cast<int64_t>(blk) * block_size + pos % block_size;
+        const uint4 *ks = key + s * row16;
+        const uint4 *vs = value + s * row16;
+        uint4 *kd = k_cache + slot * row16;
+        uint4 *vd = v_cache + slot * row16;
+        for (int64_t c0 = threadIdx.x; c0 < row16; c0 += kU * blockDim.x) {
+            uint4 a[kU], b[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = c0 + u * blockDim.x;
+                if (i < row16) {
+                    a[u] = __ldg(ks + i);
+                    b[u] = __ldg(vs + i);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = c0 + u * blockDim.x;
+                if (i < row16) {
+                    kd[i] = a[u];
+                    vd[i] = b[u];
+                }
+            }
+        }
+    }
+}
+
 // Quantising variant for an e4m3 cache: each thread turns 8 elements of a
 // 16-bit row into 8 codes, code = e4m3(x / scale) with the division in fp32
 // (IEEE, round to nearest) and nearest-even rounding that saturates finite
@@ -167,6 +217,21 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
         num_slots, row16, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_rows(const void *key, const void *value, void *k_cache, void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int max_blocks_per_seq, int max_context_len, int block_size,
+                               int64_t num_blocks, int num_seqs, int64_t row_bytes, int *err_flag,
+                               cudaStream_t stream) {
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+    const int64_t gx = num_seqs < cap ? num_seqs : cap;
+    if (gx <= 0) return cudaSuccess;
+    append_rows_kernel<<<static_cast<unsigned>(gx), 128, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), block_tables, context_lens, max_blocks_per_seq, max_context_len, block_size,
+        num_blocks, num_seqs, row_bytes / 16, err_flag);
     return cudaGetLastError();
 }
 

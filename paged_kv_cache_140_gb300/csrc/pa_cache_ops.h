@@ -12,6 +12,14 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
                                      int64_t num_tokens, int64_t num_slots, int64_t row_bytes,
                                      int *err_flag, cudaStream_t stream);
 
+// One 16-bit row per sequence ([num_seqs, row_bytes]) written at the slot the
+// block table gives position context_lens[s] - 1 (the decode step's append).
+cudaError_t launch_append_rows(const void *key, const void *value, void *k_cache, void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int max_blocks_per_seq, int max_context_len, int block_size,
+                               int64_t num_blocks, int num_seqs, int64_t row_bytes, int *err_flag,
+                               cudaStream_t stream);
+
 // Quantising variant: 16-bit rows (bf16 if `bf16`) -> e4m3 codes of
 // x / scale; `row_elems` elements per token row (a multiple of 8).
 cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, void *k_cache,

@@ -154,7 +154,12 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
-    pdl_wait();
+    // Launched with programmatic dependent launch: wait for the previous kernel
+    // before reading anything it may have written - at once, or (defer_wait)
+    // only before the stages holding a sequence's last position, the one row
+    // per sequence that kernel writes.
+    const bool defer = p.defer_wait != 0;
+    if (!defer) pdl_wait();
     for (int i = threadIdx.x; i < B; i += blockDim.x) {
         int c = p.context_lens[i];
         if (c < 0 || c > p.max_context_len) {
@@ -233,6 +238,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         uint32_t uses = 0;   // slots filled so far (the empty barrier's phase follows it)
         uint32_t items = 0;  // items started (the query ring's position and phase)
         bool ok = true;
+        bool waited = !defer;
         auto take_slot = [&]() -> int {
             const int slot = islot;
             if (uses >= static_cast<uint32_t>(S)) {
@@ -280,6 +286,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                 __syncwarp();
             }
             for (int j = 0; ok && j < ic.nst; ++j) {
+                if (!waited && ic.ntok > 0 && ic.part == ic.nparts - 1 && j == ic.nst - 1) {
+                    pdl_wait();   // this stage holds the sequence's appended row
+                    waited = true;
+                }
                 const int slot = take_slot();
                 if (!ok) break;
                 uint8_t *sp = slots + static_cast<size_t>(slot) * L::kSlotBytes;
@@ -322,6 +332,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                 mbar_arrive1(&full[slot]);
             }
         }
+        if (!waited) pdl_wait();   // the CTA does not finish before the previous kernel
         __syncwarp();
         return;
     }
@@ -351,7 +362,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
             cphase ^= 1u;
         }
         const CoopMeta m = meta[slot];
-        if (m.s < 0) break;
+        if (m.s < 0) {
+            if (defer) pdl_wait();   // the CTA does not finish before the previous kernel
+            break;
+        }
         const int kvh = m.kvh0 + warp;
         const uint32_t ka = sa + warp * kHeadTile;               // my K rows, half 0
         const uint32_t va = sa + L::kVOffset + warp * kHeadTile; // my V rows, half 0

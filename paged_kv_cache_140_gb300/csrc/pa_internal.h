@@ -51,6 +51,9 @@ struct DecodeParams {
     float v_scale_w;
     int stages;                  // shared-memory slots per warp (ring depth)
     int interleave;              // 1: a CTA's warps take every nw-th item of the CTA's range
+    int defer_wait;              // cooperative kernel: the previous kernel in the stream is the
+                                 // step's append (it writes only the rows at positions ctx - 1),
+                                 // so its completion is awaited only before those rows are read
 };
 
 // Shared memory the decode kernel needs for `warps` warps with `stages`
