@@ -681,6 +681,7 @@ def run_prefill(args, world, rank, local):
                         "(staged in one pinned buffer) -> device in one copy, the step's launches replayed as one "
                         "CUDA graph (pa.StepGraph), output -> pinned host, stream sync; the KV cache stays resident"},
         "gpu_launches": K * (2 + (1 if has_pairs else 0)),
+        "step": ("pa_copy_blocks + " if has_pairs else "") + "pa_reshape_and_cache + pa_prefill",
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
