@@ -75,6 +75,9 @@ struct Shared {
     uint64_t staged[2];                  // per query tile: its output rows staged for the TMA store
     uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
     float red[2][2][2][kTile];           // [use parity][query tile][column half][row]
+    int ctx[kRankSeqs];                  // context lengths, for the longest-first order
+    int cu[kRankSeqs + 1];               // their cu_seqlens_q entries
+    int seq;                             // this CTA's sequence
     uint32_t tmem_base;
     int abort;
     int bad;
@@ -325,17 +328,51 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work unit: (sequence, KV head, pair of query tiles), heaviest first
+    // ---- work unit: (sequence, pair of query tiles, KV head).  CTAs start
+    // roughly in index order.  For up to kRankSeqs sequences the index runs
+    // over sequences by falling context length (ties by index), then pairs
+    // heaviest first, then KV heads: the longest CTAs start first and the
+    // last wave holds short ones (longest-processing-time-first list
+    // scheduling).  Larger batches run in sequence order, then KV head, then
+    // pair, heaviest first.
     const int pairs = p.pairs_per_seq;
-    const int pi = pairs - 1 - static_cast<int>(blockIdx.x % pairs);
-    const int sk = static_cast<int>(blockIdx.x / pairs);
-    const int kvh = sk % p.num_kv_heads;
-    const int s = sk / p.num_kv_heads;
+    const bool ranked = p.num_seqs <= kRankSeqs;
+    const int per_seq = pairs * p.num_kv_heads;
+    const int rank = static_cast<int>(blockIdx.x) / per_seq;
+    const int rem = static_cast<int>(blockIdx.x) % per_seq;
+    const int pi = pairs - 1 - (ranked ? rem / p.num_kv_heads : rem % pairs);
+    const int kvh = ranked ? rem % p.num_kv_heads : rem / pairs;
     const int lg = p.log2_group;
     const int G = 1 << lg;
     const int TT = kTile >> lg;             // query tokens per tile
 
-    const int q0 = __ldg(p.cu_seqlens_q + s), q1 = __ldg(p.cu_seqlens_q + s + 1);
+    int s = rank, q0, q1, ctx;
+    if (ranked) {
+        for (int j = threadIdx.x; j <= p.num_seqs; j += blockDim.x) {
+            sh.cu[j] = __ldg(p.cu_seqlens_q + j);
+            if (j < p.num_seqs) sh.ctx[j] = __ldg(p.context_lens + j);
+        }
+        __syncthreads();
+        if (static_cast<int>(threadIdx.x) < p.num_seqs) {
+            const int j = threadIdx.x, cj = sh.ctx[j];
+            int above = 0;
+#pragma unroll 8
+            for (int i = 0; i < p.num_seqs; ++i) {
+                const int ci = sh.ctx[i];
+                above += (ci > cj) | ((ci == cj) & (i < j));
+            }
+            if (above == rank) sh.seq = j;
+        }
+        __syncthreads();
+        s = sh.seq;
+        q0 = sh.cu[s];
+        q1 = sh.cu[s + 1];
+        ctx = sh.ctx[s];
+    } else {
+        q0 = __ldg(p.cu_seqlens_q + s);
+        q1 = __ldg(p.cu_seqlens_q + s + 1);
+        ctx = __ldg(p.context_lens + s);
+    }
     if (q0 < 0 || q1 < q0 || static_cast<int64_t>(q1) > p.num_tokens) {
         if (threadIdx.x == 0 && pi == 0 && kvh == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
         return;
@@ -345,7 +382,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int t0A = 2 * pi * TT;            // first token of query tile A (B follows)
     if (t0A >= ql) return;
     const bool hasB = t0A + TT < ql;
-    const int ctx = __ldg(p.context_lens + s);
 
     // Softmax threads: query tile x, row `row` (token rtok, head kvh * G + row % G),
     // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O.

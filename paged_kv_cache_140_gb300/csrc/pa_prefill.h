@@ -11,6 +11,7 @@ namespace pa {
 
 constexpr int kPrefillTile = 128;       // rows of a query tile = KV tokens per stage
 constexpr int kPrefillThreads = 608;    // 16 softmax warps, K/Q loader, MMA issuer, V loader
+constexpr int kRankSeqs = 128;          // batches up to this many sequences run longest first
 
 struct PrefillParams {
     const void *q;                  // [num_tokens, num_heads, head_dim]
@@ -29,7 +30,7 @@ struct PrefillParams {
     int64_t num_blocks;
     int max_q_len;                  // host bound on every sequence's new-token count
     int tiles_per_seq;              // query tiles per sequence: ceil(max_q_len * group / 128)
-    int pairs_per_seq;              // CTAs per (sequence, KV head): ceil(tiles_per_seq / 2)
+    int pairs_per_seq;              // query-tile pairs per sequence: ceil(tiles_per_seq / 2)
     float scale_log2;               // softmax scale * log2(e)
     int *err_flag;
 };

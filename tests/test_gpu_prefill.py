@@ -112,6 +112,36 @@ def test_prefill_gqa_edge_lengths(torch):
     assert_attention_close(out, ref, "f32", "gqa edges")
 
 
+@pytest.mark.parametrize("num_seqs", [128, 130])
+def test_prefill_many_sequences(torch, num_seqs):
+    """CTAs take sequences longest context first for batches of up to 128
+    sequences (ranked in every CTA) and in index order above that: both
+    sides of the limit, with many equal context lengths (rank ties) and
+    empty tails, give every row once."""
+    rng = np.random.default_rng(num_seqs)
+    qlen = rng.integers(0, 40, num_seqs)
+    ctx = rng.choice([40, 90, 200, 333], num_seqs)       # few distinct lengths: ties
+    b = make("prefill", prefix_lens=list(ctx - qlen), q_lens=list(qlen), num_heads=4, num_kv_heads=4,
+             head_dim=64, block_size=16)
+    ref, _, _ = oracle.prefill_step(b)
+    out, _, err = run_prefill(torch, b)
+    assert err == 0
+    assert_attention_close(out, ref, "f32", f"{num_seqs} sequences")
+
+
+def test_prefill_equal_contexts_every_order(torch):
+    """Sequences of equal context length (rank ties broken by index) and of
+    falling, rising and mixed lengths: each CTA still owns one distinct
+    (sequence, tile pair, KV head)."""
+    prefix = [300, 300, 300, 0, 600, 20, 300, 1000]
+    qlen = [40, 40, 40, 340, 5, 320, 40, 1]
+    b = make("prefill_gqa", prefix_lens=prefix, q_lens=qlen, num_heads=16, num_kv_heads=4)
+    ref, _, _ = oracle.prefill_step(b)
+    out, _, err = run_prefill(torch, b)
+    assert err == 0
+    assert_attention_close(out, ref, "f32", "ties")
+
+
 def test_prefill_of_prefix_hit_tails(torch):
     """The prefix-sharing workload: every sample's private tail prefilled over
     the shared 1000-token prompt (after copy-on-write of the partial block)."""
