@@ -246,11 +246,11 @@ def device_tensors(b, device):
 
 def decode_kernel_name(b):
     """The decode kernel pa_decode / pa_decode_append run for this batch: the
-    CTA-cooperative one for 16-bit caches whose KV heads come in groups of 8
-    (head_dim 128, block size a multiple of 16; PA_DECODE_COOP=0 turns it off),
-    else the per-warp one."""
-    coop = (os.environ.get("PA_DECODE_COOP", "1")[:1] != "0" and b.cache_dtype != "fp8"
-            and b.head_dim == 128 and b.num_kv_heads % 8 == 0 and b.block_size % 16 == 0)
+    CTA-cooperative one for 16-bit or e4m3 caches whose KV heads come in groups
+    of 8 (head_dim 128, block size a multiple of 16; PA_DECODE_COOP=0 turns it
+    off), else the per-warp one."""
+    coop = (os.environ.get("PA_DECODE_COOP", "1")[:1] != "0" and b.head_dim == 128
+            and b.num_kv_heads % 8 == 0 and b.block_size % 16 == 0)
     return "paged_decode_coop_kernel" if coop else "paged_decode_kernel"
 
 

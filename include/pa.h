@@ -187,11 +187,12 @@ pa_status pa_decode(void *out, pa_dtype out_dtype,
  * pa_decode_append -- reshape_and_cache of the step's new token fused with
  * pa_decode.
  *
- * For 16-bit caches that pa_decode runs on its cooperative kernel (head_dim
- * 128, KV heads a multiple of 8, block size a multiple of 16), a small kernel
- * writes the new rows and the decode kernel, chained to it by programmatic
- * dependent launch, waits for it only before the stages holding those rows;
- * otherwise (e4m3 caches and other shapes) one decode kernel does both.
+ * For caches that pa_decode runs on its cooperative kernel (16-bit or e4m3,
+ * head_dim 128, KV heads a multiple of 8, block size a multiple of 16), a
+ * small kernel writes the new rows (quantised for e4m3) and the decode kernel,
+ * chained to it by programmatic dependent launch, waits for it only before
+ * the stages holding those rows; otherwise (other shapes) one decode kernel
+ * does both.
  *
  * Each decode step appends one token per sequence and then attends over the
  * context including it (Page C §2.3 steps 1-3; Page A §二).  Here the new

@@ -90,7 +90,7 @@ const Tuning &tuning() {
         r.interleave = (il != nullptr && il[0] == '0') ? 0 : 1;
         const char *co = getenv("PA_DECODE_COOP");
         r.coop = (co != nullptr && co[0] == '0') ? 0 : 1;
-        r.coop_stages = env_int("PA_DECODE_COOP_STAGES", 2, 4);
+        r.coop_stages = env_int("PA_DECODE_COOP_STAGES", 2, 8);
         return r;
     }();
     return t;
@@ -162,22 +162,24 @@ bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor map over a 16-bit cache [NB * bs, Hkv, D] with its dimensions taken
-// in the order (dim, token, head): a box {64, 16, 8} is one 64-column half of
-// 16 token rows for 8 consecutive KV heads, landing as 8 per-head tiles of 16
-// rows x 128 bytes, 128-byte swizzle (the cooperative decode kernel).
+// Tensor map over a cache [NB * bs, Hkv, D] of `es`-byte elements with its
+// dimensions taken in the order (dim, token, head): a box {128 / es, 16, 8}
+// is one 128-byte column block of 16 token rows for 8 consecutive KV heads,
+// landing as 8 per-head tiles of 16 rows x 128 bytes, 128-byte swizzle (the
+// cooperative decode kernel).
 bool encode_cache_map_heads8(CUtensorMap *map, const void *cache, int64_t num_blocks, int block_size,
-                             int num_kv_heads, int head_dim) {
+                             int num_kv_heads, int head_dim, int es) {
     EncodeTiledFn fn = encode_tiled();
     if (fn == nullptr) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
                                 static_cast<cuuint64_t>(num_blocks) * block_size,
                                 static_cast<cuuint64_t>(num_kv_heads)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2,
-                                   static_cast<cuuint64_t>(head_dim) * 2};
-    const cuuint32_t box[3] = {64u, 16u, 8u};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(num_kv_heads) * head_dim * es,
+                                   static_cast<cuuint64_t>(head_dim) * es};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 16u, 8u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(cache), dims, strides, box, estr,
+    return fn(map, es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+              const_cast<void *>(cache), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -448,36 +450,44 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
     p.v_scale_w = v_scale;
     p.interleave = tune.interleave;
 
-    // 16-bit caches whose KV heads come in groups of 8 run the CTA-cooperative
-    // kernel (8-head TMA boxes); everything else the per-warp kernel.  With new
-    // rows to append, an append kernel writes them first and the cooperative
-    // kernel, chained by programmatic dependent launch, waits for it only
-    // before the stages that hold those rows.
-    if (tune.coop && !fp8 && head_dim == 128 && num_kv_heads % 8 == 0 && block_size % 16 == 0) {
-        int cst = tune.coop_stages > 0 ? tune.coop_stages : 3;
-        while (cst > 2 && pa::decode_coop_smem_bytes(G, cst, num_seqs) > static_cast<size_t>(dev.smem_optin))
+    const int kv = fp8 ? (q_dtype == PA_F16 ? 2 : 3) : (kv_dtype == PA_BF16 ? 1 : 0);
+    // Caches whose KV heads come in groups of 8 run the CTA-cooperative
+    // kernel (8-head TMA boxes); everything else the per-warp kernel.  With
+    // new rows to append, an append kernel writes them first (quantised for
+    // an e4m3 cache) and the cooperative kernel, chained by programmatic
+    // dependent launch, waits for it only before the stages that hold them.
+    if (tune.coop && head_dim == 128 && num_kv_heads % 8 == 0 && block_size % 16 == 0) {
+        // a slot holds one 16-token stage: 64 KB for 16-bit caches, 32 KB for e4m3
+        int cst = tune.coop_stages > 0 ? tune.coop_stages : (fp8 ? 6 : 3);
+        while (cst > 2 && pa::decode_coop_smem_bytes(G, es, cst, num_seqs) > static_cast<size_t>(dev.smem_optin))
             --cst;
-        const size_t csmem = pa::decode_coop_smem_bytes(G, cst, num_seqs);
+        const size_t csmem = pa::decode_coop_smem_bytes(G, es, cst, num_seqs);
         CUtensorMap ck, cv;
         if (csmem > 0 && csmem <= static_cast<size_t>(dev.smem_optin) &&
-            encode_cache_map_heads8(&ck, k_cache, num_blocks, block_size, num_kv_heads, head_dim) &&
-            encode_cache_map_heads8(&cv, v_cache, num_blocks, block_size, num_kv_heads, head_dim)) {
+            encode_cache_map_heads8(&ck, k_cache, num_blocks, block_size, num_kv_heads, head_dim, es) &&
+            encode_cache_map_heads8(&cv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, es)) {
             p.stages = cst;
             if (new_k != nullptr) {
-                const cudaError_t ea = pa::launch_append_rows(
-                    new_k, new_v, const_cast<void *>(k_cache), const_cast<void *>(v_cache), block_tables,
-                    context_lens, max_blocks_per_seq, max_context_len, block_size, num_blocks, num_seqs,
-                    static_cast<int64_t>(num_kv_heads) * head_dim * 2, err_flag, static_cast<cudaStream_t>(stream));
+                const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+                const cudaError_t ea =
+                    fp8 ? pa::launch_append_rows_fp8(new_k, new_v, const_cast<void *>(k_cache),
+                                                     const_cast<void *>(v_cache), block_tables, context_lens,
+                                                     max_blocks_per_seq, max_context_len, block_size, num_blocks,
+                                                     num_seqs, row, q_dtype == PA_BF16, k_scale, v_scale, err_flag,
+                                                     static_cast<cudaStream_t>(stream))
+                        : pa::launch_append_rows(new_k, new_v, const_cast<void *>(k_cache),
+                                                 const_cast<void *>(v_cache), block_tables, context_lens,
+                                                 max_blocks_per_seq, max_context_len, block_size, num_blocks,
+                                                 num_seqs, row * 2, err_flag, static_cast<cudaStream_t>(stream));
                 if (ea != cudaSuccess) return PA_ERR_CUDA;
                 p.new_k = p.new_v = nullptr;
                 p.defer_wait = 1;
             }
-            const cudaError_t e = pa::launch_decode_coop(p, G, kv_dtype == PA_BF16, ck, cv, dev.sms, csmem,
+            const cudaError_t e = pa::launch_decode_coop(p, G, kv, ck, cv, dev.sms, csmem,
                                                          static_cast<cudaStream_t>(stream));
             return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
         }
     }
-    const int kv = fp8 ? (q_dtype == PA_F16 ? 2 : 3) : (kv_dtype == PA_BF16 ? 1 : 0);
     cudaError_t e = pa::launch_decode(p, head_dim, G, kv, tk, tv, dev.sms, warps,
                                       smem_used, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

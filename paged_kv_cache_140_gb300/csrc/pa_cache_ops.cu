@@ -111,10 +111,23 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// 8 elements of a 16-bit row -> 8 e4m3 codes, code = e4m3(x / scale) with
+// the division in fp32 (IEEE, round to nearest) and nearest-even rounding that
+// saturates finite values at +-448.
+template <bool BF16>
+__device__ __forceinline__ uint2 quant8(uint4 w, float sc) {
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t code[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = Half2x<BF16>::to_float2(in[k]);
+        code[k] = f32x2_to_e4m3x2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc));
+    }
+    return make_uint2(code[0] | (code[1] << 16), code[2] | (code[3] << 16));
+}
+
 // Quantising variant for an e4m3 cache: each thread turns 8 elements of a
-// 16-bit row into 8 codes, code = e4m3(x / scale) with the division in fp32
-// (IEEE, round to nearest) and nearest-even rounding that saturates finite
-// values at +-448.
+// 16-bit row into 8 codes (quant8).
 template <bool BF16>
 __global__ void __launch_bounds__(128)
     reshape_and_cache_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
@@ -124,16 +137,6 @@ __global__ void __launch_bounds__(128)
                                  int *err_flag) {
     pdl_launch_dependents();
     const int64_t i = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
-    auto quant8 = [](uint4 w, float sc) {
-        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-        uint32_t code[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = Half2x<BF16>::to_float2(in[k]);
-            code[k] = f32x2_to_e4m3x2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc));
-        }
-        return make_uint2(code[0] | (code[1] << 16), code[2] | (code[3] << 16));
-    };
     for (int64_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
         const int64_t slot = slot_mapping[t];
         if (slot < 0) continue;
@@ -144,8 +147,37 @@ __global__ void __launch_bounds__(128)
         for (int64_t c = i; c < row8; c += static_cast<int64_t>(gridDim.y) * blockDim.x) {
             const uint4 a = __ldg(key + t * row8 + c);
             const uint4 b = __ldg(value + t * row8 + c);
-            k_cache[slot * row8 + c] = quant8(a, k_scale);
-            v_cache[slot * row8 + c] = quant8(b, v_scale);
+            k_cache[slot * row8 + c] = quant8<BF16>(a, k_scale);
+            v_cache[slot * row8 + c] = quant8<BF16>(b, v_scale);
+        }
+    }
+}
+
+// The decode step's append into an e4m3 cache: append_rows_kernel's slot
+// rule, the codes of reshape_and_cache_fp8_kernel.
+template <bool BF16>
+__global__ void __launch_bounds__(128)
+    append_rows_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                           uint2 *__restrict__ k_cache, uint2 *__restrict__ v_cache,
+                           const int32_t *__restrict__ block_tables, const int32_t *__restrict__ context_lens,
+                           int max_blocks_per_seq, int max_context_len, int block_size, int64_t num_blocks,
+                           int num_seqs, int64_t row8, float k_scale, float v_scale, int *err_flag) {
+    pdl_launch_dependents();
+    for (int s = blockIdx.x; s < num_seqs; s += gridDim.x) {
+        const int c = context_lens[s];
+        if (c <= 0 || c > max_context_len) continue;
+        const int pos = c - 1;
+        const int blk = block_tables[static_cast<int64_t>(s) * max_blocks_per_seq + pos / block_size];
+        if (blk < 0 || static_cast<int64_t>(blk) >= num_blocks) {
+            if (threadIdx.x == 0) report(err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
+            continue;
+        }
+        const int64_t slot = static_cast<int64_t>(blk) * block_size + pos % block_size;
+        for (int64_t i = threadIdx.x; i < row8; i += blockDim.x) {
+            const uint4 a = __ldg(key + s * row8 + i);
+            const uint4 b = __ldg(value + s * row8 + i);
+            k_cache[slot * row8 + i] = quant8<BF16>(a, k_scale);
+            v_cache[slot * row8 + i] = quant8<BF16>(b, v_scale);
         }
     }
 }
@@ -232,6 +264,22 @@ cudaError_t launch_append_rows(const void *key, const void *value, void *k_cache
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint4 *>(k_cache),
         static_cast<uint4 *>(v_cache), block_tables, context_lens, max_blocks_per_seq, max_context_len, block_size,
         num_blocks, num_seqs, row_bytes / 16, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_rows_fp8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int max_blocks_per_seq, int max_context_len, int block_size,
+                                   int64_t num_blocks, int num_seqs, int64_t row_elems, bool bf16,
+                                   float k_scale, float v_scale, int *err_flag, cudaStream_t stream) {
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+    const int64_t gx = num_seqs < cap ? num_seqs : cap;
+    if (gx <= 0) return cudaSuccess;
+    auto kern = bf16 ? append_rows_fp8_kernel<true> : append_rows_fp8_kernel<false>;
+    kern<<<static_cast<unsigned>(gx), 128, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint2 *>(k_cache),
+        static_cast<uint2 *>(v_cache), block_tables, context_lens, max_blocks_per_seq, max_context_len, block_size,
+        num_blocks, num_seqs, row_elems / 8, k_scale, v_scale, err_flag);
     return cudaGetLastError();
 }
 

@@ -20,6 +20,14 @@ cudaError_t launch_append_rows(const void *key, const void *value, void *k_cache
                                int64_t num_blocks, int num_seqs, int64_t row_bytes, int *err_flag,
                                cudaStream_t stream);
 
+// The same append into an e4m3 cache: 16-bit rows ([num_seqs, row_elems],
+// bf16 if `bf16`) quantised as by launch_reshape_and_cache_fp8.
+cudaError_t launch_append_rows_fp8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int max_blocks_per_seq, int max_context_len, int block_size,
+                                   int64_t num_blocks, int num_seqs, int64_t row_elems, bool bf16,
+                                   float k_scale, float v_scale, int *err_flag, cudaStream_t stream);
+
 // Quantising variant: 16-bit rows (bf16 if `bf16`) -> e4m3 codes of
 // x / scale; `row_elems` elements per token row (a multiple of 8).
 cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, void *k_cache,

@@ -1,5 +1,5 @@
-// Paged decode attention, CTA-cooperative variant (16-bit caches, KV-head
-// count a multiple of 8, head_dim 128, block_size a multiple of 16).
+// Paged decode attention, CTA-cooperative variant (16-bit or e4m3 caches,
+// KV-head count a multiple of 8, head_dim 128, block_size a multiple of 16).
 //
 // Computes what the per-warp kernel in pa_decode.cu computes - softmax(q K^T *
 // scale) V over each sequence's context_lens[s] cached tokens, reached through
@@ -8,17 +8,20 @@
 // merged in order by the same merge kernel - with a different way of moving
 // the cache:
 //  * A CTA works on items (sequence, partition, group of 8 KV heads).  One
-//    producer warp brings each 16-token stage in with one TMA box per 64-column
-//    half of K and of V covering all 8 heads ({64, 16 rows, 8 heads}: 16 KB,
-//    the heads' 16 rows of one physical block, 2 KB contiguous per token),
-//    instead of one 2 KB box per head and half.  The tensor map orders its
-//    dimensions (dim, token, head) so that each head's 16 rows land
-//    contiguously with the 128-byte swizzle, as the per-warp kernel's do.
+//    producer warp brings each 16-token stage in with one TMA box per 128-byte
+//    column block of K and of V covering all 8 heads ({64, 16 rows, 8 heads}
+//    for 16-bit caches, two per row; {128, 16, 8} for e4m3, one per row: 16 KB,
+//    the heads' 16 rows of one physical block), instead of one 2 KB box per
+//    head and column block.  The tensor map orders its dimensions (dim, token,
+//    head) so that each head's 16 rows land contiguously with the 128-byte
+//    swizzle, as the per-warp kernel's do.
 //  * Eight consumer warps each take one head of the group and run the same
 //    warp-level MMA math on their slice of the shared stage: QK with the 16
 //    tokens as M and the G query heads as N (padded to 8), online softmax in
 //    base 2 with lazy rescaling, PV with the weights as a 16-bit high part
-//    plus residual.
+//    plus residual.  e4m3 codes are widened to f16 pairs in registers (every
+//    e4m3 value is exact in f16) and multiplied as f16, the query rounded to
+//    f16; the per-tensor scales are folded into the logit scale and the output.
 //  * Slots are CTA-wide: `full` completes when a stage's copies land, `empty`
 //    when all eight consumers are done with it; every wait is bounded and a
 //    timeout sets PA_FLAG_TIMEOUT.  An item's query rows go to a 2-entry ring
@@ -41,9 +44,11 @@ constexpr int kCoopThreads = (kGroupHeads + 1) * 32;
 constexpr int kRow = 128;                         // bytes of one swizzled 64-element row half
 constexpr int kHeadTile = kStageTokens * kRow;    // one head's 16 rows of one half: 2 KB
 
-template <int D, int G>
+// ES = bytes per cache element (2: f16/bf16, 1: e4m3).
+template <int D, int G, int ES>
 struct CoopLayout {
-    static constexpr int kHalves = D / 64;
+    static constexpr int kHalves = D * ES / kRow;                   // 128-byte column blocks per row
+    static constexpr int kBoxElems = kRow / ES;                     // elements per box row
     static constexpr int kBoxBytes = kGroupHeads * kHeadTile;      // 16 KB
     static constexpr int kKBytes = kHalves * kBoxBytes;
     static constexpr int kVOffset = kKBytes;
@@ -99,13 +104,18 @@ struct CoopCursor {
     }
 };
 
-template <int D, int G, bool BF16>
+// KV: 0 = f16 cache and query, 1 = bf16 cache and query, 2 / 3 = e4m3 cache
+// with an f16 / bf16 query (f16 MMAs).
+template <int D, int G, int KV>
 __global__ void __launch_bounds__(kCoopThreads, 1)
     paged_decode_coop_kernel(const __grid_constant__ DecodeParams p,
                              const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v) {
     static_assert(D == 128, "the cooperative kernel is built for head_dim 128");
-    using L = CoopLayout<D, G>;
+    constexpr bool kFp8 = KV >= 2;
+    constexpr bool BF16 = KV == 1;                 // MMA operand type
+    constexpr bool kQBf16 = KV == 1 || KV == 3;    // query type
+    using L = CoopLayout<D, G, kFp8 ? 1 : 2>;
     using Cvt = Half2x<BF16>;
     constexpr int KS = L::kSteps;
     constexpr int MT = L::kSteps;
@@ -312,9 +322,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                         const int z = id * bs + (tok0 % bs);
 #pragma unroll
                         for (int h = 0; h < L::kHalves; ++h) {
-                            tma_load_3d(sp + h * L::kBoxBytes, &tmap_k, &full[slot], h * 64, z, kvh0, policy);
-                            tma_load_3d(sp + L::kVOffset + h * L::kBoxBytes, &tmap_v, &full[slot], h * 64, z,
-                                        kvh0, policy);
+                            tma_load_3d(sp + h * L::kBoxBytes, &tmap_k, &full[slot], h * L::kBoxElems, z, kvh0,
+                                        policy);
+                            tma_load_3d(sp + L::kVOffset + h * L::kBoxBytes, &tmap_v, &full[slot],
+                                        h * L::kBoxElems, z, kvh0, policy);
                         }
                     }
                 }
@@ -381,10 +392,28 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
             }
             const uint32_t *qw =
                 reinterpret_cast<const uint32_t *>(qbuf + qi * L::kQBytes) + warp * (G * D / 2);
+            if constexpr (!kFp8) {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                qf[ks][0] = g < G ? qw[(g * D + ks * 16 + 2 * t) >> 1] : 0u;
-                qf[ks][1] = g < G ? qw[(g * D + ks * 16 + 2 * t + 8) >> 1] : 0u;
+                for (int ks = 0; ks < KS; ++ks) {
+                    qf[ks][0] = g < G ? qw[(g * D + ks * 16 + 2 * t) >> 1] : 0u;
+                    qf[ks][1] = g < G ? qw[(g * D + ks * 16 + 2 * t + 8) >> 1] : 0u;
+                }
+            } else {
+                // Dims in the order the widened K fragments arrive (see QK):
+                // step 2kc+hl takes dims 32kc + 4t + 2hl (+1) and the same + 16.
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int d = 32 * (ks >> 1) + 4 * t + 2 * (ks & 1);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        uint32_t w = g < G ? qw[(g * D + d + 16 * k) >> 1] : 0u;
+                        if constexpr (kQBf16) {
+                            const float2 f = Half2x<true>::to_float2(w);
+                            w = pack2<false>(f.x, f.y);
+                        }
+                        qf[ks][k] = w;
+                    }
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -403,12 +432,28 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         {
             const int j = lane >> 3, r = lane & 7;
             const int tok = r + 8 * (j & 1);
+            if constexpr (!kFp8) {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int ch = 2 * ks + (j >> 1);
-                uint32_t a[4];
-                ldsm_x4(a, ka + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
-                mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int ch = 2 * ks + (j >> 1);
+                    uint32_t a[4];
+                    ldsm_x4(a, ka + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
+                    mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
+                }
+            } else {
+                // ldmatrix on the byte rows viewed as 16-bit: each register holds
+                // four consecutive dims of one token, widened to two f16 pairs;
+                // each 32-dim chunk feeds two MMAs (dims permuted alike in q).
+#pragma unroll
+                for (int kc = 0; kc < D / 32; ++kc) {
+                    const int ch = 2 * kc + (j >> 1);
+                    uint32_t a[4], lo[4], hi[4];
+                    ldsm_x4(a, ka + tok * kRow + ((ch ^ r) << 4));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(a[i], lo[i], hi[i]);
+                    mma_16816<false>(c[0], lo, qf[2 * kc][0], qf[2 * kc][1]);
+                    mma_16816<false>(c[1], hi, qf[2 * kc + 1][0], qf[2 * kc + 1][1]);
+                }
             }
         }
         float x[4];
@@ -488,13 +533,32 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         {
             const int j = lane >> 3, r = lane & 7;
             const int tok = r + 8 * (j >> 1);
+            if constexpr (!kFp8) {
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const int ch = 2 * mt + (j & 1);
-                uint32_t a[4];
-                ldsm_x4_trans(a, va + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
-                mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
-                mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int ch = 2 * mt + (j & 1);
+                    uint32_t a[4];
+                    ldsm_x4_trans(a, va + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
+                    mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
+                    mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                }
+            } else {
+                // Transposed ldmatrix of the byte rows viewed as 16-bit gives
+                // (tokens 2t, 2t+1) x (dims 2g, 2g+1); regroup the bytes so each
+                // f16 pair is one dim over two tokens: even dims feed acc[2vc],
+                // odd dims acc[2vc+1].
+#pragma unroll
+                for (int vc = 0; vc < D / 32; ++vc) {
+                    const int ch = 2 * vc + (j & 1);
+                    uint32_t a[4], ev[4], od[4];
+                    ldsm_x4_trans(a, va + tok * kRow + ((ch ^ r) << 4));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(prmt(a[i], 0x3120u), ev[i], od[i]);
+                    mma_16816<false>(acc[2 * vc], ev, bhi[0], bhi[1]);
+                    mma_16816<false>(acc[2 * vc], ev, blo[0], blo[1]);
+                    mma_16816<false>(acc[2 * vc + 1], od, bhi[0], bhi[1]);
+                    mma_16816<false>(acc[2 * vc + 1], od, blo[0], blo[1]);
+                }
             }
         }
         // my reads (and zeroing) of the slot are done: it may be refilled once all
@@ -518,10 +582,20 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                 if (h < G) {
                     const float s = (final_out ? (lt[e] > 0.f ? 1.f / lt[e] : 0.f) : 1.f) * p.v_scale;
                     float *orow = obuf + h * L::kOStride;
+                    if constexpr (!kFp8) {
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        orow[mt * 16 + g] = acc[mt][e] * s;
-                        orow[mt * 16 + g + 8] = acc[mt][2 + e] * s;
+                        for (int mt = 0; mt < MT; ++mt) {
+                            orow[mt * 16 + g] = acc[mt][e] * s;
+                            orow[mt * 16 + g + 8] = acc[mt][2 + e] * s;
+                        }
+                    } else {
+#pragma unroll
+                        for (int vc = 0; vc < D / 32; ++vc) {
+                            orow[32 * vc + 2 * g] = acc[2 * vc][e] * s;
+                            orow[32 * vc + 16 + 2 * g] = acc[2 * vc][2 + e] * s;
+                            orow[32 * vc + 2 * g + 1] = acc[2 * vc + 1][e] * s;
+                            orow[32 * vc + 16 + 2 * g + 1] = acc[2 * vc + 1][2 + e] * s;
+                        }
                     }
                 }
             }
@@ -552,10 +626,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
     }
 }
 
-template <int G, bool BF16>
+template <int G, int KV>
 cudaError_t launch_coop_t(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
                           size_t smem, cudaStream_t stream) {
-    auto kern = paged_decode_coop_kernel<128, G, BF16>;
+    auto kern = paged_decode_coop_kernel<128, G, KV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(grid), dim3(kCoopThreads), smem, stream, p, tk, tv);
@@ -563,9 +637,9 @@ cudaError_t launch_coop_t(const DecodeParams &p, const CUtensorMap &tk, const CU
     return launch_decode_merge(p, 128, G, stream);
 }
 
-template <int G>
+template <int G, int ES>
 size_t coop_smem_for(int stages, int num_seqs) {
-    using L = CoopLayout<128, G>;
+    using L = CoopLayout<128, G, ES>;
     return 1024 + static_cast<size_t>(stages) * (L::kSlotBytes + sizeof(CoopMeta) + 16) +
            static_cast<size_t>(kQRing) * (L::kQBytes + 16) +
            kGroupHeads * L::kOBytes + 32 * 4 + 4 * static_cast<size_t>(num_seqs) +
@@ -574,27 +648,36 @@ size_t coop_smem_for(int stages, int num_seqs) {
 
 }  // namespace
 
-size_t decode_coop_smem_bytes(int group, int stages, int num_seqs) {
+size_t decode_coop_smem_bytes(int group, int es, int stages, int num_seqs) {
+    if (es != 1 && es != 2) return 0;
     switch (group) {
-        case 1: return coop_smem_for<1>(stages, num_seqs);
-        case 2: return coop_smem_for<2>(stages, num_seqs);
-        case 4: return coop_smem_for<4>(stages, num_seqs);
-        case 8: return coop_smem_for<8>(stages, num_seqs);
+        case 1: return es == 1 ? coop_smem_for<1, 1>(stages, num_seqs) : coop_smem_for<1, 2>(stages, num_seqs);
+        case 2: return es == 1 ? coop_smem_for<2, 1>(stages, num_seqs) : coop_smem_for<2, 2>(stages, num_seqs);
+        case 4: return es == 1 ? coop_smem_for<4, 1>(stages, num_seqs) : coop_smem_for<4, 2>(stages, num_seqs);
+        case 8: return es == 1 ? coop_smem_for<8, 1>(stages, num_seqs) : coop_smem_for<8, 2>(stages, num_seqs);
         default: return 0;
     }
 }
 
-cudaError_t launch_decode_coop(const DecodeParams &p, int group, bool bf16, const CUtensorMap &tk,
+template <int G>
+cudaError_t launch_coop_g(const DecodeParams &p, int kv, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
+                          size_t smem, cudaStream_t stream) {
+    switch (kv) {
+        case 0: return launch_coop_t<G, 0>(p, tk, tv, grid, smem, stream);
+        case 1: return launch_coop_t<G, 1>(p, tk, tv, grid, smem, stream);
+        case 2: return launch_coop_t<G, 2>(p, tk, tv, grid, smem, stream);
+        case 3: return launch_coop_t<G, 3>(p, tk, tv, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode_coop(const DecodeParams &p, int group, int kv, const CUtensorMap &tk,
                                const CUtensorMap &tv, int grid, size_t smem, cudaStream_t stream) {
     switch (group) {
-        case 1: return bf16 ? launch_coop_t<1, true>(p, tk, tv, grid, smem, stream)
-                            : launch_coop_t<1, false>(p, tk, tv, grid, smem, stream);
-        case 2: return bf16 ? launch_coop_t<2, true>(p, tk, tv, grid, smem, stream)
-                            : launch_coop_t<2, false>(p, tk, tv, grid, smem, stream);
-        case 4: return bf16 ? launch_coop_t<4, true>(p, tk, tv, grid, smem, stream)
-                            : launch_coop_t<4, false>(p, tk, tv, grid, smem, stream);
-        case 8: return bf16 ? launch_coop_t<8, true>(p, tk, tv, grid, smem, stream)
-                            : launch_coop_t<8, false>(p, tk, tv, grid, smem, stream);
+        case 1: return launch_coop_g<1>(p, kv, tk, tv, grid, smem, stream);
+        case 2: return launch_coop_g<2>(p, kv, tk, tv, grid, smem, stream);
+        case 4: return launch_coop_g<4>(p, kv, tk, tv, grid, smem, stream);
+        case 8: return launch_coop_g<8>(p, kv, tk, tv, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
 }

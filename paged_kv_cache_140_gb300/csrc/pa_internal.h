@@ -61,12 +61,14 @@ struct DecodeParams {
 size_t decode_smem_bytes(int head_dim, int group, int elem_bytes, int warps, int stages,
                          int num_seqs);
 
-// The CTA-cooperative decode kernel (pa_decode_coop.cu): 16-bit caches, head
-// dim 128, KV heads a multiple of 8, block size a multiple of 16; `tk`/`tv`
-// map each cache as (dim, token, head) with {64, 16, 8} boxes.  Launches the
-// merge kernel after it when sequences are split.
-size_t decode_coop_smem_bytes(int group, int stages, int num_seqs);
-cudaError_t launch_decode_coop(const DecodeParams &p, int group, bool bf16, const CUtensorMap &tk,
+// The CTA-cooperative decode kernel (pa_decode_coop.cu): 16-bit or e4m3
+// caches (`es` 2 or 1 bytes per element), head dim 128, KV heads a multiple of
+// 8, block size a multiple of 16; `tk`/`tv` map each cache as (dim, token,
+// head) with {128 bytes, 16, 8} boxes.  `kv` as for launch_decode (0 f16,
+// 1 bf16, 2/3 e4m3 with an f16/bf16 query).  Launches the merge kernel after
+// it when sequences are split.
+size_t decode_coop_smem_bytes(int group, int es, int stages, int num_seqs);
+cudaError_t launch_decode_coop(const DecodeParams &p, int group, int kv, const CUtensorMap &tk,
                                const CUtensorMap &tv, int grid, size_t smem, cudaStream_t stream);
 
 // The merge of split sequences' partial states (pa_decode.cu), chained with

@@ -58,6 +58,8 @@ CASES = [
     ("tiny", dict(num_heads=8, num_kv_heads=2), None),
     ("7b", dict(num_seqs=6, block_size=32), None),
     ("gqa", dict(num_seqs=3, ctx_cap=3000, block_size=8), 128),
+    ("gqa", dict(num_seqs=2, ctx_cap=9000, cache_dtype="fp8"), None),
+    ("13b", dict(num_seqs=8, block_size=8, cache_dtype="fp8"), 64),
 ]
 
 

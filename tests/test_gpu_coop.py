@@ -1,6 +1,7 @@
-"""GPU checks of the CTA-cooperative decode kernel (16-bit caches whose KV
-heads come in groups of 8, head_dim 128, block size a multiple of 16): parity
-with the oracle for every group size, including G = 8 (two-deep ring), and bit
+"""GPU checks of the CTA-cooperative decode kernel (16-bit or e4m3 caches
+whose KV heads come in groups of 8, head_dim 128, block size a multiple of
+16): parity with the oracle for every group size, including G = 8 (shallower
+ring), both query types over an e4m3 cache, and, for 16-bit caches, bit
 equality with the per-warp kernel, which a child process selects with
 PA_DECODE_COOP=0."""
 import os
@@ -61,3 +62,38 @@ def test_cooperative_and_per_warp_kernels_agree_bit_for_bit(tmp_path, hq, hkv, d
         assert r.returncode == 0, r.stderr[-2000:]
         outs[coop] = np.load(path)
     assert np.array_equal(outs["1"], outs["0"])
+
+
+FP8_CASES = [   # (Hq, Hkv, query dtype, block size)
+    (8, 8, "f16", 16),
+    (16, 8, "bf16", 16),
+    (32, 8, "f16", 32),
+    (64, 8, "bf16", 16),
+    (48, 24, "bf16", 64),
+    (40, 40, "f16", 16),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,qdt,bs", FP8_CASES, ids=[f"{c[0]}x{c[1]}-{c[2]}-bs{c[3]}" for c in FP8_CASES])
+def test_cooperative_kernel_fp8_matches_oracle(hq, hkv, qdt, bs):
+    """e4m3 cache: 8-head boxes of 128 codes per row, codes widened to f16 in
+    registers; unused slots hold NaN codes."""
+    b = W.make_batch("7b", num_seqs=6, ctx_cap=1500, num_heads=hq, num_kv_heads=hkv, dtype=qdt, block_size=bs,
+                     cache_dtype="fp8")
+    ref, _, _ = oracle.decode_step(b)
+    out, _, flag = run_step(b)
+    assert flag == 0
+    assert_attention_close(out, ref, "f32", f"coop fp8 {hq}/{hkv} {qdt} bs {bs}")
+
+
+@pytest.mark.parametrize("P", [16, 48, 0])
+def test_cooperative_kernel_fp8_ragged_lengths(P):
+    """Empty, one-token and stage-boundary contexts with small partitions
+    (ragged last stages, many split sequences) over an e4m3 cache."""
+    b = W.make_batch("13b", context_lens=[0, 1, 15, 16, 17, 31, 33, 2048, 0, 100], cache_dtype="fp8")
+    ref, _, _ = oracle.decode_step(b)
+    out, _, flag = run_step(b, partition_size=P)
+    assert flag == 0
+    assert_attention_close(out, ref, "f32", f"coop fp8 ragged P={P}")
+    o = out.cpu().numpy()
+    assert np.all(o[0] == 0) and np.all(o[8] == 0)
