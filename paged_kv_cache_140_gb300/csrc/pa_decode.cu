@@ -9,10 +9,11 @@
 // partitions whose partial softmax states are merged in partition order (the
 // "partial accumulate, then merge" v2 kernel of the same page, §4.1).
 //
-// This per-warp kernel serves e4m3 caches, the fused append, head_dim 64,
-// block size 8 and KV-head counts that are not a multiple of 8; 16-bit caches
-// with KV heads in groups of 8 run the CTA-cooperative kernel of
-// pa_decode_coop.cu (8-head TMA boxes), which shares this file's merge kernel.
+// This per-warp kernel serves head_dim 64, block size 8 and KV-head counts
+// that are not a multiple of 8 (16-bit or e4m3 caches, with or without the
+// fused append); caches with KV heads in groups of 8 run the CTA-cooperative
+// kernel of pa_decode_coop.cu (8-head TMA boxes), which shares this file's
+// merge kernel.
 //
 // How (GB300 design, not the pages' A100 kernels):
 //  * Persistent grid, one CTA per SM, every warp an independent pipeline.
