@@ -122,3 +122,45 @@ def test_argument_checks_return_before_touching_a_gpu(lib):
     misaligned = ctypes.c_void_p(0x1008)
     assert lib.pa_copy_blocks(misaligned, misaligned, misaligned, 2, 64, 16, 4, 64, 1, nul, nul) == \
         L.PA_ERR_INVALID_ARG
+
+
+def declared_prototypes():
+    """{name: (return type, [parameter types])} from include/*.h, comments removed."""
+    protos = {}
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h), encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = "\n".join(line for line in src.splitlines() if not line.lstrip().startswith("#"))
+        for m in re.finditer(r"([A-Za-z_][\w\s\*]*?)\b(pa_\w+)\s*\(([^;{]*?)\)\s*;", src):
+            ret, name, params = " ".join(m.group(1).split()), m.group(2), m.group(3)
+            params = [" ".join(p.split()) for p in params.split(",")] if params.strip() not in ("", "void") else []
+            protos[name] = (ret, params)
+    return protos
+
+
+def _ctype_of(decl: str):
+    if "*" in decl:
+        return ctypes.c_char_p if decl.startswith("const char") else ctypes.c_void_p
+    base = decl.split()[0] if decl.split()[0] != "const" else decl.split()[1]
+    return {"int": ctypes.c_int, "int32_t": ctypes.c_int, "pa_status": ctypes.c_int, "pa_dtype": ctypes.c_int,
+            "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "float": ctypes.c_float}[base]
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature has the header prototype's arity and types, so
+    no argument is shifted or truncated on the way into the library."""
+    from paged_kv_cache_140_gb300 import _lib
+    protos = declared_prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, (ret, params) in protos.items():
+        res, args = _lib.SIGNATURES[name]
+        assert len(args) == len(params), f"{name}: {len(args)} bound, {len(params)} declared"
+        for i, (a, decl) in enumerate(zip(args, params)):
+            want = _ctype_of(decl)
+            pointer_ok = want is ctypes.c_void_p and issubclass(a, ctypes._Pointer)
+            assert a is want or pointer_ok, f"{name} argument {i} ({decl}): bound as {a.__name__}"
+        want = _ctype_of(ret + (" *" if ret.endswith("*") else ""))
+        assert res is want or (res is ctypes.c_int and want is ctypes.c_int), f"{name} returns {ret}"
