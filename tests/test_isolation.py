@@ -45,3 +45,12 @@ def test_oracle_uses_nothing_of_the_cuda_path():
         assert not inc.search(open(f, encoding="utf-8").read()), f
     for f in _files(os.path.join(ROOT, "oracle"), (".py",)):
         assert not imp.search(open(f, encoding="utf-8").read()), f
+
+
+def test_missing_library_fails_loudly():
+    """Without the built CUDA library a call raises; there is no fallback."""
+    code = ("import sys, paged_kv_cache_140_gb300._lib as L, paged_kv_cache_140_gb300._build as B; "
+            "B.LIB_PATH = '/nonexistent/libpagedattn.so'; L._lib = None\n"
+            "try:\n    L.load()\nexcept ImportError as e:\n    print('raised', e); sys.exit(0)\nsys.exit(1)")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "is missing" in r.stdout, r.stdout + r.stderr
