@@ -97,3 +97,26 @@ def test_cooperative_kernel_fp8_ragged_lengths(P):
     assert_attention_close(out, ref, "f32", f"coop fp8 ragged P={P}")
     o = out.cpu().numpy()
     assert np.all(o[0] == 0) and np.all(o[8] == 0)
+
+
+def test_cooperative_kernel_fp8_bad_block_id_is_flagged_and_isolated():
+    """A block id outside the pool in an e4m3 cache is skipped and flagged;
+    the other sequences are untouched and the affected row stays finite."""
+    import paged_kv_cache_140_gb300 as pa
+    b = W.make_batch("13b", num_seqs=8, cache_dtype="fp8")
+    s_bad = int(np.argmax(b.context_lens))
+    b.block_tables[s_bad, 0] = b.num_blocks + 5
+    out, _, flag = run_step(b)
+    assert flag & pa.FLAG_BAD_BLOCK_ID
+    keep = [s for s in range(8) if s != s_bad]
+    ref, _, _ = oracle.decode_step(W.subset_batch(b, keep))
+    assert_attention_close(out[keep], ref, "f32", "unaffected sequences, fp8")
+    assert np.all(np.isfinite(out[s_bad].float().cpu().numpy()))
+
+
+def test_cooperative_kernel_fp8_is_bitwise_reproducible():
+    b = W.make_batch("gqa", num_seqs=2, ctx_cap=9000, cache_dtype="fp8")
+    a, _, fa = run_step(b)
+    c, _, fc = run_step(b)
+    assert fa == 0 and fc == 0
+    assert np.array_equal(a.cpu().numpy().view(np.uint32), c.cpu().numpy().view(np.uint32))
