@@ -27,7 +27,9 @@
 //    timeout sets PA_FLAG_TIMEOUT.  An item's query rows go to a 2-entry ring
 //    of their own (read once, at the item's first stage), so slots hold only
 //    K and V and a 3-deep ring fits for groups of up to 4 query heads per KV
-//    head.  The producer also owns the work cursor and the block-table reads,
+//    head.  An e4m3 slot holds two consecutive stages of one item (64 KB, as
+//    a 16-bit slot), consumed under one softmax update, so that each consumer's
+//    chain of dependent steps covers 32 tokens of 1-byte codes.  The producer also owns the work cursor and the block-table reads,
 //    so the consumers' loop holds only the math.
 #include "pa_decode_common.cuh"
 #include "pa_device.cuh"
@@ -45,15 +47,17 @@ constexpr int kRow = 128;                         // bytes of one swizzled 64-el
 constexpr int kHeadTile = kStageTokens * kRow;    // one head's 16 rows of one half: 2 KB
 
 // ES = bytes per cache element (2: f16/bf16, 1: e4m3).
-template <int D, int G, int ES>
+template <int D, int G, int ES, int SUB = (ES == 1 ? 2 : 1)>
 struct CoopLayout {
+    static constexpr int kSub = SUB;                                // stages per slot
     static constexpr int kHalves = D * ES / kRow;                   // 128-byte column blocks per row
     static constexpr int kBoxElems = kRow / ES;                     // elements per box row
     static constexpr int kBoxBytes = kGroupHeads * kHeadTile;      // 16 KB
     static constexpr int kKBytes = kHalves * kBoxBytes;
     static constexpr int kVOffset = kKBytes;
     static constexpr int kQBytes = kGroupHeads * G * D * 2;         // the group's query rows
-    static constexpr int kSlotBytes = 2 * kKBytes;                  // K and V of one stage
+    static constexpr int kStageBytes = 2 * kKBytes;                 // K and V of one stage
+    static constexpr int kSlotBytes = SUB * kStageBytes;
     static constexpr int kOStride = D + 4;
     static constexpr int kOBytes = G * kOStride * 4;                // per consumer warp
     static constexpr int kSteps = D / 16;
@@ -61,8 +65,8 @@ struct CoopLayout {
 };
 
 struct CoopMeta {
-    int s, kvh0, part, j;        // s < 0: no more work
-    int nst, nparts, mask, pad;
+    int s, kvh0, part, j;        // s < 0: no more work; j = the slot's first stage
+    int nst, nparts, mask, pad;  // mask bit 16 * hs + r: row r of the slot's stage hs is valid
 };
 
 // The items' query rows sit in a ring of their own (kQRing entries, one per
@@ -116,6 +120,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
     constexpr bool BF16 = KV == 1;                 // MMA operand type
     constexpr bool kQBf16 = KV == 1 || KV == 3;    // query type
     using L = CoopLayout<D, G, kFp8 ? 1 : 2>;
+    constexpr int SUB = L::kSub;
     using Cvt = Half2x<BF16>;
     constexpr int KS = L::kSteps;
     constexpr int MT = L::kSteps;
@@ -295,37 +300,50 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                 ++items;
                 __syncwarp();
             }
-            for (int j = 0; ok && j < ic.nst; ++j) {
-                if (!waited && ic.ntok > 0 && ic.part == ic.nparts - 1 && j == ic.nst - 1) {
-                    pdl_wait();   // this stage holds the sequence's appended row
+            for (int j = 0; ok && j < ic.nst; j += SUB) {
+                if (!waited && ic.ntok > 0 && ic.part == ic.nparts - 1 && j + SUB >= ic.nst) {
+                    pdl_wait();   // this slot holds the sequence's appended row
                     waited = true;
                 }
                 const int slot = take_slot();
                 if (!ok) break;
                 uint8_t *sp = slots + static_cast<size_t>(slot) * L::kSlotBytes;
-                const int tok0 = ic.part * P + j * kStageTokens;
-                const int n = ic.ntok > 0 ? min(kStageTokens, ic.ntok - j * kStageTokens) : 0;
-                int mask = n > 0 ? static_cast<int>((1u << n) - 1u) : 0;
-                const int id = __shfl_sync(kFull, bid, (tok0 / bs - fb) & 31);
-                const bool load = n > 0 && id >= 0 && static_cast<int64_t>(id) < p.num_blocks;
-                if (n > 0 && !load) {
-                    mask = 0;
-                    if (lane == 0) report(p.err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
+                uint32_t mask_all = 0, bytes = 0;
+                int zs[SUB];
+                bool loads[SUB];
+#pragma unroll
+                for (int hs = 0; hs < SUB; ++hs) {
+                    const int jj = j + hs;
+                    const int tok0 = ic.part * P + jj * kStageTokens;
+                    const int n = (ic.ntok > 0 && jj < ic.nst) ? min(kStageTokens, ic.ntok - jj * kStageTokens) : 0;
+                    uint32_t mask = n > 0 ? ((1u << n) - 1u) : 0u;
+                    const int id = __shfl_sync(kFull, bid, (tok0 / bs - fb) & 31);
+                    const bool load = n > 0 && id >= 0 && static_cast<int64_t>(id) < p.num_blocks;
+                    if (n > 0 && !load) {
+                        mask = 0;
+                        if (lane == 0) report(p.err_flag, 0x2 /* PA_FLAG_BAD_BLOCK_ID */);
+                    }
+                    mask_all |= mask << (16 * hs);
+                    loads[hs] = load;
+                    zs[hs] = load ? id * bs + (tok0 % bs) : 0;
+                    bytes += load ? 2u * L::kKBytes : 0u;
                 }
                 if (lane == 0) {
                     CoopMeta m;
                     m.s = ic.s; m.kvh0 = kvh0; m.part = ic.part; m.j = j;
-                    m.nst = ic.nst; m.nparts = ic.nparts; m.mask = mask; m.pad = 0;
+                    m.nst = ic.nst; m.nparts = ic.nparts; m.mask = static_cast<int>(mask_all); m.pad = 0;
                     meta[slot] = m;
-                    mbar_arrive_expect_tx(&full[slot], load ? 2u * L::kKBytes : 0u);
-                    if (load) {
-                        const int z = id * bs + (tok0 % bs);
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+#pragma unroll
+                    for (int hs = 0; hs < SUB; ++hs) {
+                        if (!loads[hs]) continue;
+                        uint8_t *st = sp + hs * L::kStageBytes;
 #pragma unroll
                         for (int h = 0; h < L::kHalves; ++h) {
-                            tma_load_3d(sp + h * L::kBoxBytes, &tmap_k, &full[slot], h * L::kBoxElems, z, kvh0,
+                            tma_load_3d(st + h * L::kBoxBytes, &tmap_k, &full[slot], h * L::kBoxElems, zs[hs], kvh0,
                                         policy);
-                            tma_load_3d(sp + L::kVOffset + h * L::kBoxBytes, &tmap_v, &full[slot],
-                                        h * L::kBoxElems, z, kvh0, policy);
+                            tma_load_3d(st + L::kVOffset + h * L::kBoxBytes, &tmap_v, &full[slot],
+                                        h * L::kBoxElems, zs[hs], kvh0, policy);
                         }
                     }
                 }
@@ -378,8 +396,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
             break;
         }
         const int kvh = m.kvh0 + warp;
-        const uint32_t ka = sa + warp * kHeadTile;               // my K rows, half 0
-        const uint32_t va = sa + L::kVOffset + warp * kHeadTile; // my V rows, half 0
 
         if (m.j == 0) {
             // new item: my query heads' B fragments from the query ring
@@ -427,46 +443,66 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
             for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
         }
 
-        // ---- QK^T: 16 tokens x 8 heads ----
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-            const int j = lane >> 3, r = lane & 7;
-            const int tok = r + 8 * (j & 1);
-            if constexpr (!kFp8) {
+        // A slot carries SUB stages (two for e4m3 caches, whose 16-token stage is
+        // half the bytes of a 16-bit one): QK of each, one softmax update over
+        // all of them, then PV of each.  The second stage of an item's last slot
+        // may be absent.
+        const uint32_t msk = static_cast<uint32_t>(m.mask);
+        const bool second = SUB > 1 && m.j + 1 < m.nst;
+        float x[SUB][4];
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int ch = 2 * ks + (j >> 1);
-                    uint32_t a[4];
-                    ldsm_x4(a, ka + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
-                    mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
-                }
-            } else {
-                // ldmatrix on the byte rows viewed as 16-bit: each register holds
-                // four consecutive dims of one token, widened to two f16 pairs;
-                // each 32-dim chunk feeds two MMAs (dims permuted alike in q).
+        for (int hs = 0; hs < SUB; ++hs) {
+            if (hs > 0 && !second) {
+                x[hs][0] = x[hs][1] = x[hs][2] = x[hs][3] = -INFINITY;
+                continue;
+            }
+            const uint32_t ka = sa + hs * L::kStageBytes + warp * kHeadTile;
+            const uint32_t smask = (msk >> (16 * hs)) & 0xffffu;
+            // ---- QK^T: 16 tokens x 8 heads ----
+            float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int j = lane >> 3, r = lane & 7;
+                const int tok = r + 8 * (j & 1);
+                if constexpr (!kFp8) {
 #pragma unroll
-                for (int kc = 0; kc < D / 32; ++kc) {
-                    const int ch = 2 * kc + (j >> 1);
-                    uint32_t a[4], lo[4], hi[4];
-                    ldsm_x4(a, ka + tok * kRow + ((ch ^ r) << 4));
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int ch = 2 * ks + (j >> 1);
+                        uint32_t a[4];
+                        ldsm_x4(a, ka + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
+                        mma_16816<BF16>(c[ks & 1], a, qf[ks][0], qf[ks][1]);
+                    }
+                } else {
+                    // ldmatrix on the byte rows viewed as 16-bit: each register holds
+                    // four consecutive dims of one token, widened to two f16 pairs;
+                    // each 32-dim chunk feeds two MMAs (dims permuted alike in q).
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(a[i], lo[i], hi[i]);
-                    mma_16816<false>(c[0], lo, qf[2 * kc][0], qf[2 * kc][1]);
-                    mma_16816<false>(c[1], hi, qf[2 * kc + 1][0], qf[2 * kc + 1][1]);
+                    for (int kc = 0; kc < D / 32; ++kc) {
+                        const int ch = 2 * kc + (j >> 1);
+                        uint32_t a[4], lo[4], hi[4];
+                        ldsm_x4(a, ka + tok * kRow + ((ch ^ r) << 4));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(a[i], lo[i], hi[i]);
+                        mma_16816<false>(c[0], lo, qf[2 * kc][0], qf[2 * kc][1]);
+                        mma_16816<false>(c[1], hi, qf[2 * kc + 1][0], qf[2 * kc + 1][1]);
+                    }
                 }
             }
+            {
+                const bool v_lo = (smask >> g) & 1, v_hi = (smask >> (g + 8)) & 1;
+                const bool h0 = 2 * t < G, h1 = 2 * t + 1 < G;
+                const float sc = p.scale_log2;
+                x[hs][0] = (v_lo && h0) ? (c[0][0] + c[1][0]) * sc : -INFINITY;
+                x[hs][1] = (v_lo && h1) ? (c[0][1] + c[1][1]) * sc : -INFINITY;
+                x[hs][2] = (v_hi && h0) ? (c[0][2] + c[1][2]) * sc : -INFINITY;
+                x[hs][3] = (v_hi && h1) ? (c[0][3] + c[1][3]) * sc : -INFINITY;
+            }
         }
-        float x[4];
-        {
-            const bool v_lo = (m.mask >> g) & 1, v_hi = (m.mask >> (g + 8)) & 1;
-            const bool h0 = 2 * t < G, h1 = 2 * t + 1 < G;
-            const float sc = p.scale_log2;
-            x[0] = (v_lo && h0) ? (c[0][0] + c[1][0]) * sc : -INFINITY;
-            x[1] = (v_lo && h1) ? (c[0][1] + c[1][1]) * sc : -INFINITY;
-            x[2] = (v_hi && h0) ? (c[0][2] + c[1][2]) * sc : -INFINITY;
-            x[3] = (v_hi && h1) ? (c[0][3] + c[1][3]) * sc : -INFINITY;
+        float mx[2] = {fmaxf(x[0][0], x[0][2]), fmaxf(x[0][1], x[0][3])};
+#pragma unroll
+        for (int hs = 1; hs < SUB; ++hs) {
+            mx[0] = fmaxf(mx[0], fmaxf(x[hs][0], x[hs][2]));
+            mx[1] = fmaxf(mx[1], fmaxf(x[hs][1], x[hs][3]));
         }
-        float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             mx[0] = fmaxf(mx[0], __shfl_xor_sync(kFull, mx[0], o));
@@ -493,71 +529,77 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         }
         const float mu0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
         const float mu1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
-        const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
-        const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
-        l_run[0] += p0 + p2;
-        l_run[1] += p1 + p3;
+#pragma unroll
+        for (int hs = 0; hs < SUB; ++hs) {
+            if (hs > 0 && !second) continue;
+            const uint32_t smask = (msk >> (16 * hs)) & 0xffffu;
+            const uint32_t va = sa + hs * L::kStageBytes + L::kVOffset + warp * kHeadTile;
+            const float p0 = fast_exp2(x[hs][0] - mu0), p1 = fast_exp2(x[hs][1] - mu1);
+            const float p2 = fast_exp2(x[hs][2] - mu0), p3 = fast_exp2(x[hs][3] - mu1);
+            l_run[0] += p0 + p2;
+            l_run[1] += p1 + p3;
 
-        // ---- P as the PV B fragment: lane needs p(token 2t|2t+1|2t+8|2t+9, head g) ----
-        uint32_t bhi[2], blo[2];
-        {
-            const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
-            const bool odd = g & 1;
-            const float a0 = __shfl_sync(kFull, p0, srcA), a1 = __shfl_sync(kFull, p1, srcA);
-            const float a2 = __shfl_sync(kFull, p2, srcA), a3 = __shfl_sync(kFull, p3, srcA);
-            const float b0 = __shfl_sync(kFull, p0, srcB), b1 = __shfl_sync(kFull, p1, srcB);
-            const float b2 = __shfl_sync(kFull, p2, srcB), b3 = __shfl_sync(kFull, p3, srcB);
-            const float w[4] = {odd ? a1 : a0, odd ? b1 : b0, odd ? a3 : a2, odd ? b3 : b2};
+            // ---- P as the PV B fragment: lane needs p(token 2t|2t+1|2t+8|2t+9, head g) ----
+            uint32_t bhi[2], blo[2];
+            {
+                const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
+                const bool odd = g & 1;
+                const float a0 = __shfl_sync(kFull, p0, srcA), a1 = __shfl_sync(kFull, p1, srcA);
+                const float a2 = __shfl_sync(kFull, p2, srcA), a3 = __shfl_sync(kFull, p3, srcA);
+                const float b0 = __shfl_sync(kFull, p0, srcB), b1 = __shfl_sync(kFull, p1, srcB);
+                const float b2 = __shfl_sync(kFull, p2, srcB), b3 = __shfl_sync(kFull, p3, srcB);
+                const float w[4] = {odd ? a1 : a0, odd ? b1 : b0, odd ? a3 : a2, odd ? b3 : b2};
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                bhi[k] = pack2<BF16>(w[2 * k], w[2 * k + 1]);
-                const float2 h = Cvt::to_float2(bhi[k]);
-                blo[k] = pack2<BF16>(w[2 * k] - h.x, w[2 * k + 1] - h.y);
-            }
-        }
-
-        // ---- PV; my V rows past the context are zeroed first (stale slots may hold NaN) ----
-        if (m.mask != 0xffff) {
-            uint8_t *vt = sp + L::kVOffset + warp * kHeadTile;
-#pragma unroll
-            for (int k = 0; k < kStageTokens * L::kHalves * 8 / 32; ++k) {
-                const int q16 = lane + 32 * k;             // 16-byte chunk of my head's V rows
-                const int half = q16 >> 7;                 // 128 chunks per half
-                const int within = q16 & 127;
-                const int row = within >> 3;
-                if (!((m.mask >> row) & 1))
-                    *reinterpret_cast<uint4 *>(vt + half * L::kBoxBytes + within * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncwarp();
-        }
-        {
-            const int j = lane >> 3, r = lane & 7;
-            const int tok = r + 8 * (j >> 1);
-            if constexpr (!kFp8) {
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int ch = 2 * mt + (j & 1);
-                    uint32_t a[4];
-                    ldsm_x4_trans(a, va + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
-                    mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
-                    mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                for (int k = 0; k < 2; ++k) {
+                    bhi[k] = pack2<BF16>(w[2 * k], w[2 * k + 1]);
+                    const float2 h = Cvt::to_float2(bhi[k]);
+                    blo[k] = pack2<BF16>(w[2 * k] - h.x, w[2 * k + 1] - h.y);
                 }
-            } else {
-                // Transposed ldmatrix of the byte rows viewed as 16-bit gives
-                // (tokens 2t, 2t+1) x (dims 2g, 2g+1); regroup the bytes so each
-                // f16 pair is one dim over two tokens: even dims feed acc[2vc],
-                // odd dims acc[2vc+1].
+            }
+
+            // ---- PV; my V rows past the context are zeroed first (stale slots may hold NaN) ----
+            if (smask != 0xffffu) {
+                uint8_t *vt = sp + hs * L::kStageBytes + L::kVOffset + warp * kHeadTile;
 #pragma unroll
-                for (int vc = 0; vc < D / 32; ++vc) {
-                    const int ch = 2 * vc + (j & 1);
-                    uint32_t a[4], ev[4], od[4];
-                    ldsm_x4_trans(a, va + tok * kRow + ((ch ^ r) << 4));
+                for (int k = 0; k < kStageTokens * L::kHalves * 8 / 32; ++k) {
+                    const int q16 = lane + 32 * k;             // 16-byte chunk of my head's V rows
+                    const int half = q16 >> 7;                 // 128 chunks per half
+                    const int within = q16 & 127;
+                    const int row = within >> 3;
+                    if (!((smask >> row) & 1))
+                        *reinterpret_cast<uint4 *>(vt + half * L::kBoxBytes + within * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            {
+                const int j = lane >> 3, r = lane & 7;
+                const int tok = r + 8 * (j >> 1);
+                if constexpr (!kFp8) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(prmt(a[i], 0x3120u), ev[i], od[i]);
-                    mma_16816<false>(acc[2 * vc], ev, bhi[0], bhi[1]);
-                    mma_16816<false>(acc[2 * vc], ev, blo[0], blo[1]);
-                    mma_16816<false>(acc[2 * vc + 1], od, bhi[0], bhi[1]);
-                    mma_16816<false>(acc[2 * vc + 1], od, blo[0], blo[1]);
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const int ch = 2 * mt + (j & 1);
+                        uint32_t a[4];
+                        ldsm_x4_trans(a, va + (ch >> 3) * L::kBoxBytes + tok * kRow + (((ch & 7) ^ r) << 4));
+                        mma_16816<BF16>(acc[mt], a, bhi[0], bhi[1]);
+                        mma_16816<BF16>(acc[mt], a, blo[0], blo[1]);
+                    }
+                } else {
+                    // Transposed ldmatrix of the byte rows viewed as 16-bit gives
+                    // (tokens 2t, 2t+1) x (dims 2g, 2g+1); regroup the bytes so each
+                    // f16 pair is one dim over two tokens: even dims feed acc[2vc],
+                    // odd dims acc[2vc+1].
+#pragma unroll
+                    for (int vc = 0; vc < D / 32; ++vc) {
+                        const int ch = 2 * vc + (j & 1);
+                        uint32_t a[4], ev[4], od[4];
+                        ldsm_x4_trans(a, va + tok * kRow + ((ch ^ r) << 4));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(prmt(a[i], 0x3120u), ev[i], od[i]);
+                        mma_16816<false>(acc[2 * vc], ev, bhi[0], bhi[1]);
+                        mma_16816<false>(acc[2 * vc], ev, blo[0], blo[1]);
+                        mma_16816<false>(acc[2 * vc + 1], od, bhi[0], bhi[1]);
+                        mma_16816<false>(acc[2 * vc + 1], od, blo[0], blo[1]);
+                    }
                 }
             }
         }
@@ -568,7 +610,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
         if (lane == 0) mbar_arrive1(&empty[slot]);
 
         // ---- item end: output (or partial state) staged through shared memory ----
-        if (m.j == m.nst - 1) {
+        if (m.j + SUB >= m.nst) {
             float lt[2] = {l_run[0], l_run[1]};
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
