@@ -44,8 +44,25 @@
  *    and reported by atomically OR-ing a PA_FLAG_* bit into *err_flag.  The
  *    caller reads it after synchronising; any non-zero value means the
  *    affected outputs are not to be trusted (PA_ERR_DEVICE_BOUNDS).
+ *    PA_FLAG_TIMEOUT means a bounded wait gave up: that call's outputs are
+ *    undefined (a split sequence's merge may then read partial results that
+ *    an earlier call left in the workspace).
  *  - Calls are not re-entrant on the same workspace: two pa_decode calls that
  *    may overlap on the GPU need two workspaces.
+ *  - Tuning overrides.  The library chooses its kernels and their launch
+ *    shapes itself; these environment variables, read once at the first
+ *    decode call of the process, override that choice for tuning and testing.
+ *    Under any setting the results stay within the documented tolerances and
+ *    only the speed changes; leave them unset in deployment.
+ *      PA_DECODE_COOP=0          run every decode on the per-warp kernel
+ *                                (otherwise shapes with head_dim 128, KV heads
+ *                                a multiple of 8 and block_size a multiple of
+ *                                16 run on the CTA-cooperative kernel)
+ *      PA_DECODE_COOP_STAGES=n   ring depth of the cooperative kernel (2..8)
+ *      PA_DECODE_STAGES=n        ring depth per warp of the per-warp kernel (2..8)
+ *      PA_DECODE_WARPS=n         warps per CTA of the per-warp kernel (1..16)
+ *      PA_DECODE_INTERLEAVE=0    per-warp kernel: each warp takes a contiguous
+ *                                run of its CTA's items instead of every n-th
  */
 #ifndef PA_H_
 #define PA_H_
@@ -235,19 +252,22 @@ pa_status pa_decode_append(void *out, pa_dtype out_dtype,
  * library (a static __device__ array): every GPU that loads the library holds
  * that memory until the process exits.  The call allocates nothing - no
  * cudaMalloc, cudaFree or allocating library routine.
- *  - Returns PA_ERR_WORKSPACE, enqueuing nothing, when
+ *  - Arguments are checked exactly as pa_decode checks them; then, when
  *    pa_decode_workspace_size(...) for these arguments exceeds
- *    PA_NOALLOC_SCRATCH_BYTES (use a larger partition_size, fewer sequences,
- *    or pa_decode with a workspace of your own).
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    PA_NOALLOC_SCRATCH_BYTES, the call returns PA_ERR_WORKSPACE and enqueues
+ *    nothing (use a larger partition_size, fewer sequences, or pa_decode with
+ *    a workspace of your own).
+ *  - The first call in each CUDA context - once per device with the runtime's
+ *    primary contexts, again after cudaDeviceReset or under another context -
+ *    looks up the array's device address (cudaGetSymbolAddress, with the
+ *    device current) and caches it for that context; make that first call
  *    before any stream capture on the device.
  *  - Every call on a device shares the one array, which keeps the previous
  *    call's contents; nothing in it needs clearing between calls (every
- *    partial result is written before it is read within a call).  Calls that
- *    may overlap on the GPU - different streams, threads or processes' shared
- *    contexts - race on the array and corrupt each other's results: order
- *    them (one stream, or events).
+ *    partial result is written before it is read within a call that completes
+ *    without PA_FLAG_TIMEOUT).  Calls that may overlap on the GPU - different
+ *    streams, threads or processes' shared contexts - race on the array and
+ *    corrupt each other's results: order them (one stream, or events).
  */
 #define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 pa_status pa_decode_noalloc(void *out, pa_dtype out_dtype,

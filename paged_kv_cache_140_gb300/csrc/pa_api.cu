@@ -1,7 +1,7 @@
 // The exported C ABI (declared in include/pa.h): argument validation,
 // partition and workspace planning, TMA descriptor encoding and launches.
 // The library allocates no memory and keeps no state between calls beyond
-// cached device attributes and the driver entry point.
+// cached device attributes (per device ordinal) and the driver entry point.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -9,6 +9,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "pa.h"
@@ -55,17 +56,41 @@ struct DeviceInfo {
     int smem_optin = 0;
 };
 
+// Attributes of the current device, read once per device ordinal (they are
+// properties of the hardware and do not change while the process runs).
+constexpr int kMaxDevices = 64;
+
 bool device_info(DeviceInfo &info) {
+    static DeviceInfo cache[kMaxDevices];
+    static std::atomic<bool> valid[kMaxDevices];
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    if (cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (dev >= 0 && dev < kMaxDevices && valid[dev].load(std::memory_order_acquire)) {
+        info = cache[dev];
+        return true;
+    }
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
-    if (cudaDeviceGetAttribute(&info.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
         cudaSuccess)
         return false;
+    if (dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache[dev] = d;
+        valid[dev].store(true, std::memory_order_release);
+    }
+    info = d;
     return true;
 }
 
+// Tuning overrides read once from the environment (documented in pa.h):
+// PA_DECODE_COOP=0 keeps every shape on the per-warp decode kernel;
+// PA_DECODE_COOP_STAGES, PA_DECODE_STAGES and PA_DECODE_WARPS set ring depths
+// and warps per CTA; PA_DECODE_INTERLEAVE=0 gives each per-warp pipeline a
+// contiguous run of items.  Results stay within the documented tolerance under
+// any setting; only speed changes.
 struct Tuning {
     int stages = 0;  // 0: default
     int warps = 0;
@@ -415,11 +440,6 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
     const size_t smem_used = pa::decode_smem_bytes(head_dim, G, es, warps, stages, num_seqs);
     if (smem_used > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
-    CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, es) ||
-        !encode_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, es))
-        return PA_ERR_CUDA;
-
     pa::DecodeParams p{};
     p.out = out;
     p.out_dtype = static_cast<int>(out_dtype);
@@ -457,8 +477,9 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
     // an e4m3 cache) and the cooperative kernel, chained by programmatic
     // dependent launch, waits for it only before the stages that hold them.
     if (tune.coop && head_dim == 128 && num_kv_heads % 8 == 0 && block_size % 16 == 0) {
-        // a slot holds one 16-token stage: 64 KB for 16-bit caches, 32 KB for e4m3
-        int cst = tune.coop_stages > 0 ? tune.coop_stages : (fp8 ? 6 : 3);
+        // a slot holds one 16-token stage of a 16-bit cache or two of an e4m3
+        // cache: 64 KB either way
+        int cst = tune.coop_stages > 0 ? tune.coop_stages : 3;
         while (cst > 2 && pa::decode_coop_smem_bytes(G, es, cst, num_seqs) > static_cast<size_t>(dev.smem_optin))
             --cst;
         const size_t csmem = pa::decode_coop_smem_bytes(G, es, cst, num_seqs);
@@ -488,6 +509,10 @@ pa_status decode_impl(void *out, pa_dtype out_dtype, const void *query, pa_dtype
             return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
         }
     }
+    CUtensorMap tk, tv;
+    if (!encode_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, es) ||
+        !encode_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, es))
+        return PA_ERR_CUDA;
     cudaError_t e = pa::launch_decode(p, head_dim, G, kv, tk, tv, dev.sms, warps,
                                       smem_used, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
