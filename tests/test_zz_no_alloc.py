@@ -68,10 +68,11 @@ def _noalloc(torch, lib, b, T):
     return out
 
 
-def _close(torch, a, b):
-    from pa_harness import ATOL
-    d = (a - b).abs().max().item()
-    assert torch.isfinite(a).all() and d <= ATOL, f"max abs difference {d:.3e}"
+def _same(torch, a, b):
+    """Bitwise equal: both calls run the same kernel with the same partition
+    plan, so only the workspace's address differs."""
+    assert torch.isfinite(a).all()
+    assert torch.equal(a, b), f"max abs difference {(a - b).abs().max().item():.3e}"
 
 
 def test_noalloc_matches_pa_decode_on_consecutive_calls(env):
@@ -82,7 +83,35 @@ def test_noalloc_matches_pa_decode_on_consecutive_calls(env):
     T1, T2 = _dev_batch(torch, b1), _dev_batch(torch, b2)
     r1, r2 = _reference(torch, b1, T1), _reference(torch, b2, T2)
     for b, T, r in ((b1, T1, r1), (b1, T1, r1), (b2, T2, r2), (b1, T1, r1)):
-        _close(torch, _noalloc(torch, lib, b, T), r)
+        _same(torch, _noalloc(torch, lib, b, T), r)
+
+
+def test_noalloc_matches_the_oracle(env):
+    torch, lib = env
+    import oracle
+    from paged_kv_cache_140_gb300 import workloads as W
+    from pa_harness import assert_attention_close
+    oracle.build()
+    b = W.make_batch("13b", num_seqs=24)
+    ref, _, _ = oracle.decode_step(b)
+    T = _dev_batch(torch, b)
+    for _ in range(2):
+        assert_attention_close(_noalloc(torch, lib, b, T), ref, "f32", "noalloc 13b")
+
+
+def test_noalloc_per_warp_kernel_with_split_sequences(env):
+    """head_dim 64 runs the per-warp kernel; 16-token partitions split every
+    context above 16 tokens, so its partials and merge go through the array.
+    A call with another layout runs in between."""
+    torch, lib = env
+    from paged_kv_cache_140_gb300 import workloads as W
+    b = W.make_batch("tiny", partition_size=16)
+    b2 = W.make_batch("7b", num_seqs=4, head_dim=64, partition_size=48)
+    T, T2 = _dev_batch(torch, b), _dev_batch(torch, b2)
+    r, r2 = _reference(torch, b, T), _reference(torch, b2, T2)
+    _same(torch, _noalloc(torch, lib, b, T), r)
+    _same(torch, _noalloc(torch, lib, b2, T2), r2)
+    _same(torch, _noalloc(torch, lib, b, T), r)
 
 
 def test_noalloc_without_split_sequences(env):
@@ -92,15 +121,35 @@ def test_noalloc_without_split_sequences(env):
     T = _dev_batch(torch, b)
     r = _reference(torch, b, T)
     for _ in range(2):
-        _close(torch, _noalloc(torch, lib, b, T), r)
+        _same(torch, _noalloc(torch, lib, b, T), r)
 
 
 def test_noalloc_rejects_requests_beyond_the_scratch_limit(env):
+    """Valid arguments whose workspace would exceed the array: PA_ERR_WORKSPACE,
+    nothing enqueued (the output keeps its contents).  Invalid arguments get
+    pa_decode's own answer first."""
     torch, lib = env
     from paged_kv_cache_140_gb300 import _lib as L
-    need = lib.pa_decode_workspace_size(256, 40, 40, 128, 16, 2048, 16)
+    B, H, D, bs, ctx, P = 256, 40, 128, 16, 2048, 16
+    need = lib.pa_decode_workspace_size(B, H, H, D, bs, ctx, P)
     assert need > 32 * 1024 * 1024
-    nul = ctypes.c_void_p(0)
-    st = lib.pa_decode_noalloc(nul, 2, nul, 1, nul, nul, 1, 1.0, 1.0, nul, 128, nul, 2048, 256, 40, 40, 128, 16,
-                               10000, 0.088, 16, nul, nul)
-    assert st == L.PA_ERR_WORKSPACE
+    nb = 64
+    q = torch.zeros((B, H, D), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((nb, bs, H, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    bt = torch.zeros((B, ctx // bs), dtype=torch.int32, device="cuda")
+    cl = torch.ones((B,), dtype=torch.int32, device="cuda")
+    out = torch.full((B, H, D), 7.0, dtype=torch.float32, device="cuda")
+    Pv = ctypes.c_void_p
+    stream = Pv(torch.cuda.current_stream().cuda_stream)
+
+    def call(q_ptr, head_dim=D):
+        return lib.pa_decode_noalloc(Pv(out.data_ptr()), 2, q_ptr, 1, Pv(kc.data_ptr()), Pv(vc.data_ptr()), 1,
+                                     1.0, 1.0, Pv(bt.data_ptr()), ctx // bs, Pv(cl.data_ptr()), ctx, B, H, H,
+                                     head_dim, bs, nb, 0.088, P, Pv(0), stream)
+
+    assert call(Pv(q.data_ptr())) == L.PA_ERR_WORKSPACE
+    assert call(Pv(0)) == L.PA_ERR_INVALID_ARG          # null query: pa_decode's answer
+    assert call(Pv(q.data_ptr()), head_dim=96) == L.PA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
