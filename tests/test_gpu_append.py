@@ -77,15 +77,14 @@ def test_append_matches_oracle_and_separate_path(name, kw, P):
     assert np.array_equal(out.cpu().numpy(), sep.cpu().numpy())
 
 
-def test_append_native_output_full_size_sampled():
-    b = W.make_batch("13b")
+@pytest.mark.parametrize("name", ["13b", "13b_fp8", "gqa"])
+def test_append_native_output_full_size_every_row(name):
+    """The benchmark's default step (pa_decode_append) at full size: every
+    output element against the oracle, the caches bit-exact in full."""
+    b = W.make_batch(name)
+    ref, kc, vc = oracle.decode_step(b)
     out, T, flag = run_append(b, out_dtype="native")
     assert flag == 0
-    pick = [0, 5, 77, 128, 255]
-    sub = W.subset_batch(b, pick)
-    kc, vc, _ = oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
-    ref = oracle.paged_attention(sub.q, kc, vc, b.dtype, sub.block_tables, sub.context_lens, b.scale)
-    assert_attention_close(out[pick], ref, b.dtype, "13b append sampled")
-    rows = b.slot_mapping
-    gk = cache_bits(T["k_cache"]).reshape(-1, 40 * 128)
-    assert np.array_equal(gk[rows], kc.reshape(-1, 40 * 128)[rows])
+    assert_attention_close(out, ref, b.dtype, f"{name} append full size")
+    assert np.array_equal(cache_bits(T["k_cache"]), kc)
+    assert np.array_equal(cache_bits(T["v_cache"]), vc)
