@@ -65,6 +65,60 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
 
+# --------------------------------------------------------------- configs
+
+def decode_config(b, name: str, world: int) -> dict:
+    """The decode workload's config, identical in both arms' lines
+    (partition_size as requested: 0 = the library's automatic choice)."""
+    kvb = kv_bytes(b)
+    return {
+        "workload": WORKLOAD_TEXT.get(name, name),
+        "name": name,
+        "num_seqs": b.num_seqs, "num_heads": b.num_heads, "num_kv_heads": b.num_kv_heads,
+        "head_dim": b.head_dim, "block_size": b.block_size, "num_blocks": b.num_blocks,
+        "dtype": b.dtype, "cache_dtype": b.cache_dtype,
+        "tokens": int(b.context_lens.sum()), "max_context_len": b.max_context_len,
+        "partition_size": int(b.partition_size), "kv_bytes_per_step": kvb,
+        "l2": "no flush: each step reads %.2f GB of K/V, far larger than the 126 MB L2" % (kvb / 1e9),
+        "parallelism": f"replicas x{world} (independent batches per GPU)",
+    }
+
+
+def prefill_config(b, name: str, world: int) -> dict:
+    """The prefill workload's config, identical in both arms' lines."""
+    kvb = kv_bytes(b)
+    return {
+        "workload": WORKLOAD_TEXT[name], "name": name,
+        "num_seqs": b.num_seqs, "num_heads": b.num_heads, "num_kv_heads": b.num_kv_heads,
+        "head_dim": b.head_dim, "block_size": b.block_size, "num_blocks": b.num_blocks,
+        "query_tokens": b.num_tokens, "context_tokens": int(b.context_lens.sum()),
+        "flops_per_step": prefill_flops(b), "kv_bytes_read_once": kvb,
+        "l2": "no flush: K/V %.2f GB plus queries %.2f GB per step, above the 126 MB L2"
+              % (kvb / 1e9, b.q.nbytes / 1e9),
+        "parallelism": f"replicas x{world} (independent batches per GPU)",
+    }
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 # --------------------------------------------------------------- accounting
 
 def kv_bytes(b) -> int:
@@ -283,6 +337,37 @@ def stage_inputs(tensors, device):
     return flat_h, flat_d, views
 
 
+def time_e2e_direct(launch, flat_h, flat_d, out, out_h, stream, K, warmup, world):
+    """The end-to-end step with the library's entry points called through the
+    Python binding every step (no graph): one pinned-input copy, the calls,
+    the output back to pinned host memory, a stream sync.  Host milliseconds
+    per step."""
+    def one():
+        flat_d.copy_(flat_h, non_blocking=True)
+        launch()
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(3, warmup)):
+        one()
+    barrier(world)
+    w0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    ms = (time.perf_counter() - w0) * 1e3 / K
+    barrier(world)
+    return ms
+
+
+def e2e_direct_entry(units_all, unit, ms, world, h2d, d2h):
+    ms_max, _ = aggregate(ms, 0.0, world)
+    return {"value": round(units_all / (ms_max * 1e-3), 2 if unit == "TFLOP/s" else 1), "unit": unit,
+            "ms_per_step": round(ms_max, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "as e2e, but the step's C-ABI calls made through the Python binding every step "
+                    "(argument checks, tensor-map encoding and launches on the host each time) instead of a "
+                    "graph replay"}
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -445,6 +530,7 @@ def run_ours(args, world, rank, local):
         e2e_step()
     e2e_ms = (time.perf_counter() - w0) * 1e3 / K
     barrier(world)
+    e2e_direct_ms = time_e2e_direct(e2e_kernels, flat_h, flat_d, out, out_h, stream, K, args.warmup, world)
 
     kvb = kv_bytes(b)
     ms_max, kv_all = aggregate(ms_step, float(kvb), world)
@@ -475,17 +561,10 @@ def run_ours(args, world, rank, local):
         "dtype": b.dtype if b.cache_dtype == b.dtype else f"{b.dtype} q, {b.cache_dtype} kv",
         "data": "synthetic (seeded N(0,1) K/V/Q, seeded block permutation, NaN in unused slots)",
         "impl": "ours",
-        "config": {
-            "workload": WORKLOAD_TEXT.get(args.workload, args.workload),
-            "name": args.workload,
-            "num_seqs": b.num_seqs, "num_heads": b.num_heads, "num_kv_heads": b.num_kv_heads,
-            "head_dim": b.head_dim, "block_size": b.block_size, "num_blocks": b.num_blocks,
-            "tokens": int(b.context_lens.sum()), "max_context_len": b.max_context_len,
-            "partition_size": P, "kv_bytes_per_step": kvb, "step_bytes": step_bytes(b, P),
-            "seqs_tokens_per_s": round(float(b.context_lens.sum()) * world / (ms_max * 1e-3), 1),
-            "l2": "no flush: each step reads %.2f GB of K/V, far larger than the 126 MB L2" % (kvb / 1e9),
-            "parallelism": f"replicas x{world} (independent batches per GPU)",
-        },
+        "config": decode_config(b, args.workload, world),
+        "partition_size": P,
+        "step_bytes": step_bytes(b, P),
+        "seqs_tokens_per_s": round(float(b.context_lens.sum()) * world / (ms_max * 1e-3), 1),
         "roofline": {
             "kernel": decode_kernel_name(b),
             "bound": "hbm",
@@ -504,6 +583,7 @@ def run_ours(args, world, rank, local):
                         "slot_mapping too for the separate calls) staged in one pinned buffer -> device in one "
                         "copy, the step's launches replayed as one CUDA graph (pa.StepGraph), output -> pinned "
                         "host, stream sync; the KV cache stays resident"},
+        "e2e_direct": e2e_direct_entry(kv_all / 1e9, "GB/s", e2e_direct_ms, world, h2d, d2h),
         # fused on the cooperative kernel: an append kernel, then the decode
         "gpu_launches": K * ((2 if (not fused or decode_kernel_name(b) == "paged_decode_coop_kernel") else 1) +
                              (1 if has_pairs else 0) + (1 if split else 0)),
@@ -629,6 +709,8 @@ def run_prefill(args, world, rank, local):
         e2e_step()
     e2e_ms = (time.perf_counter() - w0) * 1e3 / K
     barrier(world)
+    e2e_direct_ms = time_e2e_direct(lambda: step(src=e2e_in), flat_h, flat_d, out, out_h, stream, K, args.warmup,
+                                    world)
 
     flops = prefill_flops(b)
     ms_max, fl_all = aggregate(ms_step, float(flops), world)
@@ -653,16 +735,7 @@ def run_prefill(args, world, rank, local):
         "dtype": b.dtype,
         "data": "synthetic (seeded N(0,1) K/V/Q, seeded block permutation, NaN in unused slots)",
         "impl": "ours",
-        "config": {
-            "workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-            "num_seqs": b.num_seqs, "num_heads": b.num_heads, "num_kv_heads": b.num_kv_heads,
-            "head_dim": b.head_dim, "block_size": b.block_size, "num_blocks": b.num_blocks,
-            "query_tokens": b.num_tokens, "context_tokens": int(b.context_lens.sum()),
-            "flops_per_step": flops, "kv_bytes_read_once": kvb,
-            "l2": "no flush: K/V %.2f GB plus queries %.2f GB per step, above the 126 MB L2"
-                  % (kvb / 1e9, b.q.nbytes / 1e9),
-            "parallelism": f"replicas x{world} (independent batches per GPU)",
-        },
+        "config": prefill_config(b, args.workload, world),
         "roofline": {
             "kernel": "paged_prefill_kernel",
             "bound": "tensor",
@@ -680,6 +753,7 @@ def run_prefill(args, world, rank, local):
                 "note": "per step: pinned host q/new K,V/slot_mapping/block_tables/context_lens/cu_seqlens_q "
                         "(staged in one pinned buffer) -> device in one copy, the step's launches replayed as one "
                         "CUDA graph (pa.StepGraph), output -> pinned host, stream sync; the KV cache stays resident"},
+        "e2e_direct": e2e_direct_entry(fl_all / 1e12, "TFLOP/s", e2e_direct_ms, world, h2d, d2h),
         "gpu_launches": K * (2 + (1 if has_pairs else 0)),
         "step": ("pa_copy_blocks + " if has_pairs else "") + "pa_reshape_and_cache + pa_prefill",
         "clocks": clocks,
@@ -721,7 +795,8 @@ def prefill_cpu_baseline(b, target_s):
     _prefill_oracle_rows(b, kc, vc, rows)
     dt = time.perf_counter() - t
     fl = prefill_flops(b, rows)
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "cpu_model": cpu_model(),
+            "kind": "oracle",
             "seconds": round(dt, 2),
             "sample": f"{len(rows)} of {b.num_tokens} query rows (evenly spaced, all heads; {fl} FLOPs) over the "
                       f"post-step caches; fp64 C oracle, OpenMP over (row, head)"}
@@ -747,8 +822,9 @@ def run_prefill_reference(args, world, rank):
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": b.dtype, "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "sample_rows": len(rows)},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        "config": prefill_config(b, args.workload, world),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "cpu_model": cpu_model(),
+                         "kind": "oracle",
                          "sample": f"{len(rows)} of {b.num_tokens} query rows per step ({fl} FLOPs)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -882,7 +958,8 @@ def cpu_baseline(b, target_s):
             break
     dt = (time.perf_counter() - t) / runs
     sb = kv_bytes(sub)
-    return {"value": round(sb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+    return {"value": round(sb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "cpu_model": cpu_model(),
+            "kind": "oracle",
             "seconds": round(dt * runs, 2),
             "sample": f"attention of {len(pick)} of {b.num_seqs} sequences (every "
                       f"{max(1, b.num_seqs // max(1, len(pick)))}th; {int(sub.context_lens.sum())} tokens, "
@@ -919,9 +996,9 @@ def run_reference(args, world, rank):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": b.dtype, "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload), "name": args.workload,
-                   "sample_seqs": len(pick), "sample_tokens": int(sub.context_lens.sum())},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+        "config": decode_config(b, args.workload, world),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "cpu_model": cpu_model(),
+                         "kind": "oracle",
                          "sample": f"attention of {len(pick)} of {b.num_seqs} sequences per step "
                                    f"({int(sub.context_lens.sum())} tokens, {sb} KV bytes)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
