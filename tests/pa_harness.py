@@ -92,3 +92,49 @@ def cache_bits(t) -> np.ndarray:
     if t.element_size() == 1:
         return t.cpu().view(torch.uint8).numpy()
     return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def share_prefixes(b, chains):
+    """Make sequences read the physical blocks of another: for each
+    (head, members, blocks) in ``chains``, every member's first ``blocks``
+    table entries become the head's (at most the member's block count and the
+    head's blocks before its last, which hold only the head's history rows).  A
+    sequence whose new-token slot then lies in a block another sequence also
+    reads gets slot -1 (no write), so that the step writes only private
+    blocks.  Modifies ``b`` in place and returns it."""
+    bs = b.block_size
+    for head, members, nblk in chains:
+        for s in members:
+            # only the head's full history blocks (positions it has written)
+            n = min(int(nblk), -(-int(b.context_lens[s]) // bs), (int(b.context_lens[head]) - 1) // bs)
+            b.block_tables[s, :n] = b.block_tables[head, :n]
+    readers = {}
+    for s in range(b.num_seqs):
+        for blk in b.block_tables[s, : -(-int(b.context_lens[s]) // bs)]:
+            readers[int(blk)] = readers.get(int(blk), 0) + 1
+    with_token = np.nonzero(b.context_lens > 0)[0]
+    slots = []
+    for s in with_token:
+        last = int(b.context_lens[s]) - 1
+        blk = int(b.block_tables[s, last // bs])
+        slots.append(-1 if readers[blk] > 1 else blk * bs + last % bs)
+    b.slot_mapping = np.asarray(slots, dtype=np.int64)
+    return b
+
+
+SHARED_CHAINS = [   # (head, members, shared blocks): chains of 4 and 6 (longer than one run), two
+    # sequences equal but for their last block, members ending inside the shared blocks
+    (0, [1, 2, 3], 40),
+    (4, [5, 6, 7, 8, 9], 12),
+    (10, [11], 124),
+]
+
+
+def shared_prefix_batch(name="7b", **kw):
+    """A 14-sequence batch whose sequences share leading blocks in the
+    chains of SHARED_CHAINS, with contexts that end before, inside and after
+    the shared blocks."""
+    from paged_kv_cache_140_gb300 import workloads as W
+    ctx = [1500, 900, 1500, 700, 300, 250, 190, 192, 600, 193, 2000, 2000, 64, 0]
+    b = W.make_batch(name, context_lens=ctx, **kw)
+    return share_prefixes(b, SHARED_CHAINS)

@@ -1,9 +1,10 @@
 """GPU checks of the CTA-cooperative decode kernel (16-bit or e4m3 caches
 whose KV heads come in groups of 8, head_dim 128, block size a multiple of
 16): parity with the oracle for every group size, including G = 8 (shallower
-ring), both query types over an e4m3 cache, and, for 16-bit caches, bit
-equality with the per-warp kernel, which a child process selects with
-PA_DECODE_COOP=0."""
+ring), both query types over an e4m3 cache, sequences that share physical
+blocks (served together from one copy of each shared stage), and, for 16-bit
+caches, bit equality with the per-warp kernel, which a child process selects
+with PA_DECODE_COOP=0."""
 import os
 import subprocess
 import sys
@@ -51,17 +52,73 @@ def test_cooperative_kernel_matches_oracle(name, hq, hkv, dtype, bs):
     assert_attention_close(out, ref, "f32", f"coop {hq}/{hkv} {dtype} bs {bs}")
 
 
-@pytest.mark.parametrize("hq,hkv,dtype", [(40, 40, "bf16"), (32, 8, "bf16"), (64, 8, "f16")])
-def test_cooperative_and_per_warp_kernels_agree_bit_for_bit(tmp_path, hq, hkv, dtype):
+BIT_CASES = [   # (workload, Hq, Hkv, dtype, partition size)
+    ("7b", 40, 40, "bf16", None),
+    ("7b", 32, 8, "bf16", None),
+    ("7b", 64, 8, "f16", None),
+    ("shared", 8, 8, "f16", None),       # runs of sequences sharing blocks, one member column each
+    ("shared", 16, 8, "bf16", 48),       # G = 2: two members per run
+    ("shared", 8, 8, "bf16", 16),        # every stage its own partition
+    ("prefix", 32, 32, "f16", None),     # the prefix-sharing workload (three prompt groups)
+]
+
+
+@pytest.mark.parametrize("name,hq,hkv,dtype,P", BIT_CASES,
+                         ids=[f"{c[0]}-{c[1]}x{c[2]}-{c[3]}-P{c[4]}" for c in BIT_CASES])
+def test_cooperative_and_per_warp_kernels_agree_bit_for_bit(tmp_path, name, hq, hkv, dtype, P):
+    """The per-warp kernel handles every sequence on its own; the cooperative
+    kernel serves sequences that share a stage's block from one copy of it.
+    Each sequence's arithmetic is the same, so the outputs agree bit for bit."""
     outs = {}
     for coop in ("1", "0"):
         path = str(tmp_path / f"out_{coop}.npy")
         env = dict(os.environ, PA_DECODE_COOP=coop)
-        r = subprocess.run([sys.executable, os.path.join(HERE, "coop_child.py"), "7b", str(hq), str(hkv), dtype,
-                            path], env=env, capture_output=True, text=True, timeout=600)
+        args = [sys.executable, os.path.join(HERE, "coop_child.py"), name, str(hq), str(hkv), dtype, path]
+        if P is not None:
+            args.append(str(P))
+        r = subprocess.run(args, env=env, capture_output=True, text=True, timeout=600)
         assert r.returncode == 0, r.stderr[-2000:]
         outs[coop] = np.load(path)
     assert np.array_equal(outs["1"], outs["0"])
+
+
+SHARED_CASES = [   # (Hq, Hkv, dtype, block size, partition size)
+    (8, 8, "f16", 16, 0),
+    (8, 8, "bf16", 16, 16),
+    (16, 8, "bf16", 32, 48),
+    (8, 8, "f16", 64, 256),
+    (32, 8, "bf16", 16, 0),     # G = 4: no runs, every sequence on its own
+]
+
+
+@pytest.mark.parametrize("hq,hkv,dtype,bs,P", SHARED_CASES,
+                         ids=[f"{c[0]}x{c[1]}-{c[2]}-bs{c[3]}-P{c[4]}" for c in SHARED_CASES])
+def test_sequences_sharing_blocks_match_oracle(hq, hkv, dtype, bs, P):
+    """Chains of sequences reading the same leading physical blocks: longer
+    than one run, with members ending before, inside and after the shared
+    blocks, and two sequences equal but for their last block."""
+    from pa_harness import cache_bits, shared_prefix_batch
+    b = shared_prefix_batch(num_heads=hq, num_kv_heads=hkv, dtype=dtype, block_size=bs)
+    ref, kc, vc = oracle.decode_step(b)
+    out, T, flag = run_step(b, partition_size=P)
+    assert flag == 0
+    assert_attention_close(out, ref, "f32", f"shared blocks {hq}/{hkv} {dtype} bs {bs} P {P}")
+    assert np.array_equal(cache_bits(T["k_cache"]), kc)
+
+
+def test_shared_block_with_bad_id_is_flagged_and_isolated():
+    """A bad block id inside a run's shared prefix: the run's members skip it
+    and flag it; sequences outside the run are untouched."""
+    import paged_kv_cache_140_gb300 as pa
+    from pa_harness import shared_prefix_batch
+    b = shared_prefix_batch(num_heads=8, num_kv_heads=8)
+    b.block_tables[0:4, 3] = b.num_blocks + 9
+    out, _, flag = run_step(b)
+    assert flag & pa.FLAG_BAD_BLOCK_ID
+    keep = list(range(4, b.num_seqs))
+    ref, _, _ = oracle.decode_step(W.subset_batch(b, keep))
+    assert_attention_close(out[keep], ref, "f32", "sequences outside the run")
+    assert np.all(np.isfinite(out[:4].float().cpu().numpy()))
 
 
 FP8_CASES = [   # (Hq, Hkv, query dtype, block size)
