@@ -79,6 +79,7 @@ def decode_config(b, name: str, world: int) -> dict:
         "dtype": b.dtype, "cache_dtype": b.cache_dtype,
         "tokens": int(b.context_lens.sum()), "max_context_len": b.max_context_len,
         "partition_size": int(b.partition_size), "kv_bytes_per_step": kvb,
+        "kv_bytes_unique_per_step": kv_bytes_unique(b),
         "l2": "no flush: each step reads %.2f GB of K/V, far larger than the 126 MB L2" % (kvb / 1e9),
         "parallelism": f"replicas x{world} (independent batches per GPU)",
     }
@@ -126,10 +127,24 @@ def kv_bytes(b) -> int:
     return int(b.context_lens.astype("int64").sum()) * b.num_kv_heads * b.head_dim * 2 * b.elem_bytes
 
 
+def kv_bytes_unique(b) -> int:
+    """Bytes of K and V in the distinct cache slots a decode step reads: a
+    slot that several sequences read through shared blocks counts once (the
+    decode kernel loads a shared stage once for all of them)."""
+    import numpy as np
+    ctx = b.context_lens.astype(np.int64)
+    parts = []
+    for s in range(b.num_seqs):
+        pos = np.arange(int(ctx[s]), dtype=np.int64)
+        parts.append(b.block_tables[s, pos // b.block_size].astype(np.int64) * b.block_size + pos % b.block_size)
+    slots = np.unique(np.concatenate(parts)) if parts else np.zeros(0, np.int64)
+    return int(slots.size) * b.num_kv_heads * b.head_dim * 2 * b.elem_bytes
+
+
 def decode_bytes(b, partition: int) -> int:
-    """Algorithmic bytes of one pa_decode launch: KV rows, queries, outputs,
-    block-table entries, context lengths and the split-K partial states
-    (written once, read once by the merge)."""
+    """Algorithmic bytes of one pa_decode launch: the K/V rows of the distinct
+    slots read, queries, outputs, block-table entries, context lengths and the
+    split-K partial states (written once, read once by the merge)."""
     import numpy as np
     ctx = b.context_lens.astype(np.int64)
     G = b.num_heads // b.num_kv_heads
@@ -138,7 +153,7 @@ def decode_bytes(b, partition: int) -> int:
     tables = int(np.ceil(ctx / b.block_size).sum()) * 4 * b.num_kv_heads
     nparts = np.where(ctx > 0, -(-ctx // partition), 1)
     split = int(nparts[nparts > 1].sum()) * b.num_kv_heads * G * (b.head_dim + 2) * 4 * 2
-    return kv_bytes(b) + q + out + tables + b.num_seqs * 4 + split
+    return kv_bytes_unique(b) + q + out + tables + b.num_seqs * 4 + split
 
 
 def step_bytes(b, partition: int) -> int:
