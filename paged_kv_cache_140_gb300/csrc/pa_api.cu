@@ -610,7 +610,7 @@ PA_EXPORT pa_status pa_prefill(void *out, pa_dtype out_dtype, const void *query,
     DeviceInfo dev;
     if (!device_info(dev)) return PA_ERR_CUDA;
     const size_t smem = pa::prefill_smem_bytes(head_dim);
-    // + the kernel's static shared memory (barriers, row exchange, the sequence order), under 8 KB
+    // + the kernel's static shared memory (barriers, the sequence order), under 8 KB
     if (smem + 8192 > static_cast<size_t>(dev.smem_optin)) return PA_ERR_UNSUPPORTED;
 
     CUtensorMap tq, tk, tv, to;

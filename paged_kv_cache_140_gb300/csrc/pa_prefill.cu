@@ -14,13 +14,14 @@
 // MMAs interleave in the tensor pipe.  Per K/V tile j and query tile X:
 //   S_X = Q_X K_j^T   tcgen05.mma, Q and K tiles in shared memory (TMA,
 //                     128-byte swizzle), S in tensor memory;
-//   softmax           eight warps per query tile, two threads per row (64
-//                     columns each, the row max traded through shared memory);
-//                     running max and sum in registers, the output rescaled
-//                     only when the max grows by more than 2^8; the weights P
-//                     written as 16-bit pairs over the S columns they came
-//                     from, released to the MMA in two 32-key chunks so that
-//                     half of PV runs while the second chunk is made;
+//   softmax           four warps per query tile, one thread per row holding
+//                     the row's 128 scores in registers (one tensor-memory
+//                     read, no exchange between threads); running max and
+//                     sum in registers, the output rescaled only when the max
+//                     grows by more than 2^8; the weights P written as 16-bit
+//                     pairs over the S columns they came from, released to
+//                     the MMA in four 32-key chunks so that PV starts while
+//                     the later chunks are made;
 //   O_X += P_X V_j    tcgen05.mma with P read from tensor memory and V
 //                     (MN-major) from shared memory, O in tensor memory.
 // The MMA stream runs ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...; tcgen05
@@ -31,14 +32,20 @@
 // bf16, P_lo = P - P_hi) and PV runs twice; binary16 weights are used as is.
 // Full query tiles leave through shared-memory staging and TMA stores.
 //
-// Warp roles: warps 0-15 run the softmax and the epilogue (warp w: query tile
-// w / 8, column half (w / 4) % 2, TMEM lanes 32 (w % 4)..); warp 16 loads the
-// query tiles and the K tiles, warp 18 the V tiles (both read the block table
-// 32 entries at a time); warp 17 owns the tensor memory and runs the MMA
-// issue loop in uniform control flow, one elected lane issuing (tcgen05
-// operands computed per lane inside a one-lane branch cost ~40 % of the MMA
-// rate).  Every mbarrier wait is bounded (2 s); a timeout sets
-// PA_FLAG_TIMEOUT and the CTA winds down without further MMAs.
+// A unit with a single query tile (a short tail) leaves the second tile's S
+// columns idle; there they serve as a second S buffer, so that QK of the next
+// K/V tile runs while the softmax of this one does (S no longer waits for the
+// PV that reads P out of the same columns).
+//
+// Warp roles (11 warps, so that a sub-partition holds at most 3 and every
+// thread gets 168 registers): warps 0-7 run the softmax and the epilogue
+// (warp w: query tile w / 4, TMEM lanes 32 (w % 4)..); warp 8 loads the query
+// tiles and the K tiles, warp 10 the V tiles (both read the block table 32
+// entries at a time); warp 9 owns the tensor memory and runs the MMA issue
+// loop in uniform control flow, one elected lane issuing (tcgen05 operands
+// computed per lane inside a one-lane branch cost ~40 % of the MMA rate).
+// Every mbarrier wait is bounded (2 s); a timeout sets PA_FLAG_TIMEOUT and the
+// CTA winds down without further MMAs.
 #include <math_constants.h>
 
 #include "pa.h"
@@ -52,11 +59,14 @@ namespace {
 constexpr int kTile = kPrefillTile;
 constexpr int kRegion = kTile * 128;     // 128 rows x 128 bytes: one swizzled operand region
 constexpr uint32_t kTmemCols = 512;
-// Tensor memory: S/P of query tile X at columns 128 X, O of X at 256 + 128 X.
+// Tensor memory: S/P of query tile X at columns 128 X, O of X at 256 + 128 X
+// (a single-tile unit alternates its S/P between columns 0 and 128).
 // P of a 32-key chunk sits in that chunk's own S columns: 16 columns of hi
 // pairs, then (bf16) 16 columns of lo pairs.
 constexpr uint32_t kColS = 0, kColO = 256;
-constexpr int kWarpK = 16, kWarpMma = 17, kWarpV = 18;
+constexpr int kSoftmaxWarps = 8;        // four per query tile, one thread per row
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+constexpr int kChunks = 4;              // 32-key chunks of a row's weights, released one by one
 constexpr int kMaxRing = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -69,12 +79,11 @@ struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
     uint64_t s_full[2];                  // per query tile
-    uint64_t p_full[2][2];               // [query tile][32-key chunk of each thread's 64 keys]
+    uint64_t p_full[2][kChunks];         // [query tile][32-key chunk of the row]
     uint64_t zeroed;                     // once: stale V rows of the last K/V tile zeroed
     uint64_t done;
+    uint64_t pv_done;                    // single-tile unit: each PV has completed
     uint64_t staged[2];                  // per query tile: its output rows staged for the TMA store
-    uint64_t pair[2][2][4];              // [use parity][query tile][lane quarter]: a row's two warps
-    float red[2][2][2][kTile];           // [use parity][query tile][column half][row]
     int ctx[kRankSeqs];                  // context lengths, for the longest-first order
     int cu[kRankSeqs + 1];               // their cu_seqlens_q entries
     int seq;                             // this CTA's sequence
@@ -122,19 +131,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Trade a per-row value with the partner thread that holds the other half of
-// the row: publish `mine`, wait (bounded) for the pair's phase, read theirs.
-// `use` counts the exchanges of this pair (K/V tile index, then one more).
-__device__ __forceinline__ bool pair_exchange(Shared &sh, int use, int x, int q, int h, int row, float mine,
-                                              float &theirs, int *err_flag) {
-    const int b = use & 1;
-    sh.red[b][x][h][row] = mine;
-    mbar_arrive(&sh.pair[b][x][q]);
-    if (!warp_wait_bar(&sh.pair[b][x][q], (use >> 1) & 1, sh, err_flag)) return false;
-    theirs = sh.red[b][x][h ^ 1][row];
-    return true;
-}
-
 // 3-D tiled TMA load without an L2 hint (K/V tiles are re-read by the other
 // query tiles of the same sequence and head, which run next to this one).
 __device__ __forceinline__ void tma_load_3d_plain(void *dst, const CUtensorMap *map, uint64_t *bar,
@@ -144,11 +140,6 @@ __device__ __forceinline__ void tma_load_3d_plain(void *dst, const CUtensorMap *
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
         : "memory");
-}
-
-__device__ __forceinline__ void st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-    umma::st_32x32b_x16(taddr, r);
-    umma::st_32x32b_x16(taddr + 16, r + 16);
 }
 
 // ------------------------------------------------ packed fp32 pair arithmetic
@@ -314,7 +305,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     constexpr int NK = Rings<D>::K, NV = Rings<D>::V;
     constexpr int kKSteps = D / 16;         // QK MMAs per tile (K = 16 each)
     constexpr int kPVSteps = kTile / 16;    // PV MMAs per tile and weight part
-    constexpr int kHalfD = D / 2;           // O columns per softmax thread
     constexpr uint32_t kIdescQK = umma::idesc_f16(BF16, kTile, kTile, false);
     constexpr uint32_t kIdescPV = umma::idesc_f16(BF16, kTile, D, true);
 
@@ -384,8 +374,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const bool hasB = t0A + TT < ql;
 
     // Softmax threads: query tile x, row `row` (token rtok, head kvh * G + row % G),
-    // columns [64 h, 64 h + 64) of S and [D/2 h, D/2 h + D/2) of O.
-    const int x = (warp >> 3) & 1, q4 = warp & 3, h = (warp >> 2) & 1;
+    // all 128 columns of S and all D columns of O.
+    const int x = (warp >> 2) & 1, q4 = warp & 3;
     const int row = 32 * q4 + lane;
     const int rtok = row >> lg;
     const int t0x = t0A + x * TT;
@@ -395,13 +385,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     if (ctx < ql || static_cast<int64_t>(ctx) > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
         if (threadIdx.x == 0 && pi == 0 && kvh == 0) report(p.err_flag, PA_FLAG_BAD_CONTEXT_LEN);
-        if (warp < 16 && rtok < ntokx) {
+        if (warp < kSoftmaxWarps && rtok < ntokx) {
             float z[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < kHalfD / 32; ++c)
-                store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, z);
+            for (int c = 0; c < D / 32; ++c) store_chunk(p.out, p.out_dtype, out_row * D + c * 32, z);
         }
         return;
     }
@@ -414,6 +403,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // unloaded V rows are zeroed (by the query tile that reaches furthest)
     // before any PV reads it, so that 0-weights cannot meet NaNs.
     const bool zero_tail = n_tiles * kTile - 1 > qpos_max;
+    // A unit with a single query tile over two or more K/V tiles uses the
+    // second tile's S columns as a second S buffer: QK of K/V tile j + 1 runs
+    // while the softmax of tile j does, instead of after PV(j) (which reads P(j)
+    // from the columns S(j) came in).  The output is then rescaled only after
+    // the previous PV has completed.
+    const bool solo = !hasB && nA >= 2;
 
     if (threadIdx.x == 0) {
         mbar_init(&sh.q_full, 1);
@@ -425,15 +420,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i][0], 256);
-            mbar_init(&sh.p_full[i][1], 256);
-            for (int y = 0; y < 2; ++y)
-                for (int q = 0; q < 4; ++q) mbar_init(&sh.pair[i][y][q], 64);
+            for (int c = 0; c < kChunks; ++c) mbar_init(&sh.p_full[i][c], 128);
         }
         mbar_init(&sh.done, 1);
-        mbar_init(&sh.zeroed, 256);
-        mbar_init(&sh.staged[0], 256);
-        mbar_init(&sh.staged[1], 256);
+        mbar_init(&sh.pv_done, 1);
+        mbar_init(&sh.zeroed, 128);
+        mbar_init(&sh.staged[0], 128);
+        mbar_init(&sh.staged[1], 128);
         sh.abort = 0;
         sh.bad = 0;
         fence_barrier_init();
@@ -494,59 +487,124 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const uint64_t kd0 = umma::desc_sw128(smem_addr(sK), 16, 1024);
         const uint64_t vd0 = umma::desc_sw128(smem_addr(sV), kRegion, 1024);
         constexpr uint32_t kOpDesc = kOp >> 4;
-        const int nx[2] = {nA, nB};
         bool ok = warp_wait_bar(&sh.q_full, 0, sh, p.err_flag);
-        int k_ready = -1;                      // last K tile known to have landed
-        auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
-            const int kst = t % NK;
-            if (k_ready < t) {
-                if (!warp_wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
-                k_ready = t;
-            }
-            umma::fence_after_sync();
-            const uint64_t qd = qd0 + static_cast<uint32_t>(xx) * kOpDesc;
-            const uint64_t kd = kd0 + static_cast<uint32_t>(kst) * kOpDesc;
-            const uint32_t ts = tmem + kColS + 128u * xx;
-            if (leader) {
-#pragma unroll
-                for (int k = 0; k < kKSteps; ++k) {
-                    constexpr uint32_t kRegDesc = kRegion >> 4;
-                    const uint32_t off = (k >> 2) * kRegDesc + (k & 3) * 2;
-                    umma::mma_ss(ts, qd + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
+        if (!solo) {
+            const int nx[2] = {nA, nB};
+            int k_ready = -1;                      // last K tile known to have landed
+            auto qk = [&](int xx, int t) -> bool {      // S_xx = Q_xx K_t^T
+                const int kst = t % NK;
+                if (k_ready < t) {
+                    if (!warp_wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                    k_ready = t;
                 }
-                umma::commit(smem_addr(&sh.s_full[xx]));
-            }
+                umma::fence_after_sync();
+                const uint64_t qd = qd0 + static_cast<uint32_t>(xx) * kOpDesc;
+                const uint64_t kd = kd0 + static_cast<uint32_t>(kst) * kOpDesc;
+                const uint32_t ts = tmem + kColS + 128u * xx;
+                if (leader) {
+    #pragma unroll
+                    for (int k = 0; k < kKSteps; ++k) {
+                        constexpr uint32_t kRegDesc = kRegion >> 4;
+                        const uint32_t off = (k >> 2) * kRegDesc + (k & 3) * 2;
+                        umma::mma_ss(ts, qd + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
+                    }
+                    umma::commit(smem_addr(&sh.s_full[xx]));
+                }
+                __syncwarp();
+                return true;
+            };
+            if (ok) ok = qk(0, 0);
+            if (ok && hasB) ok = qk(1, 0);
+            if (ok && leader) umma::commit(smem_addr(&sh.k_empty[0]));
             __syncwarp();
-            return true;
-        };
-        if (ok) ok = qk(0, 0);
-        if (ok && hasB) ok = qk(1, 0);
-        if (ok && leader) umma::commit(smem_addr(&sh.k_empty[0]));
-        __syncwarp();
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            const int vst = j % NV;
-            if (zero_tail && j == n_tiles - 1 && !warp_wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
-                ok = false;
-                break;
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int vst = j % NV;
+                if (zero_tail && j == n_tiles - 1 && !warp_wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
+                const uint64_t vd = vd0 + static_cast<uint32_t>(vst) * kOpDesc;
+                for (int xx = 0; ok && xx < 2; ++xx) {
+                    if (j >= nx[xx]) continue;
+                    const uint32_t tP = tmem + kColS + 128u * xx;
+                    const uint32_t tO = tmem + kColO + 128u * xx;
+                    const uint32_t acc0 = j > 0 ? 1u : 0u;
+                    // Each softmax thread writes its row's weights in four 32-key
+                    // chunks; chunk c feeds k-steps 2c and 2c + 1, so PV starts
+                    // while the later chunks are still being made.
+    #pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        if (!warp_wait_bar(&sh.p_full[xx][c], j & 1, sh, p.err_flag)) { ok = false; break; }
+                        umma::fence_after_sync();
+                        if (leader) {
+    #pragma unroll
+                            for (int kk = 0; kk < kPVSteps / kChunks; ++kk) {
+                                const int k = (kPVSteps / kChunks) * c + kk;
+                                umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1),
+                                             vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV,
+                                             (c > 0 || kk > 0) ? 1u : acc0);
+                                if constexpr (BF16)
+                                    umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1) + 16u,
+                                                 vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV, 1u);
+                            }
+                        }
+                        __syncwarp();
+                    }
+                    if (!ok) break;
+                    if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
+                }
+                if (!ok) break;
+                if (leader) {
+                    umma::commit(smem_addr(&sh.v_empty[vst]));
+                    if (j + 1 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 1) % NK]));
+                }
+                __syncwarp();
             }
-            if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-            const uint64_t vd = vd0 + static_cast<uint32_t>(vst) * kOpDesc;
-            for (int xx = 0; ok && xx < 2; ++xx) {
-                if (j >= nx[xx]) continue;
-                const uint32_t tP = tmem + kColS + 128u * xx;
-                const uint32_t tO = tmem + kColO + 128u * xx;
-                const uint32_t acc0 = j > 0 ? 1u : 0u;
-                // Each softmax thread writes its 64 keys' weights in two 32-key
-                // chunks; chunk c of both row halves feeds k-steps {2c, 2c+1,
-                // 4+2c, 5+2c}, so half of PV runs while the second chunk is made.
+        } else {
+            // S(t) goes to buffer t & 1; QK(t + 2) follows PV(t), which has read
+            // P(t) from the same columns (tcgen05 operations of one thread run in
+            // issue order).
+            auto qk_solo = [&](int t) -> bool {
+                const int kst = t % NK, b = t & 1;
+                if (!warp_wait_bar(&sh.k_full[kst], (t / NK) & 1, sh, p.err_flag)) return false;
+                umma::fence_after_sync();
+                const uint64_t kd = kd0 + static_cast<uint32_t>(kst) * kOpDesc;
+                const uint32_t ts = tmem + kColS + 128u * b;
+                if (leader) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (!warp_wait_bar(&sh.p_full[xx][c], j & 1, sh, p.err_flag)) { ok = false; break; }
+                    for (int k = 0; k < kKSteps; ++k) {
+                        constexpr uint32_t kRegDesc = kRegion >> 4;
+                        const uint32_t off = (k >> 2) * kRegDesc + (k & 3) * 2;
+                        umma::mma_ss(ts, qd0 + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
+                    }
+                    umma::commit(smem_addr(&sh.s_full[b]));
+                    umma::commit(smem_addr(&sh.k_empty[kst]));
+                }
+                __syncwarp();
+                return true;
+            };
+            if (ok) ok = qk_solo(0);
+            if (ok) ok = qk_solo(1);
+            const uint32_t tO = tmem + kColO;
+            for (int j = 0; ok && j < nA; ++j) {
+                const int vst = j % NV, b = j & 1;
+                if (zero_tail && j == nA - 1 && !warp_wait_bar(&sh.zeroed, 0, sh, p.err_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
+                const uint64_t vd = vd0 + static_cast<uint32_t>(vst) * kOpDesc;
+                const uint32_t tP = tmem + kColS + 128u * b;
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    if (!warp_wait_bar(&sh.p_full[b][c], (j >> 1) & 1, sh, p.err_flag)) { ok = false; break; }
                     umma::fence_after_sync();
                     if (leader) {
 #pragma unroll
-                        for (int kk = 0; kk < kPVSteps / 2; ++kk) {
-                            const int k = 2 * c + (kk & 1) + 4 * (kk >> 1);
+                        for (int kk = 0; kk < kPVSteps / kChunks; ++kk) {
+                            const int k = (kPVSteps / kChunks) * c + kk;
                             umma::mma_ts(tO, tP + 32u * (k >> 1) + 8u * (k & 1),
                                          vd + static_cast<uint32_t>(k * (2048 >> 4)), kIdescPV,
                                          (c > 0 || kk > 0) ? 1u : acc0);
@@ -558,27 +616,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     __syncwarp();
                 }
                 if (!ok) break;
-                if (j + 1 < nx[xx]) ok = qk(xx, j + 1);
+                if (leader) {
+                    umma::commit(smem_addr(&sh.pv_done));
+                    umma::commit(smem_addr(&sh.v_empty[vst]));
+                }
+                __syncwarp();
+                if (j + 2 < nA) ok = qk_solo(j + 2);
             }
-            if (!ok) break;
-            if (leader) {
-                umma::commit(smem_addr(&sh.v_empty[vst]));
-                if (j + 1 < n_tiles) umma::commit(smem_addr(&sh.k_empty[(j + 1) % NK]));
-            }
-            __syncwarp();
         }
         if (leader) {
             umma::commit(smem_addr(&sh.done));
             mbar_wait_bounded(&sh.done, 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp < 16 && (x == 0 || hasB)) {
+    } else if (warp < kSoftmaxWarps && (x == 0 || hasB)) {
         // ------------------------------------------- softmax and epilogue
         const int nx = x == 0 ? nA : nB;
         const int qpos = rtok < ntokx ? qstartA + x * TT + rtok : -1;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-        const uint32_t tS = tmem + kColS + 128u * x + lane_off + 64u * h;
-        const uint32_t tO = tmem + kColO + 128u * x + lane_off + kHalfD * h;
+        const uint32_t tS0 = tmem + kColS + lane_off;
+        const uint32_t tO = tmem + kColO + 128u * x + lane_off;
         // The tile that reaches furthest zeroes the stale V rows of the last K/V tile.
         const bool zeroer = zero_tail && x == (hasB ? 1 : 0);
         const float sl = p.scale_log2;
@@ -587,53 +644,56 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         float l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < nx; ++j) {
-            if (!warp_wait_bar(&sh.s_full[x], j & 1, sh, p.err_flag)) { ok = false; break; }
+            // S buffer: the tile's own, or (single-tile unit) alternating
+            const int b = solo ? (j & 1) : x;
+            if (!warp_wait_bar(&sh.s_full[b], solo ? (j >> 1) & 1 : j & 1, sh, p.err_flag)) { ok = false; break; }
             umma::fence_after_sync();
-            const int lim = qpos - j * kTile - 64 * h;   // columns c <= lim are attended
-            const bool masked = !__all_sync(0xffffffffu, lim >= 63);
-            float mx = -CUDART_INF_F;
+            const uint32_t tS = tS0 + 128u * b;
+            const int lim = qpos - j * kTile;   // columns c <= lim are attended
+            const bool masked = !__all_sync(0xffffffffu, lim >= kTile - 1);
+            // the whole S row in registers: four loads in flight, one wait
+            uint32_t v[kTile];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v[32];
-                umma::ld_32x32b_x32(tS + 32 * c, v);
-                umma::wait_ld();
-                if (masked) {
+            for (int c = 0; c < kChunks; ++c)
+                umma::ld_32x32b_x32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+            umma::wait_ld();
+            if (masked) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 * c + i > lim) v[i] = 0xff800000u;     // -inf
-                }
-                float a0 = mx, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    a0 = max3(a0, __uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
-                    a1 = max3(a1, __uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
-                    a2 = max3(a2, __uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
-                    a3 = max3(a3, __uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
-                }
-                mx = max3(a0, a1, fmaxf(a2, a3));
+                for (int i = 0; i < kTile; ++i)
+                    if (i > lim) v[i] = 0xff800000u;     // -inf
             }
-            float mx_other;
-            if (!pair_exchange(sh, j, x, q4, h, row, mx, mx_other, p.err_flag)) { ok = false; break; }
-            mx = fmaxf(mx, mx_other);
+            float a[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a[k] = fmaxf(__uint_as_float(v[k]), __uint_as_float(v[k + 8]));
+#pragma unroll
+            for (int i = 1; i < kTile / 16; ++i)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    a[k] = max3(a[k], __uint_as_float(v[16 * i + k]), __uint_as_float(v[16 * i + 8 + k]));
+            const float mx = max3(max3(a[0], a[1], a[2]), max3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
             const float x_tile = mx * sl;
             const bool need = x_tile > m_run + 8.f;
             if (__any_sync(0xffffffffu, need)) {
                 // O_x already holds tile j-1: PV(j-1) preceded QK(j) in the MMA stream.
                 const float f = need ? fast_exp2(m_run - x_tile) : 1.f;
                 if (j > 0) {
+                    // single-tile unit: PV(j-1) may still be running
+                    if (solo && !warp_wait_bar(&sh.pv_done, (j - 1) & 1, sh, p.err_flag)) { ok = false; break; }
+                    umma::fence_after_sync();
                     const uint64_t f2x = f2(f, f);
+                    // 16 columns at a time: the S row stays live in registers meanwhile
 #pragma unroll
-                    for (int c = 0; c < kHalfD / 32; ++c) {
-                        uint32_t o[32];
-                        umma::ld_32x32b_x32(tO + 32 * c, o);
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint32_t o[16];
+                        umma::ld_32x32b_x16(tO + 16 * c, o);
                         umma::wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float2 v = unf2(mul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2x));
-                            o[2 * i] = __float_as_uint(v.x);
-                            o[2 * i + 1] = __float_as_uint(v.y);
+                        for (int i = 0; i < 8; ++i) {
+                            const float2 w = unf2(mul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2x));
+                            o[2 * i] = __float_as_uint(w.x);
+                            o[2 * i + 1] = __float_as_uint(w.y);
                         }
-                        st_32x32b_x32(tO + 32 * c, o);
+                        umma::st_32x32b_x16(tO + 16 * c, o);
                     }
                 }
                 if (need) {
@@ -644,10 +704,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             if (zeroer && j == nx - 1) {
                 const int vst = j % NV;
                 if (!warp_wait_bar(&sh.v_full[vst], (j / NV) & 1, sh, p.err_flag)) { ok = false; break; }
-                if (j * kTile + row > qpos_max && (R > 1 || h == 0)) {
-                    uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + (R > 1 ? h : 0) * kRegion + row * 128);
+                if (j * kTile + row > qpos_max) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int r = 0; r < R; ++r) {
+                        uint4 *d = reinterpret_cast<uint4 *>(sV + vst * kOp + r * kRegion + row * 128);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&sh.zeroed);
@@ -658,19 +721,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const uint64_t nm2 = f2(-mref, -mref);
             uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v[32];
-                umma::ld_32x32b_x32(tS + 32 * c, v);
-                umma::wait_ld();
-                if (masked) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 * c + i > lim) v[i] = 0xff800000u;
-                }
-                uint32_t hi[16], lo[16];
+            for (int c = 0; c < kChunks; ++c) {
+                uint32_t hi[16];
+                [[maybe_unused]] uint32_t lo[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float2 xv = unf2(fma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2, nm2));
+                    const float2 xv = unf2(fma2(f2(__uint_as_float(v[32 * c + 2 * i]), __uint_as_float(v[32 * c + 2 * i + 1])),
+                                                sl2, nm2));
                     const float p0 = fast_exp2(xv.x), p1 = fast_exp2(xv.y);
                     hi[i] = pack2<BF16>(p0, p1);
                     const float2 hv = Half2x<BF16>::to_float2(hi[i]);
@@ -686,7 +743,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 if constexpr (BF16) umma::st_32x32b_x16(tS + 32 * c + 16, lo);
                 umma::wait_st();
                 umma::fence_before_sync();
-                mbar_arrive(&sh.p_full[x][c]);
+                mbar_arrive(&sh.p_full[b][c]);
             }
             const float2 acc = unf2(add2(acc0, acc1));
             l_run += acc.x + acc.y;
@@ -694,11 +751,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // `done` completes once every MMA of the CTA (the last PV included) has.
         if (ok && warp_wait_bar(&sh.done, 0, sh, p.err_flag)) {
             umma::fence_after_sync();
-            float l_other = 0.f;
-            const bool have = pair_exchange(sh, nx, x, q4, h, row, l_run, l_other, p.err_flag);
-            const float l = l_run + l_other;
             const bool zero = *reinterpret_cast<volatile int *>(&sh.bad) != 0;
-            const float inv = (l > 0.f && !zero && have) ? 1.f / l : 0.f;
+            const float inv = (l_run > 0.f && !zero) ? 1.f / l_run : 0.f;
             // A full query tile (all its rows belong to this sequence) is staged in
             // shared memory, idle now that every MMA is done (K ring for tile A,
             // V ring for tile B), and written by TMA stores; a partial tile is
@@ -706,7 +760,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const bool full_tile = ntokx == TT;
             uint8_t *stage = x == 0 ? sK : sV;
 #pragma unroll
-            for (int c = 0; c < kHalfD / 32; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 umma::ld_32x32b_x32(tO + 32 * c, o);
                 umma::wait_ld();
@@ -714,14 +768,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ov[i] = zero ? 0.f : __uint_as_float(o[i]) * inv;
                 if (full_tile)
-                    stage_chunk(stage, p.out_dtype, row, kHalfD * h + 32 * c, ov);
+                    stage_chunk(stage, p.out_dtype, row, 32 * c, ov);
                 else if (qpos >= 0)
-                    store_chunk(p.out, p.out_dtype, out_row * D + kHalfD * h + c * 32, ov);
+                    store_chunk(p.out, p.out_dtype, out_row * D + c * 32, ov);
             }
             if (full_tile) {
                 fence_proxy_async_smem();
                 mbar_arrive(&sh.staged[x]);
-                if (warp == 8 * x && lane == 0 && mbar_wait_bounded(&sh.staged[x], 0, kWaitLimitNs)) {
+                if (warp == 4 * x && lane == 0 && mbar_wait_bounded(&sh.staged[x], 0, kWaitLimitNs)) {
                     const int es = p.out_dtype == PA_F32 ? 4 : 2;
                     const int regions = D * es / 128;
                     for (int r = 0; r < regions; ++r)

@@ -10,7 +10,7 @@
 namespace pa {
 
 constexpr int kPrefillTile = 128;       // rows of a query tile = KV tokens per stage
-constexpr int kPrefillThreads = 608;    // 16 softmax warps, K/Q loader, MMA issuer, V loader
+constexpr int kPrefillThreads = 352;    // 8 softmax warps, K/Q loader, MMA issuer, V loader
 constexpr int kRankSeqs = 128;          // batches up to this many sequences run longest first
 
 struct PrefillParams {

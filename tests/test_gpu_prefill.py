@@ -6,7 +6,8 @@ on an evenly spaced sample of rows (every head of each), each computed by the
 oracle on its own, with the caches compared in full.  Edge cases: empty
 and one-token tails, tails with no cached prefix, lengths on and next to the
 128-token tile boundary, every supported group size, head_dim 64, block
-sizes 8/32/64, all output types, and a bad block id."""
+sizes 8/32/64, all output types, single-tile tails over contexts of many
+K/V tiles, and bad block ids."""
 import numpy as np
 import pytest
 
@@ -111,6 +112,51 @@ def test_prefill_gqa_edge_lengths(torch):
     out, _, err = run_prefill(torch, b)
     assert err == 0
     assert_attention_close(out, ref, "f32", "gqa edges")
+
+
+TAIL_CASES = {
+    # name: (workload, prefix lengths, tail lengths, overrides)
+    "mha_bf16": ("prefill", [128, 200, 383, 256, 700, 900, 1000, 0], [1, 128, 1, 128, 64, 17, 100, 128],
+                 dict(num_heads=4, num_kv_heads=4)),
+    "mha_f16": ("prefill", [129, 511, 384, 2000], [127, 1, 128, 3], dict(num_heads=4, num_kv_heads=4, dtype="f16")),
+    "g4": ("prefill_gqa", [500, 97, 31, 4000], [32, 5, 1, 20], dict(num_heads=16, num_kv_heads=4)),
+    "g8_bs8": ("prefill_gqa", [333, 250, 16], [16, 9, 1], dict(num_heads=64, num_kv_heads=8, block_size=8)),
+    "d64_bs64": ("prefill", [600, 129, 64], [128, 1, 100], dict(num_heads=8, num_kv_heads=8, head_dim=64,
+                                                                 dtype="f16", block_size=64)),
+}
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", sorted(TAIL_CASES))
+def test_prefill_single_tile_tails(torch, case, out_dtype):
+    """Tails that fit one query tile (the CTA's second query tile is empty),
+    over contexts of one to 32 K/V tiles: odd and even K/V tile counts,
+    contexts on and off the 128-token boundary, full tiles (TMA-store
+    epilogue for 16-bit outputs), one-row tiles, every group size class,
+    head_dim 64 and block sizes 8 / 64."""
+    name, prefix, qlen, kw = TAIL_CASES[case]
+    kw = dict(kw)
+    bs = kw.pop("block_size", None)
+    b = make(name, prefix_lens=prefix, q_lens=qlen, block_size=bs, **kw)
+    ref, _, _ = oracle.prefill_step(b)
+    out, _, err = run_prefill(torch, b, out_dtype)
+    assert err == 0
+    assert_attention_close(out, ref, out_dtype, f"tails {case}")
+
+
+def test_prefill_bad_block_late_in_context(torch):
+    """A bad block id in a late K/V tile of a one-tile tail zeroes the whole
+    query tile and sets PA_FLAG_BAD_BLOCK_ID; the other sequence is
+    unaffected."""
+    import paged_kv_cache_140_gb300 as pa
+    b = make("prefill", prefix_lens=[600, 300], q_lens=[20, 50], num_heads=4, num_kv_heads=4)
+    ref, _, _ = oracle.prefill_step(b)
+    T = to_device(b)
+    T["block_tables"][0, 25] = b.num_blocks + 3      # positions 400 .. 415: K/V tile 3 of 5
+    out, _, err = run_prefill(torch, b, dev=T)
+    assert err & pa.FLAG_BAD_BLOCK_ID
+    assert float(out[:20].abs().max()) == 0.0
+    assert_attention_close(out[20:], ref[20:], "f32", "good sequence")
 
 
 @pytest.mark.parametrize("num_seqs", [128, 130])
