@@ -159,6 +159,56 @@ def test_prefill_bad_block_late_in_context(torch):
     assert_attention_close(out[20:], ref[20:], "f32", "good sequence")
 
 
+def _ramp_keys(b, per_token):
+    """The batch with every key row at position p scaled by 1 + p * per_token
+    (the cached prefix rows and the step's new rows alike; other slots keep
+    their bits), so that each later K/V tile's scores exceed the earlier
+    ones' by far more than the lazy-rescale margin."""
+    import dataclasses
+
+    def dec(bits):
+        if b.dtype == "f16":
+            return bits.view(np.float16).astype(np.float32)
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+
+    def enc(x):
+        if b.dtype == "f16":
+            return x.astype(np.float16).view(np.uint16)
+        u = x.astype(np.float32).view(np.uint32)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+    bs = b.block_size
+    cu = b.cu_seqlens_q.astype(np.int64)
+    prefix = b.context_lens.astype(np.int64) - np.diff(cu)
+    kc = b.k_cache.copy()
+    key = b.key.copy()
+    for s in range(len(prefix)):
+        for pos in range(int(prefix[s])):
+            blk, off = b.block_tables[s, pos // bs], pos % bs
+            kc[blk, off] = enc(dec(kc[blk, off]) * (1.0 + pos * per_token))
+        for r in range(int(cu[s]), int(cu[s + 1])):
+            key[r] = enc(dec(key[r]) * (1.0 + (prefix[s] + r - cu[s]) * per_token))
+    return dataclasses.replace(b, k_cache=kc, key=key)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("name,heads", [("prefill", (4, 4)), ("prefill_gqa", (16, 4))])
+def test_prefill_rescales_at_every_tile(torch, name, heads, dtype):
+    """Keys that grow with their position push every row's running max up by
+    more than the lazy-rescale margin at each K/V tile, so the output is
+    rescaled throughout: in two-tile units (the PV before each QK), and in
+    single-tile units that double-buffer S (the rescale waits for the
+    previous PV)."""
+    prefix = [300, 700, 129, 900, 40, 0]
+    qlen = [100, 128, 250, 20, 256, 200]
+    b = _ramp_keys(make(name, prefix_lens=prefix, q_lens=qlen, num_heads=heads[0], num_kv_heads=heads[1],
+                        dtype=dtype), 1.0 / 32)
+    ref, _, _ = oracle.prefill_step(b)
+    out, _, err = run_prefill(torch, b)
+    assert err == 0
+    assert_attention_close(out, ref, "f32", f"rescaled {name} {dtype}")
+
+
 @pytest.mark.parametrize("num_seqs", [128, 130])
 def test_prefill_many_sequences(torch, num_seqs):
     """CTAs take sequences longest context first for batches of up to 128
