@@ -177,3 +177,67 @@ def test_cooperative_kernel_fp8_is_bitwise_reproducible():
     c, _, fc = run_step(b)
     assert fa == 0 and fc == 0
     assert np.array_equal(a.cpu().numpy().view(np.uint32), c.cpu().numpy().view(np.uint32))
+
+
+def _ramp_keys(b, per_token):
+    """The decode batch with every key row at position p scaled by
+    1 + p * per_token (each physical cache row once, and the step's new rows
+    at position ctx - 1), so that a row's running max keeps growing past the
+    lazy-rescale margin from stage to stage."""
+    import dataclasses
+
+    def dec(bits):
+        if b.dtype == "f16":
+            return bits.view(np.float16).astype(np.float32)
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+
+    def enc(x):
+        if b.dtype == "f16":
+            return x.astype(np.float16).view(np.uint16)
+        u = x.astype(np.float32).view(np.uint32)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+    bs = b.block_size
+    kc = b.k_cache.copy()
+    key = b.key.copy()
+    seen = set()
+    for s in range(b.num_seqs):
+        ctx = int(b.context_lens[s])
+        for pos in range(ctx - 1):
+            blk, off = int(b.block_tables[s, pos // bs]), pos % bs
+            if (blk, off) not in seen:
+                seen.add((blk, off))
+                kc[blk, off] = enc(dec(kc[blk, off]) * (1.0 + pos * per_token))
+        if ctx > 0:
+            key[s] = enc(dec(key[s]) * (1.0 + (ctx - 1) * per_token))
+    return dataclasses.replace(b, k_cache=kc, key=key)
+
+
+RAMP_CASES = [   # (batch, Hq, Hkv, dtype, head_dim, partition size)
+    ("7b", 8, 8, "f16", 128, 0),        # cooperative kernel, one query row per KV head
+    ("7b", 32, 8, "bf16", 128, 48),     # cooperative, G = 4, many partitions
+    ("7b", 8, 4, "bf16", 128, 0),       # per-warp kernel (KV heads not a multiple of 8)
+    ("7b", 8, 8, "f16", 64, 16),        # per-warp kernel, head_dim 64, a partition per stage
+    ("shared", 8, 8, "f16", 128, 0),    # runs of sequences sharing blocks, one member column each
+    ("shared", 16, 8, "bf16", 128, 48), # runs with G = 2
+]
+
+
+@pytest.mark.parametrize("name,hq,hkv,dtype,d,P", RAMP_CASES,
+                         ids=[f"{c[0]}-{c[1]}x{c[2]}-{c[3]}-d{c[4]}-P{c[5]}" for c in RAMP_CASES])
+def test_decode_rescales_as_the_max_grows(name, hq, hkv, dtype, d, P):
+    """Keys that grow with their position raise each row's running max past
+    the lazy-rescale margin every few stages, so the partial outputs are
+    rescaled throughout the context (and the merge combines partitions whose
+    maxima differ widely), on both kernels and in runs of shared blocks."""
+    from pa_harness import shared_prefix_batch
+    if name == "shared":
+        b = shared_prefix_batch(num_heads=hq, num_kv_heads=hkv, dtype=dtype, block_size=16)
+    else:
+        b = W.make_batch(name, num_seqs=6, ctx_cap=1500, num_heads=hq, num_kv_heads=hkv, dtype=dtype,
+                         head_dim=d)
+    b = _ramp_keys(b, 1.0 / 16)
+    ref, _, _ = oracle.decode_step(b)
+    out, _, flag = run_step(b, partition_size=P)
+    assert flag == 0
+    assert_attention_close(out, ref, "f32", f"ramped keys {name} {hq}/{hkv} {dtype} D {d} P {P}")
