@@ -88,3 +88,46 @@ def test_fp8_full_size_every_row():
     assert_attention_close(out, ref, b.dtype, "13b_fp8 full size")
     assert np.array_equal(cache_bits(T["k_cache"]), kc)
     assert np.array_equal(cache_bits(T["v_cache"]), vc)
+
+
+def _spike_keys(b, every=64, step=9.0):
+    """The e4m3 batch with a spike key every `every` positions: at the i-th
+    one (position every * i) each KV head's cache row points along the first
+    query of its group, with a length that puts that query's score at
+    step * i in log2 units, so a row's running max jumps past the
+    lazy-rescale margin (8) again and again."""
+    import dataclasses
+    G = b.num_heads // b.num_kv_heads
+    sl = float(b.scale) * 1.4426950408889634
+    bs = b.block_size
+    q = b.q.astype(np.uint32)
+    qf = (q << 16).view(np.float32) if b.dtype == "bf16" else b.q.view(np.float16).astype(np.float32)
+    kc = b.k_cache.copy()
+    seen = set()
+    for s in range(b.num_seqs):
+        ctx = int(b.context_lens[s])
+        for i, pos in enumerate(range(every, ctx - 1, every), start=1):
+            blk, off = int(b.block_tables[s, pos // bs]), pos % bs
+            if (blk, off) in seen:
+                continue
+            seen.add((blk, off))
+            for h in range(b.num_kv_heads):
+                qm = qf[s, h * G].astype(np.float64)
+                n2 = float(qm @ qm)
+                k = qm * (step * i / sl) / n2
+                kc[blk, off, h] = oracle.e4m3_encode((k / b.k_scale).astype(np.float32))
+    return dataclasses.replace(b, k_cache=kc)
+
+
+@pytest.mark.parametrize("hq,hkv,qdt,P", [(8, 8, "bf16", 0), (32, 8, "f16", 48), (16, 4, "bf16", 0)])
+def test_fp8_rescales_as_the_max_grows(hq, hkv, qdt, P):
+    """Spike keys whose scores climb by 9 (log2 units) every 64 positions make
+    each row's running max overtake the lazy-rescale margin throughout the
+    context, in the two-stages-per-slot e4m3 consumer (G = 1 and 4) and in
+    the per-warp kernel (4 KV heads)."""
+    b = W.make_batch("7b", num_seqs=4, ctx_cap=700, num_heads=hq, num_kv_heads=hkv, dtype=qdt,
+                     cache_dtype="fp8")
+    b = _spike_keys(b)
+    codes = oracle.e4m3_decode(b.k_cache)
+    assert np.nanmax(np.abs(codes)) < 448     # no spike saturated
+    check(b, "f32", partition_size=P)
