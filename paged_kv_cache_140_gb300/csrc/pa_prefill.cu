@@ -78,8 +78,8 @@ template <> struct Rings<64> { static constexpr int K = 4, V = 4; };
 struct Shared {
     uint64_t q_full;
     uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
-    uint64_t s_full[2];                  // per query tile
-    uint64_t p_full[2][kChunks];         // [query tile][32-key chunk of the row]
+    uint64_t s_full[2];                  // per S/P buffer (a query tile's own; alternating in a single-tile unit)
+    uint64_t p_full[2][kChunks];         // [S/P buffer][32-key chunk of the row]
     uint64_t zeroed;                     // once: stale V rows of the last K/V tile zeroed
     uint64_t done;
     uint64_t pv_done;                    // single-tile unit: each PV has completed
