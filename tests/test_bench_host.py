@@ -73,3 +73,17 @@ def test_decode_kernel_choice(monkeypatch):
     assert bench.decode_kernel_name(W.make_batch("tiny", num_heads=8, num_kv_heads=2)) == warp
     monkeypatch.setenv("PA_DECODE_COOP", "0")
     assert bench.decode_kernel_name(W.make_batch("13b", num_seqs=4)) == warp
+
+
+def test_end_to_end_entries_report_their_own_time_and_bytes():
+    """The direct-call and overlapped end-to-end entries: value = the units of
+    one step over that step's own host time, with the step's copies declared."""
+    d = bench.e2e_direct_entry(2.0, "GB/s", 0.5, 1, 8_000_000, 2_600_000)
+    assert d["value"] == 4000.0 and d["unit"] == "GB/s" and d["ms_per_step"] == 0.5
+    assert d["h2d_bytes_per_step"] == 8_000_000 and d["d2h_bytes_per_step"] == 2_600_000
+    p = bench.e2e_pipelined_entry(2.0, "GB/s", 0.25, 1, 8_000_000, 2_600_000)
+    assert p["value"] == 8000.0 and p["ms_per_step"] == 0.25
+    assert p["h2d_bytes_per_step"] == 8_000_000 and p["d2h_bytes_per_step"] == 2_600_000
+    assert "overlapping" in p["note"] and "graph" in d["note"]
+    t = bench.e2e_pipelined_entry(0.2083835, "TFLOP/s", 0.3, 1, 0, 0)
+    assert t["value"] == round(0.2083835 / 0.3e-3, 2)
