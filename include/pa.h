@@ -173,7 +173,18 @@ int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads,
  *                  a bfloat16 query is rounded to binary16 (exact for
  *                  |q| in [2^-14, 65504]).
  *   block_tables : [num_seqs, max_blocks_per_seq] int32; only the first
- *                  ceil(context_lens[s] / bs) entries of row s are read
+ *                  ceil(context_lens[s] / bs) entries of row s are read.
+ *                  Sequences may share physical blocks.  Where neighbouring
+ *                  rows start with the same block id, the blocks they share
+ *                  must form a common prefix of both rows (as copy-on-write
+ *                  sharing produces: once two rows differ, no later entry is
+ *                  shared again).  With a 16-bit cache, head_dim 128, KV heads
+ *                  a multiple of 8 and a group size of 1 or 2, such a run of
+ *                  sequences is
+ *                  served from one copy of each shared block, and the
+ *                  shared length is found by bisection on that property;
+ *                  rows that share a block again after a differing one read
+ *                  the first row's blocks in between.
  *   context_lens : [num_seqs] int32, each in [0, max_context_len]; 0 gives a
  *                  zero output row
  *   max_context_len : host-known upper bound of context_lens (sizes the
