@@ -180,9 +180,8 @@ int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads,
  *                  sharing produces: once two rows differ, no later entry is
  *                  shared again).  With a 16-bit cache, head_dim 128, KV heads
  *                  a multiple of 8 and a group size of 1 or 2, such a run of
- *                  sequences is
- *                  served from one copy of each shared block, and the
- *                  shared length is found by bisection on that property;
+ *                  sequences is served from one copy of each shared block,
+ *                  the shared length found by bisection on that property;
  *                  rows that share a block again after a differing one read
  *                  the first row's blocks in between.
  *   context_lens : [num_seqs] int32, each in [0, max_context_len]; 0 gives a
